@@ -1,0 +1,206 @@
+/*
+ * Selective-scan oracle: plain, sequential, fp64 CPU restatement of the
+ * Mamba selective state-space recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it computes, and where each step comes from:
+ *
+ *   - The discrete linear recurrence  h_t = Abar h_{t-1} + Bbar x_t,
+ *     y_t = C h_t  ("Mamba", elemedex.maurosantelli.com.ar, section
+ *     "How it works"; "State Spaces, Selectively - Mamba", papermap
+ *     interactive paper explainer, Chapter 02 "The Discretized View").
+ *   - Zero-order-hold discretisation with step size Delta: Abar = exp(Delta A)
+ *     ("Mamba remembers by forgetting, read closely", interactiveml.org,
+ *     the scalar recurrence h_t = exp(-Delta_t) h_{t-1} + ...), and the
+ *     first-order input term Bbar x = Delta B x (the plain reading adopted by
+ *     this library; the pages say only that Abar and Bbar are derived from
+ *     (Delta, A, B)).
+ *   - Selection: Delta, B and C are given per token ("How it works",
+ *     elemedex; "The Discretized View", papermap).  A is diagonal: one real
+ *     decay per (channel, state) pair.
+ *   - The state starts at zero (the interactiveml.org listing starts its
+ *     state at 0).
+ *   - Options that the pages do not spell out and that follow the usual
+ *     Mamba layer interface: Delta = softplus(delta + delta_bias) when
+ *     requested, a per-channel skip term D x_t, and an output gate
+ *     y_t *= silu(z_t) ("output gate" in "Simplifications and limits" of the
+ *     sghael.github.io Mamba page; "multiplicative gate" in the elemedex
+ *     entry).  The gate multiplies the whole output, skip term included.
+ *
+ * The recurrence is exact, so the oracle is the definition itself, written
+ * as loops in the order the pages state the steps; no blocking, fusion or
+ * reordering.  Inputs are read from the same host arrays the GPU receives
+ * (fp32 widened, bf16 decoded exactly) or from fp64 arrays.
+ *
+ * Parity status: pinned (see the oracle pin tests).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* element type codes for the array arguments */
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
+
+/* Read element i of an array of the given type, widened to double.  bf16 is
+ * the top half of an IEEE fp32, so shifting it up decodes it exactly. */
+static double load(int type, const void* p, int64_t i) {
+    if (type == OR_F64) return ((const double*)p)[i];
+    if (type == OR_F32) return (double)((const float*)p)[i];
+    uint32_t bits = (uint32_t)((const uint16_t*)p)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* softplus(v) = log(1 + e^v), written so that neither branch overflows. */
+static double softplus(double v) {
+    if (v > 0.0) return v + log1p(exp(-v));
+    return log1p(exp(v));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+    int64_t batch, dim, dstate, seqlen;
+    int io, pio; /* element types: io for u/delta/B/C/z, pio for A/D/bias */
+    const void *u, *delta, *A, *B, *C, *D, *z, *bias;
+    int softplus_on;
+    const int64_t* chan; /* flat channel ids b*dim + d, or NULL for all */
+    int64_t nchan;
+    double* y;          /* nchan x seqlen */
+    double* last_state; /* nchan x dstate, or NULL */
+    const double* h0;   /* nchan x dstate initial state, or NULL for zero */
+    int64_t next;       /* work counter, guarded by mu */
+    pthread_mutex_t mu;
+} scan_job;
+
+/* One channel (b, d): the recurrence over t = 0 .. L-1. */
+static void scan_channel(const scan_job* j, int64_t k, double* h) {
+    const int64_t L = j->seqlen, N = j->dstate;
+    const int64_t c = j->chan ? j->chan[k] : k;
+    const int64_t b = c / j->dim, d = c % j->dim;
+    const int64_t row = c * L;            /* u, delta, z: (batch, dim, L) */
+    const int64_t bc_row = b * L * N;     /* B, C: (batch, L, N) */
+    const double bias = j->bias ? load(j->pio, j->bias, d) : 0.0;
+    const double Dskip = j->D ? load(j->pio, j->D, d) : 0.0;
+    for (int64_t n = 0; n < N; n++) h[n] = j->h0 ? j->h0[k * N + n] : 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        const double v = load(j->io, j->delta, row + t) + bias;
+        const double dt = j->softplus_on ? softplus(v) : v;
+        const double x = load(j->io, j->u, row + t);
+        double yv = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            const double a = load(j->pio, j->A, d * N + n);
+            const double Bv = load(j->io, j->B, bc_row + t * N + n);
+            h[n] = exp(dt * a) * h[n] + dt * Bv * x;
+        }
+        for (int64_t n = 0; n < N; n++)
+            yv += load(j->io, j->C, bc_row + t * N + n) * h[n];
+        yv += Dskip * x;
+        if (j->z) yv *= silu(load(j->io, j->z, row + t));
+        j->y[k * L + t] = yv;
+    }
+    if (j->last_state)
+        for (int64_t n = 0; n < N; n++) j->last_state[k * N + n] = h[n];
+}
+
+static void* scan_worker(void* arg) {
+    scan_job* j = (scan_job*)arg;
+    double* h = (double*)malloc(sizeof(double) * (size_t)j->dstate);
+    if (!h) return NULL;
+    for (;;) {
+        pthread_mutex_lock(&j->mu);
+        const int64_t k = j->next++;
+        pthread_mutex_unlock(&j->mu);
+        if (k >= j->nchan) break;
+        scan_channel(j, k, h);
+    }
+    free(h);
+    return NULL;
+}
+
+/*
+ * Forward selective scan over the channels listed in `chan` (flat ids
+ * b*dim + d; NULL means every channel in order, and then nchan must equal
+ * batch*dim).  Outputs are compact: y is nchan x seqlen, last_state is
+ * nchan x dstate.  h0 (nchan x dstate, fp64) is an optional initial state;
+ * NULL means zero.  Channels are independent, so they are spread over
+ * `nthreads` POSIX threads; each channel's loop is sequential.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io, int pio,
+                    const void* u, const void* delta, const void* A, const void* B,
+                    const void* C, const void* D, const void* z, const void* delta_bias,
+                    int delta_softplus, const int64_t* chan, int64_t nchan, const double* h0,
+                    double* y, double* last_state, int nthreads) {
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || nchan < 0) return -1;
+    if (!u || !delta || !A || !B || !C || !y) return -1;
+    if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
+    if (!chan && nchan != batch * dim) return -1;
+    if (chan)
+        for (int64_t k = 0; k < nchan; k++)
+            if (chan[k] < 0 || chan[k] >= batch * dim) return -1;
+    scan_job j;
+    memset(&j, 0, sizeof j);
+    j.batch = batch; j.dim = dim; j.dstate = dstate; j.seqlen = seqlen;
+    j.io = io; j.pio = pio;
+    j.u = u; j.delta = delta; j.A = A; j.B = B; j.C = C; j.D = D; j.z = z;
+    j.bias = delta_bias; j.softplus_on = delta_softplus;
+    j.chan = chan; j.nchan = nchan; j.y = y; j.last_state = last_state; j.h0 = h0;
+    j.next = 0;
+    pthread_mutex_init(&j.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < nthreads; i++)
+        if (pthread_create(&th[started], NULL, scan_worker, &j) == 0) started++;
+    scan_worker(&j);
+    for (int i = 0; i < started; i++) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&j.mu);
+    return 0;
+}
+
+/*
+ * One token of recurrent (generation) mode: the same update with L = 1,
+ * starting from the given state, which is updated in place.  Recurrent mode
+ * costs the same for every token ("Training without stepping token by
+ * token", sghael.github.io Mamba page).
+ * Shapes: state (batch, dim, dstate) fp64; x, delta, z, y (batch, dim);
+ * B, C (batch, dstate); A (dim, dstate); D, delta_bias (dim).
+ */
+int oracle_state_step(int64_t batch, int64_t dim, int64_t dstate, int io, int pio,
+                      double* state, const void* x, const void* delta, const void* A,
+                      const void* B, const void* C, const void* D, const void* z,
+                      const void* delta_bias, int delta_softplus, double* y) {
+    if (batch <= 0 || dim <= 0 || dstate <= 0) return -1;
+    if (!state || !x || !delta || !A || !B || !C || !y) return -1;
+    if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
+    for (int64_t b = 0; b < batch; b++) {
+        for (int64_t d = 0; d < dim; d++) {
+            const int64_t c = b * dim + d;
+            const double bias = delta_bias ? load(pio, delta_bias, d) : 0.0;
+            const double v = load(io, delta, c) + bias;
+            const double dt = delta_softplus ? softplus(v) : v;
+            const double xv = load(io, x, c);
+            double* h = state + c * dstate;
+            double yv = 0.0;
+            for (int64_t n = 0; n < dstate; n++) {
+                const double a = load(pio, A, d * dstate + n);
+                h[n] = exp(dt * a) * h[n] + dt * load(io, B, b * dstate + n) * xv;
+            }
+            for (int64_t n = 0; n < dstate; n++) yv += load(io, C, b * dstate + n) * h[n];
+            yv += (D ? load(pio, D, d) : 0.0) * xv;
+            if (z) yv *= silu(load(io, z, c));
+            y[c] = yv;
+        }
+    }
+    return 0;
+}
