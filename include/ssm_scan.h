@@ -1,0 +1,177 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) selective-scan library.
+ *
+ * The operation is the selective state-space recurrence of Mamba: a
+ * diagonal linear recurrence whose step size Delta and input/output maps
+ * B, C are given per token ("Mamba", elemedex.maurosantelli.com.ar, section
+ * "How it works": h_t = Abar h_{t-1} + Bbar x_t, y_t = C h_t; "State Spaces,
+ * Selectively - Mamba", papermap explainer, Chapter 02 "The Discretized
+ * View": Delta, B, C are functions of the input, Abar and Bbar derive from
+ * (Delta, A, B)).  For every channel (b, d) and state index n, over tokens
+ * t = 0 .. L-1, starting from h = 0:
+ *
+ *     v        = delta[b,d,t] + delta_bias[d]            (bias optional)
+ *     Delta    = delta_softplus ? softplus(v) : v
+ *     h[n]     = exp(Delta * A[d,n]) * h[n] + Delta * B[b,t,n] * u[b,d,t]
+ *     y[b,d,t] = (sum_n C[b,t,n] * h[n] + D[d] * u[b,d,t]) * silu(z[b,d,t])
+ *
+ * exp(Delta A) is the zero-order-hold decay ("Mamba remembers by forgetting,
+ * read closely", interactiveml.org: the scalar update weights the old state
+ * by exp(-Delta)); Delta*B*u is the first-order input term.  softplus,
+ * delta_bias, the skip term D and the silu(z) output gate follow the usual
+ * Mamba layer ("output gate", sghael.github.io Mamba page, "Simplifications
+ * and limits"; "multiplicative gate", elemedex entry) and are optional.
+ *
+ * Layouts (row-major, contiguous, all device memory):
+ *     u, delta, z, y   (batch, dim, seqlen)   seqlen fastest
+ *     B, C             (batch, seqlen, dstate) one token's B row is contiguous
+ *     A                (dim, dstate)          fp32
+ *     D, delta_bias    (dim)                  fp32
+ *     last_state/state (batch, dim, dstate)   fp32
+ *   Single-token step: x, delta, z, y (batch, dim); B, C (batch, dstate).
+ * u, delta, z, B, C and y share the I/O element type (fp32 or bf16); the
+ * recurrence and the state are always fp32; bf16 outputs are rounded to
+ * nearest even once, at the store.
+ *
+ * Ownership and execution: the caller owns every buffer.  Every pointer is
+ * a device pointer (or a host-mapped pointer the device can read).  The
+ * library never allocates, frees or synchronises: each call validates its
+ * arguments on the host, enqueues work on the caller's stream and returns.
+ * Outputs must not alias inputs (state, the only in/out buffer, excepted).
+ * The library keeps no global state and prints nothing; calls on different
+ * streams with disjoint outputs may run concurrently.
+ *
+ * Errors: 0 on success, else a negative ssm_status.  Argument errors are
+ * detected on the host before anything is enqueued.  A launch error is
+ * reported as SSM_ERR_CUDA (the CUDA error is left for the caller's next
+ * CUDA call to see, as the runtime does).  Faults inside a kernel surface
+ * at the caller's next synchronisation, as for any CUDA kernel.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ssm_status {
+    SSM_OK = 0,
+    SSM_ERR_NULL_ARG = -1,      /* a required pointer is NULL */
+    SSM_ERR_BAD_DIMS = -2,      /* a size is out of range or overflows */
+    SSM_ERR_UNSUPPORTED_N = -3, /* dstate is not 1, 2, 4, 8 or 16 */
+    SSM_ERR_BAD_DTYPE = -4,     /* unknown I/O element type */
+    SSM_ERR_MISALIGNED = -5,    /* a pointer is not aligned to its element size */
+    SSM_ERR_CUDA = -6,          /* the CUDA runtime refused the launch */
+    SSM_ERR_WORKSPACE = -7,     /* workspace missing, too small or misaligned */
+    SSM_ERR_ALIAS = -8,         /* an output overlaps an input */
+    SSM_ERR_TIMEOUT = -9        /* a bounded on-device wait gave up */
+} ssm_status;
+
+typedef enum ssm_io_dtype { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
+
+/* Problem sizes.  seqlen is ignored by ssm_state_step. */
+typedef struct ssm_dims {
+    int64_t batch;   /* Bt >= 1 */
+    int64_t dim;     /* D >= 1: channels per batch row */
+    int64_t dstate;  /* N in {1, 2, 4, 8, 16}: state entries per channel */
+    int64_t seqlen;  /* L >= 0: tokens */
+    int32_t io;      /* ssm_io_dtype of u, delta, z, B, C, y */
+    int32_t chunk;   /* 0: library default.  Otherwise the number of tokens per
+                        L-chunk that one CTA scans before handing its carry on
+                        (a multiple of 64).  It changes only how the sequence is
+                        scheduled: results agree up to fp32 rounding order. */
+} ssm_dims;
+
+/*
+ * Forward selective scan (the definition above) over every channel.
+ *
+ *   dims           sizes; see ssm_dims
+ *   u, delta       (batch, dim, seqlen) I/O type; required (when seqlen is 0,
+ *                  u, delta, B, C, z and y hold no elements and may be NULL)
+ *   A              (dim, dstate) fp32; required.  A <= 0 is the intended use
+ *                  (decaying state); other values are computed but not tuned
+ *   B, C           (batch, seqlen, dstate) I/O type; required
+ *   D              (dim) fp32 skip weights, or NULL for no skip term
+ *   z              (batch, dim, seqlen) I/O type gate input, or NULL for no gate
+ *   delta_bias     (dim) fp32, or NULL for zero bias
+ *   delta_softplus nonzero: Delta = softplus(delta + bias); zero: Delta = delta + bias
+ *   y              (batch, dim, seqlen) I/O type output; required
+ *   last_state     (batch, dim, dstate) fp32 final state h after token L-1, or
+ *                  NULL to skip writing it
+ *   workspace      device scratch of at least ssm_scan_fwd_workspace_size()
+ *                  bytes, 256-byte aligned; may be NULL when that size is 0.
+ *                  Its contents on entry do not matter; the call owns it until
+ *                  the enqueued work finishes.
+ *   stream         cudaStream_t to enqueue on (NULL: the legacy default stream)
+ *
+ * Pointers of the I/O type must be aligned to the element size; the library
+ * picks 16-byte vector and bulk-copy paths by itself when every row allows it.
+ * Returns SSM_OK or a negative ssm_status.
+ */
+SSM_API int ssm_scan_fwd(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 void* y, float* last_state,
+                 void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Bytes of device workspace ssm_scan_fwd needs for these sizes (may be 0).
+ * Returns SSM_OK or a negative ssm_status (bad dims). */
+SSM_API int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes);
+
+/*
+ * One token of recurrent (generation) mode: the same update with L = 1,
+ * starting from `state` and writing the new state back in place.
+ * Recurrent mode costs the same for every token and keeps no cache that
+ * grows ("Mamba", sghael.github.io, "Training without stepping token by
+ * token"; papermap explainer, "The hardware-aware scan": inference is a pure
+ * recurrence, O(1) per token).
+ *
+ *   state          (batch, dim, dstate) fp32, read and overwritten; required
+ *   x, delta, z, y (batch, dim) I/O type (z may be NULL)
+ *   B, C           (batch, dstate) I/O type
+ *   A, D, delta_bias, delta_softplus: as for ssm_scan_fwd
+ *
+ * Running ssm_state_step for tokens 0..k-1 from a zero state reproduces the
+ * scan's outputs y[..., t] and, after token k-1, the scan's last_state for
+ * the first k tokens (up to fp32 rounding order).
+ */
+SSM_API int ssm_state_step(const ssm_dims* dims, float* state,
+                   const void* x, const void* delta, const float* A,
+                   const void* B, const void* C, const float* D, const void* z,
+                   const float* delta_bias, int delta_softplus,
+                   void* y, void* stream);
+
+/*
+ * Diagnostic, not part of the scan: enqueue a throughput probe of the
+ * special-function unit's 2^x.  It launches `blocks` x `threads` threads
+ * that each evaluate iters * 8 dependent 2^x chains and writes nothing
+ * (`sink`, a device buffer of at least `threads` floats, is only named so the
+ * work cannot be optimised away).  The caller times the launch on `stream`;
+ * the number of 2^x evaluations is blocks * threads * iters * 8.
+ * threads must be a multiple of 32 in [32, 1024]; blocks and iters >= 1.
+ */
+SSM_API int ssm_probe_ex2(int32_t blocks, int32_t threads, int32_t iters, float* sink,
+                          void* stream);
+
+/* Static text for a status code (never NULL). */
+SSM_API const char* ssm_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,181 @@
+"""B300-native selective scan (Mamba's selective state-space recurrence).
+
+Python face of ``libssm_scan.so``: the functions here check and marshal
+torch tensors into raw pointers and call the C ABI of include/ssm_scan.h
+with the same names.  Every step of the scan runs in the library's CUDA
+kernels; PyTorch only supplies device memory and the current stream.
+
+Host (CPU) tensors are accepted as well: they are copied to the current CUDA
+device on the current stream, the scan runs there, and the outputs are
+copied back into host tensors (pinned when the inputs were pinned).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import SSMError, ssm_dims
+
+__all__ = ["ssm_scan_fwd", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
+           "library_path", "version"]
+
+_IO = {torch.float32: _lib.SSM_IO_F32, torch.bfloat16: _lib.SSM_IO_BF16}
+
+
+def library_path() -> str:
+    return _lib.LIBRARY
+
+
+def version() -> int:
+    return _lib.load().ssm_version()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(t, name, shape, dtype, device, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _to_device(tensors: dict, device):
+    return {k: (None if v is None else v.to(device, non_blocking=True)) for k, v in tensors.items()}
+
+
+def _host_like(t, pinned):
+    return torch.empty(t.shape, dtype=t.dtype, pin_memory=pinned)
+
+
+def _dims(batch, dim, dstate, seqlen, io, chunk=0):
+    return ssm_dims(int(batch), int(dim), int(dstate), int(seqlen), int(io), int(chunk))
+
+
+def ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen, dtype=torch.bfloat16, chunk=0) -> int:
+    """Bytes of device workspace one scan of these sizes needs."""
+    out = ctypes.c_size_t(0)
+    d = _dims(batch, dim, dstate, seqlen, _IO[dtype], chunk)
+    rc = _lib.load().ssm_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(out))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_fwd_workspace_size")
+    return int(out.value)
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                 return_last_state=True, y=None, last_state=None, workspace=None, chunk=0):
+    """Forward selective scan.
+
+    u, delta, z: (batch, dim, L); B, C: (batch, L, N), all fp32 or all bf16.
+    A: (dim, N) fp32; D, delta_bias: (dim,) fp32 or None.
+    Returns (y, last_state); last_state is None unless return_last_state.
+    ``y``/``last_state``/``workspace`` may be passed preallocated.
+    """
+    if u.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        pinned = u.is_pinned()
+        g = _to_device(dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=delta_bias), dev)
+        yd, hd = ssm_scan_fwd(**g, delta_softplus=delta_softplus,
+                              return_last_state=return_last_state, chunk=chunk)
+        y_h = _host_like(yd, pinned) if y is None else y
+        y_h.copy_(yd, non_blocking=pinned)
+        h_h = None
+        if hd is not None:
+            h_h = _host_like(hd, pinned) if last_state is None else last_state
+            h_h.copy_(hd, non_blocking=pinned)
+        if pinned:
+            torch.cuda.current_stream(dev).synchronize()
+        return y_h, h_h
+
+    device = u.device
+    if device.type != "cuda":
+        raise ValueError("ssm_scan_fwd needs CUDA (or host) tensors")
+    if u.dim() != 3 or A.dim() != 2:
+        raise ValueError("u must be (batch, dim, L) and A (dim, N)")
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    if io not in _IO:
+        raise TypeError(f"unsupported I/O dtype {io}; use float32 or bfloat16")
+    _check(u, "u", (batch, dim, L), io, device)
+    _check(delta, "delta", (batch, dim, L), io, device)
+    _check(A, "A", (dim, N), torch.float32, device)
+    _check(B, "B", (batch, L, N), io, device)
+    _check(C, "C", (batch, L, N), io, device)
+    _check(D, "D", (dim,), torch.float32, device, optional=True)
+    _check(z, "z", (batch, dim, L), io, device, optional=True)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, device, optional=True)
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=io, device=device)
+    _check(y, "y", (batch, dim, L), io, device)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((batch, dim, N), dtype=torch.float32, device=device)
+    if last_state is not None:
+        _check(last_state, "last_state", (batch, dim, N), torch.float32, device)
+    d = _dims(batch, dim, N, L, _IO[io], chunk)
+    lib = _lib.load()
+    need = ctypes.c_size_t(0)
+    rc = lib.ssm_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(need))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_fwd_workspace_size")
+    if need.value and workspace is None:
+        workspace = torch.empty(int(need.value), dtype=torch.uint8, device=device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.ssm_scan_fwd(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                          _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                          _ptr(y), _ptr(last_state), _ptr(workspace), ws_bytes,
+                          _stream(device))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_fwd")
+    return y, (last_state if return_last_state else None)
+
+
+def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                   delta_softplus=False, y=None):
+    """One generation step: updates ``state`` (batch, dim, N) fp32 in place
+    and returns y (batch, dim).  x, delta, z: (batch, dim); B, C: (batch, N)."""
+    device = state.device
+    if device.type != "cuda":
+        raise ValueError("ssm_state_step needs CUDA tensors")
+    if state.dim() != 3:
+        raise ValueError("state must be (batch, dim, N)")
+    batch, dim, N = state.shape
+    io = x.dtype
+    if io not in _IO:
+        raise TypeError(f"unsupported I/O dtype {io}; use float32 or bfloat16")
+    _check(state, "state", (batch, dim, N), torch.float32, device)
+    _check(x, "x", (batch, dim), io, device)
+    _check(delta, "delta", (batch, dim), io, device)
+    _check(A, "A", (dim, N), torch.float32, device)
+    _check(B, "B", (batch, N), io, device)
+    _check(C, "C", (batch, N), io, device)
+    _check(D, "D", (dim,), torch.float32, device, optional=True)
+    _check(z, "z", (batch, dim), io, device, optional=True)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, device, optional=True)
+    if y is None:
+        y = torch.empty((batch, dim), dtype=io, device=device)
+    _check(y, "y", (batch, dim), io, device)
+    d = _dims(batch, dim, N, 1, _IO[io])
+    rc = _lib.load().ssm_state_step(ctypes.byref(d), _ptr(state), _ptr(x), _ptr(delta), _ptr(A),
+                                    _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                                    int(bool(delta_softplus)), _ptr(y), _stream(device))
+    if rc != 0:
+        raise SSMError(rc, "ssm_state_step")
+    return y

@@ -1,0 +1,78 @@
+"""ctypes view of libssm_scan.so (declared in include/ssm_scan.h).
+
+Loading fails loudly when the library has not been built; there is no
+fallback implementation anywhere in this package.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libssm_scan.so")
+
+# ssm_status codes (include/ssm_scan.h)
+SSM_OK = 0
+SSM_ERR_NULL_ARG = -1
+SSM_ERR_BAD_DIMS = -2
+SSM_ERR_UNSUPPORTED_N = -3
+SSM_ERR_BAD_DTYPE = -4
+SSM_ERR_MISALIGNED = -5
+SSM_ERR_CUDA = -6
+SSM_ERR_WORKSPACE = -7
+SSM_ERR_ALIAS = -8
+SSM_ERR_TIMEOUT = -9
+
+SSM_IO_F32 = 0
+SSM_IO_BF16 = 1
+
+# every symbol include/ssm_scan.h declares
+EXPORTS = ("ssm_probe_ex2", "ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_state_step",
+           "ssm_status_string", "ssm_version")
+
+
+class ssm_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("io", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load(path: str = LIBRARY) -> ctypes.CDLL:
+    """Load the library once.  Raises if it is missing: build it first."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library {path} is missing; build it with "
+            "`python -m selective_state_space_116_b300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    dims_p = ctypes.POINTER(ssm_dims)
+    lib.ssm_scan_fwd.restype = i32
+    lib.ssm_scan_fwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.ssm_scan_fwd_workspace_size.restype = i32
+    lib.ssm_scan_fwd_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
+    lib.ssm_state_step.restype = i32
+    lib.ssm_state_step.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+    lib.ssm_probe_ex2.restype = i32
+    lib.ssm_probe_ex2.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [i32]
+    lib.ssm_version.restype = i32
+    lib.ssm_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().ssm_status_string(int(status)).decode()

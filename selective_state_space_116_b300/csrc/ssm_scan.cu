@@ -1,0 +1,261 @@
+// C ABI of the selective-scan library: argument checks on the host, then a
+// launch of the kernel instance that matches (I/O type, N, gate, softplus,
+// alignment) on the caller's stream.  See include/ssm_scan.h for the contract.
+#include "ssm_scan.h"
+
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "probe.cuh"
+#include "scan_fwd.cuh"
+#include "state_step.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool valid_n(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16; }
+
+size_t io_size(int io) { return io == SSM_IO_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a * b with overflow check against INT64_MAX
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+struct Range {
+    const void* p;
+    int64_t bytes;
+};
+
+bool overlap(Range a, Range b) {
+    if (!a.p || !b.p || a.bytes <= 0 || b.bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + (uintptr_t)b.bytes && b0 < a0 + (uintptr_t)a.bytes;
+}
+
+// Sizes of the problem in elements, with overflow checks.
+struct Sizes {
+    int64_t chan;    // batch * dim
+    int64_t seq;     // batch * dim * L        (u, delta, z, y)
+    int64_t bc;      // batch * L * N          (B, C)
+    int64_t state;   // batch * dim * N
+    int64_t par;     // dim * N                (A)
+};
+
+int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
+    if (!dims) return SSM_ERR_NULL_ARG;
+    if (dims->io != SSM_IO_F32 && dims->io != SSM_IO_BF16) return SSM_ERR_BAD_DTYPE;
+    if (dims->batch < 1 || dims->dim < 1 || dims->dstate < 1) return SSM_ERR_BAD_DIMS;
+    if (scan && dims->seqlen < 0) return SSM_ERR_BAD_DIMS;
+    if (!valid_n(dims->dstate)) return SSM_ERR_UNSUPPORTED_N;
+    if (scan && dims->chunk != 0 && (dims->chunk < 0 || dims->chunk % 64 != 0))
+        return SSM_ERR_BAD_DIMS;
+    if (scan && dims->batch > 65535) return SSM_ERR_BAD_DIMS;  // grid.y limit of the scan launch
+    const int64_t L = scan ? dims->seqlen : 1;
+    int64_t bytes;
+    if (!mul_ok(dims->batch, dims->dim, &s->chan) || !mul_ok(s->chan, L, &s->seq) ||
+        !mul_ok(dims->batch * 1, L, &s->bc) || !mul_ok(s->bc, dims->dstate, &s->bc) ||
+        !mul_ok(s->chan, dims->dstate, &s->state) || !mul_ok(dims->dim, dims->dstate, &s->par) ||
+        !mul_ok(s->seq, 4, &bytes) || !mul_ok(s->bc, 4, &bytes) || !mul_ok(s->state, 4, &bytes))
+        return SSM_ERR_BAD_DIMS;
+    return SSM_OK;
+}
+
+template <typename T, int N, bool Z, bool SP, bool VEC>
+int launch_scan(const ssm::ScanParams& p, cudaStream_t stream) {
+    using namespace ssm::v1;
+    auto kern = scan_fwd_kernel<T, N, Z, SP, VEC>;
+    const size_t smem = smem_bytes<T, N>(Z);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return SSM_ERR_CUDA;
+    const dim3 grid((unsigned)((p.dim + kChannels - 1) / kChannels), (unsigned)p.batch);
+    kern<<<grid, kChannels, smem, stream>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int N>
+int dispatch_scan_n(const ssm::ScanParams& p, bool z, bool sp, bool vec, cudaStream_t s) {
+#define SSM_SCAN_CASE(Z, SP, V) \
+    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, Z, SP, V>(p, s);
+    SSM_SCAN_CASE(false, false, false)
+    SSM_SCAN_CASE(false, false, true)
+    SSM_SCAN_CASE(false, true, false)
+    SSM_SCAN_CASE(false, true, true)
+    SSM_SCAN_CASE(true, false, false)
+    SSM_SCAN_CASE(true, false, true)
+    SSM_SCAN_CASE(true, true, false)
+    SSM_SCAN_CASE(true, true, true)
+#undef SSM_SCAN_CASE
+    return SSM_ERR_BAD_DIMS;
+}
+
+template <typename T>
+int dispatch_scan(const ssm::ScanParams& p, int64_t n, bool z, bool sp, bool vec, cudaStream_t s) {
+    switch (n) {
+        case 1: return dispatch_scan_n<T, 1>(p, z, sp, vec, s);
+        case 2: return dispatch_scan_n<T, 2>(p, z, sp, vec, s);
+        case 4: return dispatch_scan_n<T, 4>(p, z, sp, vec, s);
+        case 8: return dispatch_scan_n<T, 8>(p, z, sp, vec, s);
+        case 16: return dispatch_scan_n<T, 16>(p, z, sp, vec, s);
+    }
+    return SSM_ERR_UNSUPPORTED_N;
+}
+
+template <typename T, int N, bool Z, bool SP, bool VEC>
+int launch_step(const ssm::StepParams& p, cudaStream_t stream) {
+    constexpr int kG = ssm::StepShape<N>::kG;
+    const int64_t threads = p.batch * p.dim * kG;
+    const int64_t blocks = (threads + ssm::kStepThreads - 1) / ssm::kStepThreads;
+    if (blocks > INT32_MAX) return SSM_ERR_BAD_DIMS;
+    ssm::state_step_kernel<T, N, Z, SP, VEC><<<(unsigned)blocks, ssm::kStepThreads, 0, stream>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int N>
+int dispatch_step_n(const ssm::StepParams& p, bool z, bool sp, bool vec, cudaStream_t s) {
+#define SSM_STEP_CASE(Z, SP, V) \
+    if (z == Z && sp == SP && vec == V) return launch_step<T, N, Z, SP, V>(p, s);
+    SSM_STEP_CASE(false, false, false)
+    SSM_STEP_CASE(false, false, true)
+    SSM_STEP_CASE(false, true, false)
+    SSM_STEP_CASE(false, true, true)
+    SSM_STEP_CASE(true, false, false)
+    SSM_STEP_CASE(true, false, true)
+    SSM_STEP_CASE(true, true, false)
+    SSM_STEP_CASE(true, true, true)
+#undef SSM_STEP_CASE
+    return SSM_ERR_BAD_DIMS;
+}
+
+template <typename T>
+int dispatch_step(const ssm::StepParams& p, int64_t n, bool z, bool sp, bool vec, cudaStream_t s) {
+    switch (n) {
+        case 1: return dispatch_step_n<T, 1>(p, z, sp, vec, s);
+        case 2: return dispatch_step_n<T, 2>(p, z, sp, vec, s);
+        case 4: return dispatch_step_n<T, 4>(p, z, sp, vec, s);
+        case 8: return dispatch_step_n<T, 8>(p, z, sp, vec, s);
+        case 16: return dispatch_step_n<T, 16>(p, z, sp, vec, s);
+    }
+    return SSM_ERR_UNSUPPORTED_N;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_version(void) { return kVersion; }
+
+const char* ssm_status_string(int status) {
+    switch (status) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_NULL_ARG: return "a required pointer is NULL";
+        case SSM_ERR_BAD_DIMS: return "a size is out of range or overflows";
+        case SSM_ERR_UNSUPPORTED_N: return "dstate must be 1, 2, 4, 8 or 16";
+        case SSM_ERR_BAD_DTYPE: return "unknown I/O element type";
+        case SSM_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
+        case SSM_ERR_CUDA: return "the CUDA runtime refused the launch";
+        case SSM_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
+        case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
+    }
+    return "unknown status";
+}
+
+int ssm_probe_ex2(int32_t blocks, int32_t threads, int32_t iters, float* sink, void* stream) {
+    if (!sink) return SSM_ERR_NULL_ARG;
+    if (blocks < 1 || iters < 1 || threads < 32 || threads > 1024 || threads % 32 != 0)
+        return SSM_ERR_BAD_DIMS;
+    ssm::probe_ex2_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, sink);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
+    Sizes s;
+    const int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    if (!bytes) return SSM_ERR_NULL_ARG;
+    *bytes = 0;
+    return SSM_OK;
+}
+
+int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus, void* y, float* last_state,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    Sizes s;
+    int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    // With L = 0 the (batch, dim, L) and (batch, L, N) tensors are empty and
+    // may be NULL; only last_state is written (zeros).
+    const bool empty = dims->seqlen == 0;
+    if (!A || (!empty && (!u || !delta || !B || !C || !y))) return SSM_ERR_NULL_ARG;
+    const size_t es = io_size(dims->io);
+    for (const void* q : {u, delta, B, C, z, static_cast<const void*>(y)})
+        if (q && !aligned(q, es)) return SSM_ERR_MISALIGNED;
+    for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
+                          static_cast<const void*>(delta_bias),
+                          static_cast<const void*>(last_state)})
+        if (q && !aligned(q, 4)) return SSM_ERR_MISALIGNED;
+    const Range in[] = {{u, s.seq * (int64_t)es}, {delta, s.seq * (int64_t)es},
+                        {z, s.seq * (int64_t)es}, {B, s.bc * (int64_t)es},
+                        {C, s.bc * (int64_t)es},  {A, s.par * 4},
+                        {D, dims->dim * 4},       {delta_bias, dims->dim * 4}};
+    const Range out_y{y, s.seq * (int64_t)es}, out_h{last_state, s.state * 4};
+    for (const Range& r : in)
+        if (overlap(r, out_y) || overlap(r, out_h)) return SSM_ERR_ALIAS;
+    if (overlap(out_y, out_h)) return SSM_ERR_ALIAS;
+
+    ssm::ScanParams p{u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                      dims->batch, dims->dim, dims->seqlen};
+    // 16-byte vector path: every row of u/delta/z/y starts on a 16-byte boundary
+    const bool vec = (dims->seqlen * (int64_t)es) % 16 == 0 && aligned(u, 16) &&
+                     aligned(delta, 16) && aligned(y, 16) && (!z || aligned(z, 16));
+    const bool sp = delta_softplus != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->io == SSM_IO_BF16) return dispatch_scan<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
+    return dispatch_scan<float>(p, dims->dstate, z != nullptr, sp, vec, st);
+}
+
+int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void* delta,
+                   const float* A, const void* B, const void* C, const float* D, const void* z,
+                   const float* delta_bias, int delta_softplus, void* y, void* stream) {
+    Sizes s;
+    int rc = check_dims(dims, false, &s);
+    if (rc != SSM_OK) return rc;
+    if (!state || !x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL_ARG;
+    const size_t es = io_size(dims->io);
+    for (const void* q : {x, delta, B, C, z, static_cast<const void*>(y)})
+        if (q && !aligned(q, es)) return SSM_ERR_MISALIGNED;
+    for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
+                          static_cast<const void*>(delta_bias), static_cast<const void*>(state)})
+        if (q && !aligned(q, 4)) return SSM_ERR_MISALIGNED;
+    const Range in[] = {{x, s.chan * (int64_t)es}, {delta, s.chan * (int64_t)es},
+                        {z, s.chan * (int64_t)es}, {B, dims->batch * dims->dstate * (int64_t)es},
+                        {C, dims->batch * dims->dstate * (int64_t)es}, {A, s.par * 4},
+                        {D, dims->dim * 4}, {delta_bias, dims->dim * 4}};
+    const Range out_y{y, s.chan * (int64_t)es}, io_h{state, s.state * 4};
+    for (const Range& r : in)
+        if (overlap(r, out_y) || overlap(r, io_h)) return SSM_ERR_ALIAS;
+    if (overlap(out_y, io_h)) return SSM_ERR_ALIAS;
+
+    ssm::StepParams p{state, x, delta, A, B, C, D, z, delta_bias, y, dims->batch, dims->dim};
+    const bool vec = aligned(state, 16);
+    const bool sp = delta_softplus != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->io == SSM_IO_BF16) return dispatch_step<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
+    return dispatch_step<float>(p, dims->dstate, z != nullptr, sp, vec, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/*.h declares, and rejects bad arguments on the host.
+
+Every call here fails argument validation before anything is enqueued, so the
+placeholder pointer values below are never dereferenced by host or device.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from selective_state_space_116_b300 import _lib
+from selective_state_space_116_b300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"SSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = declared_functions()
+    assert declared, "no SSM_API declarations found"
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert sorted(_lib.EXPORTS) == declared
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssm_version() >= 100
+    for code in range(0, -10, -1):
+        s = _lib.status_string(code)
+        assert s and s != "unknown status", code
+    assert _lib.status_string(-99) == "unknown status"
+
+
+# placeholder addresses: aligned, far apart, never dereferenced
+P = [0x10000000 * (i + 1) for i in range(16)]
+
+
+def dims(batch=2, dim=8, dstate=16, seqlen=64, io=_lib.SSM_IO_BF16, chunk=0):
+    return _lib.ssm_dims(batch, dim, dstate, seqlen, io, chunk)
+
+
+def scan(lib, d, u=P[0], delta=P[1], A=P[2], B=P[3], C=P[4], D=P[5], z=P[6], bias=P[7],
+         y=P[8], last=P[9], ws=None, ws_bytes=0):
+    return lib.ssm_scan_fwd(ctypes.byref(d) if d is not None else None, u, delta, A, B, C, D, z,
+                            bias, 1, y, last, ws, ws_bytes, None)
+
+
+def step(lib, d, state=P[0], x=P[1], delta=P[2], A=P[3], B=P[4], C=P[5], D=P[6], z=P[7],
+         bias=P[8], y=P[9]):
+    return lib.ssm_state_step(ctypes.byref(d) if d is not None else None, state, x, delta, A,
+                              B, C, D, z, bias, 1, y, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), _lib.SSM_ERR_BAD_DIMS),
+    (dict(dim=0), _lib.SSM_ERR_BAD_DIMS),
+    (dict(seqlen=-1), _lib.SSM_ERR_BAD_DIMS),
+    (dict(dstate=3), _lib.SSM_ERR_UNSUPPORTED_N),
+    (dict(dstate=32), _lib.SSM_ERR_UNSUPPORTED_N),
+    (dict(dstate=0), _lib.SSM_ERR_BAD_DIMS),
+    (dict(io=7), _lib.SSM_ERR_BAD_DTYPE),
+    (dict(chunk=100), _lib.SSM_ERR_BAD_DIMS),
+    (dict(chunk=-64), _lib.SSM_ERR_BAD_DIMS),
+    (dict(batch=1 << 40, dim=1 << 40), _lib.SSM_ERR_BAD_DIMS),
+    (dict(batch=70000), _lib.SSM_ERR_BAD_DIMS),
+])
+def test_scan_rejects_bad_dims(lib, kw, code):
+    assert scan(lib, dims(**kw)) == code
+    out = ctypes.c_size_t(123)
+    if code != _lib.SSM_OK:
+        assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(dims(**kw)), ctypes.byref(out)) == code
+
+
+def test_scan_null_arguments(lib):
+    assert scan(lib, None) == _lib.SSM_ERR_NULL_ARG
+    for name in ("u", "delta", "A", "B", "C", "y"):
+        assert scan(lib, dims(), **{name: None}) == _lib.SSM_ERR_NULL_ARG, name
+    assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(dims()), None) == _lib.SSM_ERR_NULL_ARG
+
+
+def test_scan_misaligned(lib):
+    assert scan(lib, dims(io=_lib.SSM_IO_BF16), u=P[0] + 1) == _lib.SSM_ERR_MISALIGNED
+    assert scan(lib, dims(io=_lib.SSM_IO_F32), y=P[8] + 2) == _lib.SSM_ERR_MISALIGNED
+    assert scan(lib, dims(), A=P[2] + 2) == _lib.SSM_ERR_MISALIGNED
+    assert scan(lib, dims(), last=P[9] + 1) == _lib.SSM_ERR_MISALIGNED
+
+
+def test_scan_aliasing(lib):
+    d = dims(batch=2, dim=8, dstate=16, seqlen=64)
+    assert scan(lib, d, y=P[0]) == _lib.SSM_ERR_ALIAS            # y == u
+    assert scan(lib, d, y=P[0] + 64) == _lib.SSM_ERR_ALIAS       # y inside u
+    assert scan(lib, d, last=P[3] + 16) == _lib.SSM_ERR_ALIAS    # last_state inside B
+    assert scan(lib, d, last=P[8]) == _lib.SSM_ERR_ALIAS         # last_state == y
+
+
+def test_step_errors(lib):
+    assert step(lib, None) == _lib.SSM_ERR_NULL_ARG
+    assert step(lib, dims(dstate=5)) == _lib.SSM_ERR_UNSUPPORTED_N
+    assert step(lib, dims(io=9)) == _lib.SSM_ERR_BAD_DTYPE
+    for name in ("state", "x", "delta", "A", "B", "C", "y"):
+        assert step(lib, dims(), **{name: None}) == _lib.SSM_ERR_NULL_ARG, name
+    assert step(lib, dims(), x=P[1] + 1) == _lib.SSM_ERR_MISALIGNED
+    assert step(lib, dims(), state=P[0] + 2) == _lib.SSM_ERR_MISALIGNED
+    assert step(lib, dims(), y=P[0]) == _lib.SSM_ERR_ALIAS       # y == state
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    missing = os.path.join(tmp_path, "nope.so")
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            _lib.load(missing)
+    finally:
+        _lib._lib = saved

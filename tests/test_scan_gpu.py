@@ -1,0 +1,164 @@
+"""Forward-scan parity: the CUDA library (through its C ABI) against the fp64
+oracle on the same seeded inputs.  Tolerances are stated in parity.py:
+1e-4*(1+|ref|) for fp32 I/O, 2e-2*(1+|ref|) for bf16 I/O, on y and last_state."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle_pins
+from parity import TOL, as64, assert_close, gpu_scan, oracle_scan, sample_channels
+from selective_state_space_116_b300.workloads import WORKLOADS, Workload, make_scan_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def check_full(w: Workload, seed=0, chunk=0):
+    inp = make_scan_inputs(w, seed)
+    y, h = gpu_scan(inp, chunk=chunk)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, w.torch_io, f"{w.name} y")
+    assert_close(as64(h), h_ref, w.torch_io, f"{w.name} last_state")
+    return inp, y, h
+
+
+def test_tiny_workload():
+    check_full(WORKLOADS["tiny"])
+
+
+# small shapes that span several channel blocks and token tiles plus ragged tails
+BASE = Workload("opt", 2, 67, 16, 131, "bf16", bias_range=(-4.0, -2.0), a_kind="neg_index",
+                gate=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+def test_state_sizes(io, N):
+    check_full(BASE.scaled(io=io, dstate=N, a_kind="neg_exp_uniform"), seed=N)
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("softplus", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+@pytest.mark.parametrize("skip", [False, True])
+def test_options(gate, softplus, bias, skip):
+    w = BASE.scaled(io="f32", gate=gate, softplus=softplus, skip=skip,
+                    bias_range=(-4.0, -2.0) if bias else None,
+                    delta_mean=0.0 if softplus else 0.0)
+    inp = make_scan_inputs(w, seed=11)
+    if not softplus:  # a positive step size without softplus
+        inp["delta"] = inp["delta"].abs() * 0.1
+        if inp["delta_bias"] is not None:
+            inp["delta_bias"] = inp["delta_bias"].abs() * 0.01
+    y, h = gpu_scan(inp)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.float32, "y")
+    assert_close(as64(h), h_ref, torch.float32, "last_state")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 7, 63, 64, 65, 256, 1000])
+@pytest.mark.parametrize("dim", [1, 3, 64, 130])
+def test_ragged_shapes(io, L, dim):
+    check_full(BASE.scaled(io=io, dim=dim, seqlen=L, batch=1 if dim > 64 else 3), seed=L + dim)
+
+
+def test_empty_sequence():
+    w = BASE.scaled(seqlen=0)
+    inp = make_scan_inputs(w)
+    y, h = gpu_scan(inp)
+    assert y.shape == (2, 67, 0)
+    assert torch.count_nonzero(h).item() == 0
+
+
+def test_without_last_state():
+    w = BASE.scaled(io="bf16")
+    inp = make_scan_inputs(w, seed=5)
+    y, h = gpu_scan(inp, return_last_state=False)
+    assert h is None
+    y_ref, _ = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.bfloat16, "y")
+
+
+# -- the pages' worked examples, run through the CUDA kernel --------------------
+def _scalar_inputs(deltas, us, h_A=-1.0):
+    L = len(deltas)
+    f = lambda a: torch.tensor(np.asarray(a, np.float32))
+    return {
+        "u": f(us).reshape(1, 1, L), "delta": f(deltas).reshape(1, 1, L),
+        "A": torch.tensor([[h_A]], dtype=torch.float32),
+        "B": torch.ones(1, L, 1), "C": torch.ones(1, L, 1), "D": None, "z": None,
+        "delta_bias": None, "delta_softplus": False,
+    }
+
+
+def test_gate_example_on_gpu():
+    gold = oracle_pins.read_golden("gate_memory.txt")
+    xs = gold["inputs"]
+    d, u = oracle_pins.gate_inputs([gold["fixed_gate"][0]] * len(xs), xs)
+    y, _ = gpu_scan(_scalar_inputs(d, u))
+    assert_close(as64(y).reshape(-1)[:4], gold["fixed_states_first4"], torch.float32, "fixed")
+    d, u = oracle_pins.gate_inputs(gold["selective_gates"], xs)
+    y, _ = gpu_scan(_scalar_inputs(d, u))
+    assert_close(as64(y).reshape(-1), gold["selective_states"], torch.float32, "selective")
+
+
+def test_affine_compose_on_gpu():
+    gold = oracle_pins.read_golden("affine_compose.txt")
+    (a1, b1), (_, b2) = gold["first"], gold["second"]
+    dt = -math.log(a1)
+    y, h = gpu_scan(_scalar_inputs([dt, dt], [b1 / dt, b2 / dt]))
+    assert_close(as64(h).reshape(-1), [gold["composed"][1]], torch.float32, "composed b")
+
+
+def test_closed_form_on_gpu():
+    L, d = 5000, 0.01
+    y, h = gpu_scan(_scalar_inputs(np.full(L, d), np.ones(L)))
+    t = np.arange(L)
+    want = d * (-np.expm1((t + 1) * -d)) / (-math.expm1(-d))
+    assert_close(as64(y).reshape(-1), want, torch.float32, "closed form")
+
+
+# -- properties of the kernel -------------------------------------------------
+def test_causality_bitwise():
+    w = BASE.scaled(io="bf16", seqlen=300)
+    inp = make_scan_inputs(w, seed=21)
+    y0, _ = gpu_scan(inp)
+    t0 = 170
+    pert = dict(inp)
+    for k in ("u", "delta", "z"):
+        t = inp[k].clone()
+        t[..., t0:] = t[..., t0:] * -3.0 + 1.0
+        pert[k] = t
+    B = inp["B"].clone()
+    B[:, t0:] += 1.0
+    pert["B"] = B
+    y1, _ = gpu_scan(pert)
+    assert torch.equal(y0[..., :t0], y1[..., :t0]), "outputs before t0 must not change"
+    assert not torch.equal(y0[..., t0:], y1[..., t0:])
+
+
+def test_deterministic():
+    inp = make_scan_inputs(BASE.scaled(io="bf16", seqlen=500), seed=4)
+    y0, h0 = gpu_scan(inp)
+    y1, h1 = gpu_scan(inp)
+    assert torch.equal(y0, y1) and torch.equal(h0, h1)
+
+
+# -- the full-size workloads --------------------------------------------------
+@pytest.mark.parametrize("name", ["m130", "m2p8"])
+def test_layer_workloads_full(name):
+    check_full(WORKLOADS[name])
+
+
+def test_dna_workload_sampled_channels():
+    w = WORKLOADS["dna"]
+    inp = make_scan_inputs(w)
+    y, h = gpu_scan(inp)
+    chans = sample_channels(w.batch, w.dim, 32)
+    y_ref, h_ref = oracle_scan(inp, channels=chans)
+    yv = as64(y.reshape(-1, w.seqlen)[torch.from_numpy(chans).cuda()])
+    hv = as64(h.reshape(-1, w.dstate)[torch.from_numpy(chans).cuda()])
+    assert_close(yv, y_ref, torch.float32, "dna y")
+    assert_close(hv, h_ref, torch.float32, "dna last_state")
