@@ -85,10 +85,13 @@ typedef struct ssm_dims {
     int64_t dstate;  /* N in {1, 2, 4, 8, 16}: state entries per channel */
     int64_t seqlen;  /* L >= 0: tokens */
     int32_t io;      /* ssm_io_dtype of u, delta, z, B, C, y */
-    int32_t chunk;   /* 0: library default.  Otherwise the number of tokens per
-                        L-chunk that one CTA scans before handing its carry on
-                        (a multiple of 64).  It changes only how the sequence is
-                        scheduled: results agree up to fp32 rounding order. */
+    int32_t chunk;   /* ssm_scan_fwd only.  0: library default schedule.
+                        Otherwise a cap on the work of one CTA, in tokens of a
+                        channel group, at least seqlen: the scan then runs on
+                        at most ceil(groups * seqlen / chunk) CTAs, splitting a
+                        group's tokens between two CTAs where the ranges fall.
+                        It changes only the schedule: the arithmetic of every
+                        channel is the same, so outputs are bitwise equal. */
 } ssm_dims;
 
 /*
@@ -109,8 +112,15 @@ typedef struct ssm_dims {
  *                  NULL to skip writing it
  *   workspace      device scratch of at least ssm_scan_fwd_workspace_size()
  *                  bytes, 256-byte aligned; may be NULL when that size is 0.
- *                  Its contents on entry do not matter; the call owns it until
- *                  the enqueued work finishes.
+ *                  Its contents on entry do not matter (the call clears what it
+ *                  needs with cudaMemsetAsync on `stream`); the call owns it
+ *                  until the enqueued work finishes, so concurrent calls need
+ *                  separate workspaces.  The scan splits the token range of
+ *                  some channel groups between two CTAs and hands the state
+ *                  over through the workspace; that hand-over waits at most
+ *                  about a second.  When the work has finished, the first
+ *                  int32 of the workspace is SSM_OK, or SSM_ERR_TIMEOUT if a
+ *                  hand-over gave up (the affected outputs are then NaN).
  *   stream         cudaStream_t to enqueue on (NULL: the legacy default stream)
  *
  * Pointers of the I/O type must be aligned to the element size; the library

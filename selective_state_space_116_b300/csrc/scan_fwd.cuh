@@ -1,13 +1,30 @@
-// Forward selective scan, channel-parallel kernel.
+// Forward selective scan: state-split sequential kernel.
 //
-// Mapping: one thread owns one channel (b, d) and keeps all N state entries
-// h[0..N) in registers for the whole sequence, so the expanded state
-// (batch x dim x L x N) never leaves the SM.  A CTA owns kChannels channels
-// of one batch row and walks the sequence in tiles of kTile tokens: the
-// tile's u / delta / z rows and its B / C rows (shared by every channel of
-// the batch row) are staged in shared memory with coalesced loads, each
-// thread runs the recurrence over the tile, and y goes back through shared
-// memory for coalesced stores.
+// The recurrence h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t u_t is diagonal,
+// so the N state entries of a channel are N independent scalar recurrences
+// that only meet in the output sum y_t = sum_n C_{t,n} h_{t,n}.  This kernel
+// therefore walks each channel's sequence in order, exactly once, with its
+// state held in registers: S state entries per thread and G = N / S threads
+// per channel.  Per element-state that is the minimum work of the method (one
+// 2^x on the special-function unit, a multiply for Delta*A, a multiply for
+// Delta*u*B, one FMA for the state and one for the output); no second pass and
+// no scan of affine pairs is needed, and the B x D x L x N expanded state
+// never leaves the register file.
+//
+// The G threads of a channel sit in different warps (the group index is
+// warp-uniform), so every warp reads the same B/C row of shared memory
+// (a broadcast) and the G partial output sums meet in shared memory, not
+// through shuffles.
+//
+// A CTA owns CH = 128 / G channels of one batch row and a contiguous range of
+// that row's tokens, walked in tiles of kTL tokens.  Per tile:
+//   load      u, delta, z rows and the B, C tile -> shared memory (16-byte
+//             cp.async, double-buffered, zero-filled past the edges)
+//   prologue  Delta = softplus(delta + bias), Delta*u  -> fp32 (Delta, Delta u)
+//             pairs; B, C -> fp32, grouped by thread group
+//   recur     every thread advances its S states over the tile's tokens and
+//             writes its partial output sums
+//   epilogue  y = (sum of partials + D u) * silu(z) -> global, 16-byte stores
 #pragma once
 
 #include "common.cuh"
@@ -26,102 +43,237 @@ struct ScanParams {
     void* y;
     float* last_state;    // may be null
     int64_t batch, dim, L;
+    // schedule (see scan_fwd_kernel)
+    int64_t groups_per_row;   // ceil(dim / channels per CTA)
+    int64_t ngroups;          // batch * groups_per_row
+    int64_t ntiles;           // ceil(L / tile)
+    // workspace: status word, one flag per group, one carried state per group
+    int* status;
+    unsigned* flags;
+    float* carry;
 };
 
-namespace v1 {
+// Value a kernel leaves in the workspace status word when a bounded wait
+// gives up (the ABI's SSM_ERR_TIMEOUT).
+constexpr int kStatusTimeout = -9;
 
-constexpr int kChannels = 64;   // threads per CTA = channels per CTA
-constexpr int kTile = 64;       // tokens per staged tile
+namespace seq {
 
-template <typename T>
-struct Layout {
-    static constexpr int kRow = kTile + 16 / (int)sizeof(T);  // padded row, elements
-    static constexpr int kRowBytes = kRow * (int)sizeof(T);
-    static constexpr int kPlane = kChannels * kRowBytes;       // one (channel x token) plane
+constexpr int kThreads = 128;   // 4 warps
+constexpr int kTL = 32;         // tokens per tile
+
+// Shared-memory layout.  Row paddings of 16 bytes make every access pattern
+// below free of bank conflicts (each quarter-warp touches 8 distinct 16-byte
+// bank groups).
+template <typename T, int N, int S, bool HAS_Z>
+struct Shape {
+    static constexpr int G = N / S;                    // thread groups per channel
+    static constexpr int CH = kThreads / G;            // channels per CTA
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int EPC = 16 / ES;                // elements per 16-byte chunk
+    static constexpr int RAW_ROW = kTL * ES + 16;      // one channel's tokens, raw
+    static constexpr int RAW_PLANE = CH * RAW_ROW;
+    static constexpr int BC_RAW = kTL * N * ES;        // one raw B (or C) tile
+    static constexpr int NPLANES = HAS_Z ? 3 : 2;
+    static constexpr int RAW_BUF = NPLANES * RAW_PLANE + 2 * BC_RAW;
+    static constexpr int W_ROW = kTL * 8 + 16;         // (Delta, Delta u) per token
+    static constexpr int Y_ROW = kTL * 4 + 16;         // partial output per token
+    static constexpr int OFF_W = 2 * RAW_BUF;
+    static constexpr int OFF_BC = OFF_W + CH * W_ROW;
+    static constexpr int OFF_Y = OFF_BC + kTL * N * 2 * 4;
+    static constexpr int SMEM = OFF_Y + G * CH * Y_ROW;
+    // (row, 8-token chunk) work items of the prologue / epilogue per thread
+    static constexpr int CHUNKS = CH * kTL / 8;
+    static constexpr int CHUNK_ITERS = CHUNKS / kThreads;
+    static_assert(N % S == 0 && CH % 32 == 0, "bad state split");
+    static_assert(CHUNKS % kThreads == 0 && kTL % 32 == 0, "bad tile");
+    static_assert(RAW_BUF % 16 == 0 && OFF_BC % 16 == 0 && OFF_Y % 16 == 0, "alignment");
 };
 
-template <typename T, int N>
-constexpr size_t smem_bytes(bool has_z) {
-    return (size_t)(has_z ? 3 : 2) * Layout<T>::kPlane + 2u * kTile * N * sizeof(float);
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+// The (row, chunk) item a thread handles in prologue / epilogue iteration `it`:
+// a warp covers 8 rows x 4 consecutive 8-token chunks, lanes 0..7 on rows 0..7.
+template <int CH>
+__device__ __forceinline__ void chunk_of(int it, int& r, int& q) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int blk = it * (kThreads / 32) + warp;
+    constexpr int RB = CH / 8;
+    r = (blk % RB) * 8 + (lane & 7);
+    q = (blk / RB) * 4 + (lane >> 3);
 }
 
-// Copy a (kChannels x kTile) tile of a (batch, dim, L) tensor into a padded
-// shared-memory plane; out-of-range rows and columns read as zero.
-template <typename T, bool VEC>
-__device__ __forceinline__ void load_plane(T* plane, const T* g, int64_t row0, int rows,
-                                           int64_t L, int64_t t0) {
-    if constexpr (VEC) {
-        constexpr int kEpv = 16 / sizeof(T);            // elements per 16-byte vector
-        constexpr int kVpr = kTile / kEpv;              // vectors per row
-        for (int i = threadIdx.x; i < kChannels * kVpr; i += kChannels) {
-            const int r = i / kVpr, c = i % kVpr;
-            const int64_t t = t0 + (int64_t)c * kEpv;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < rows && t < L)   // L is a multiple of kEpv on this path
-                v = *reinterpret_cast<const uint4*>(g + (row0 + r) * L + t);
-            *reinterpret_cast<uint4*>(plane + r * Layout<T>::kRow + c * kEpv) = v;
-        }
-    } else {
-        for (int i = threadIdx.x; i < kChannels * kTile; i += kChannels) {
-            const int r = i / kTile, c = i % kTile;
-            const int64_t t = t0 + c;
-            T v = io<T>::from_f32(0.0f);
-            if (r < rows && t < L) v = g[(row0 + r) * L + t];
-            plane[r * Layout<T>::kRow + c] = v;
+// 8 consecutive elements of a raw shared-memory row -> fp32
+template <typename T> __device__ __forceinline__ void unpack8(const unsigned char* p, float (&v)[8]);
+template <> __device__ __forceinline__ void unpack8<float>(const unsigned char* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 16);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <> __device__ __forceinline__ void unpack8<__nv_bfloat16>(const unsigned char* p, float (&v)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    const unsigned w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// 8 consecutive fp32 values -> global row (16-byte stores; dst 16-byte aligned)
+template <typename T> __device__ __forceinline__ void store8(T* dst, const float (&v)[8]);
+template <> __device__ __forceinline__ void store8<float>(float* dst, const float (&v)[8]) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[8]) {
+    uint4 q;
+    unsigned* w = reinterpret_cast<unsigned*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);  // RNE
+        w[i] = *reinterpret_cast<const unsigned*>(&p);
+    }
+    *reinterpret_cast<uint4*>(dst) = q;
+}
+
+// Gate: silu(z).  bf16 outputs take the one-instruction tanh form
+// silu(z) = z/2 (1 + tanh(z/2)) (relative error ~2^-11, far below bf16's
+// 2^-9 rounding); fp32 outputs take z / (1 + 2^(-z log2 e)).
+template <typename T> __device__ __forceinline__ float gate(float z);
+template <> __device__ __forceinline__ float gate<float>(float z) { return silu(z); }
+template <> __device__ __forceinline__ float gate<__nv_bfloat16>(float z) {
+    const float hz = 0.5f * z;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hz));
+    return fmaf(hz, t, hz);
+}
+
+// Copy tile [t0, t0 + kTL) of CH rows of a (rows, L) tensor into a raw plane.
+// VEC: rows are 16-byte aligned and L is a multiple of EPC, so a 16-byte chunk
+// is either wholly inside or wholly outside the tensor.
+template <typename T, int CH, int RAW_ROW, bool VEC>
+__device__ __forceinline__ void load_plane(unsigned char* plane, const T* g, int64_t row0,
+                                           int rows, int64_t L, int64_t t0) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    constexpr int CPR = kTL / EPC;  // chunks per row
+    static_assert((CH * CPR) % kThreads == 0, "plane chunks must split evenly");
+#pragma unroll
+    for (int k = 0; k < CH * CPR / kThreads; k++) {
+        const int i = k * kThreads + threadIdx.x;
+        const int r = i / CPR, c = i % CPR;
+        const int64_t t = t0 + (int64_t)c * EPC;
+        unsigned char* dst = plane + r * RAW_ROW + c * 16;
+        if constexpr (VEC) {
+            const bool ok = r < rows && t < L;
+            cp_async16(dst, ok ? static_cast<const void*>(g + (row0 + r) * L + t) : g, ok ? 16 : 0);
+        } else {
+            T* d = reinterpret_cast<T*>(dst);
+#pragma unroll
+            for (int e = 0; e < EPC; e++)
+                d[e] = (r < rows && t + e < L) ? g[(row0 + r) * L + t + e] : io<T>::from_f32(0.0f);
         }
     }
 }
 
-template <typename T, bool VEC>
-__device__ __forceinline__ void store_plane(T* g, const T* plane, int64_t row0, int rows,
-                                            int64_t L, int64_t t0) {
-    if constexpr (VEC) {
-        constexpr int kEpv = 16 / sizeof(T);
-        constexpr int kVpr = kTile / kEpv;
-        for (int i = threadIdx.x; i < kChannels * kVpr; i += kChannels) {
-            const int r = i / kVpr, c = i % kVpr;
-            const int64_t t = t0 + (int64_t)c * kEpv;
-            if (r < rows && t < L)
-                *reinterpret_cast<uint4*>(g + (row0 + r) * L + t) =
-                    *reinterpret_cast<const uint4*>(plane + r * Layout<T>::kRow + c * kEpv);
-        }
-    } else {
-        for (int i = threadIdx.x; i < kChannels * kTile; i += kChannels) {
-            const int r = i / kTile, c = i % kTile;
-            const int64_t t = t0 + c;
-            if (r < rows && t < L) g[(row0 + r) * L + t] = plane[r * Layout<T>::kRow + c];
+// Copy tokens [t0, t0 + kTL) of one batch row of B or C (contiguous kTL*N run).
+template <typename T, int N, bool VEC>
+__device__ __forceinline__ void load_bc(unsigned char* dst, const T* g, int64_t L, int64_t t0) {
+    constexpr int EPC = 16 / (int)sizeof(T);
+    constexpr int CHUNKS = kTL * N / EPC;
+    const int64_t valid = (L - t0) * N;  // elements of this tile inside the tensor
+    for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
+        const int64_t e0 = (int64_t)i * EPC;
+        if constexpr (VEC) {
+            const bool ok = e0 < valid;
+            cp_async16(dst + i * 16, ok ? static_cast<const void*>(g + t0 * N + e0) : g, ok ? 16 : 0);
+        } else {
+            T* d = reinterpret_cast<T*>(dst + i * 16);
+#pragma unroll
+            for (int e = 0; e < EPC; e++)
+                d[e] = (e0 + e < valid) ? g[t0 * N + e0 + e] : io<T>::from_f32(0.0f);
         }
     }
 }
 
-template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool VEC>
-__global__ void __launch_bounds__(kChannels) scan_fwd_kernel(ScanParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    T* s_u = reinterpret_cast<T*>(smem);                        // u, then y in place
-    T* s_dl = reinterpret_cast<T*>(smem + Layout<T>::kPlane);
-    T* s_z = reinterpret_cast<T*>(smem + 2 * Layout<T>::kPlane);
-    float* s_B = reinterpret_cast<float*>(smem + (HAS_Z ? 3 : 2) * Layout<T>::kPlane);
-    float* s_C = s_B + kTile * N;
+// One token for one thread: advance S states, return the partial C.h.
+template <int S>
+__device__ __forceinline__ float token_step(float dt, float dtx, const float* __restrict__ bc,
+                                            float (&h)[S], const float (&A2)[S]) {
+    float Bv[S], Cv[S];
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int n = 0; n < S; n += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
+            const float4 c4 = *reinterpret_cast<const float4*>(bc + S + n);
+            Bv[n] = b4.x; Bv[n + 1] = b4.y; Bv[n + 2] = b4.z; Bv[n + 3] = b4.w;
+            Cv[n] = c4.x; Cv[n + 1] = c4.y; Cv[n + 2] = c4.z; Cv[n + 3] = c4.w;
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < S; n++) { Bv[n] = bc[n]; Cv[n] = bc[S + n]; }
+    }
+    if constexpr (S == 1) {
+        h[0] = fmaf(ex2(dt * A2[0]), h[0], dtx * Bv[0]);
+        return Cv[0] * h[0];
+    } else {
+        const float2 dt2 = make_float2(dt, dt);
+        const float2 dtx2 = make_float2(dtx, dtx);
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
+            const float2 a = make_float2(ex2(e.x), ex2(e.y));
+            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+            acc = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc);
+        }
+        return acc.x + acc.y;
+    }
+}
 
-    const int64_t b = blockIdx.y;
-    const int64_t d0 = (int64_t)blockIdx.x * kChannels;
-    const int rows = (int)(p.dim - d0 < kChannels ? p.dim - d0 : kChannels);
-    const int r = threadIdx.x;
-    const int64_t d = d0 + r;
-    const bool active = r < rows;
-    const int64_t row0 = b * p.dim + d0;          // first (b, d) row of this CTA
+// softplus(v) from x = v log2(e): ln2 * log2(1 + 2^x), or v itself once
+// v > 20 (the correction e^-v is then below half an fp32 ulp of v).
+__device__ __forceinline__ float softplus_log2(float x) {
+    constexpr float kX20 = 20.0f * kLog2e;
+    const float s = lg2(1.0f + ex2(x));
+    return kLn2 * (x > kX20 ? x : s);
+}
+
+// Bounded wait for the carry of `group` (set by the CTA that scanned the
+// group's earlier tokens).  Returns false if the wait gave up.
+__device__ __forceinline__ bool wait_flag(const unsigned* flag) {
+    constexpr long kSpinLimit = 1l << 22;   // ~1 s with the back-off below
+    for (long it = 0; it < kSpinLimit; it++) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v) return true;
+        __nanosleep(256);
+    }
+    return false;
+}
+
+template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC>
+__device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* smem, int64_t grp,
+                                          int64_t tb, int64_t te, int* s_ok) {
+    using Sh = Shape<T, N, S, HAS_Z>;
+    constexpr int G = Sh::G, CH = Sh::CH;
+
+    const int64_t b = grp / p.groups_per_row;
+    const int64_t d0 = (grp % p.groups_per_row) * CH;
+    const int rows = (int)(p.dim - d0 < CH ? p.dim - d0 : CH);
+    const int64_t row0 = b * p.dim + d0;   // first flat (b, d) row of the group
     const int64_t L = p.L;
-
-    // Per-channel constants.  A is pre-scaled by log2(e) so exp(Delta A) = 2^(Delta A').
-    float A2[N];
-#pragma unroll
-    for (int n = 0; n < N; n++) A2[n] = active ? p.A[d * N + n] * kLog2e : 0.0f;
-    const float Dv = (active && p.D) ? p.D[d] : 0.0f;
-    const float bias = (active && p.bias) ? p.bias[d] : 0.0f;
-
-    float h[N];
-#pragma unroll
-    for (int n = 0; n < N; n++) h[n] = 0.0f;
 
     const T* gu = static_cast<const T*>(p.u);
     const T* gdl = static_cast<const T*>(p.delta);
@@ -130,63 +282,234 @@ __global__ void __launch_bounds__(kChannels) scan_fwd_kernel(ScanParams p) {
     const T* gC = static_cast<const T*>(p.C) + b * L * N;
     T* gy = static_cast<T*>(p.y);
 
-    for (int64_t t0 = 0; t0 < L; t0 += kTile) {
-        const int tl = (int)(L - t0 < kTile ? L - t0 : kTile);
-        load_plane<T, VEC>(s_u, gu, row0, rows, L, t0);
-        load_plane<T, VEC>(s_dl, gdl, row0, rows, L, t0);
-        if constexpr (HAS_Z) load_plane<T, VEC>(s_z, gz, row0, rows, L, t0);
-        for (int i = threadIdx.x; i < kTile * N; i += kChannels) {
-            const bool in = i < tl * N;
-            s_B[i] = in ? io<T>::load(gB, t0 * N + i) : 0.0f;
-            s_C[i] = in ? io<T>::load(gC, t0 * N + i) : 0.0f;
+    // recurrence role: group g, channel ch; g is warp-uniform
+    const int g = threadIdx.x / CH, ch = threadIdx.x % CH;
+    const bool active = ch < rows;
+    float A2[S], h[S];
+#pragma unroll
+    for (int j = 0; j < S; j++)   // exp(Delta A) = 2^(Delta A log2 e)
+        A2[j] = active ? p.A[(d0 + ch) * N + g * S + j] * kLog2e : 0.0f;
+
+    // prologue / epilogue role: constants of the rows this thread touches
+    float bias_r[Sh::CHUNK_ITERS], D_r[Sh::CHUNK_ITERS];
+#pragma unroll
+    for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
+        int r, q;
+        chunk_of<CH>(it, r, q);
+        const float bv = (p.bias && r < rows) ? p.bias[d0 + r] : 0.0f;
+        bias_r[it] = SOFTPLUS ? bv * kLog2e : bv;
+        D_r[it] = (p.D && r < rows) ? p.D[d0 + r] : 0.0f;
+    }
+
+    auto load_tile = [&](int64_t tile, int slot) {
+        unsigned char* buf = smem + slot * Sh::RAW_BUF;
+        const int64_t t0 = tile * kTL;
+        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0);
+        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0);
+        if constexpr (HAS_Z)
+            load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0);
+        unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
+        load_bc<T, N, VEC>(bcraw, gB, L, t0);
+        load_bc<T, N, VEC>(bcraw + Sh::BC_RAW, gC, L, t0);
+    };
+
+    // the first tile's copies overlap the wait for the carry
+    load_tile(tb, 0);
+    cp_async_commit();
+
+    // initial state: zero at the sequence start, else the carry handed over
+    if (tb == 0) {
+#pragma unroll
+        for (int j = 0; j < S; j++) h[j] = 0.0f;
+    } else {
+        if (threadIdx.x == 0) {
+            const bool ok = wait_flag(p.flags + grp);
+            if (!ok) atomicExch(p.status, kStatusTimeout);
+            __threadfence();
+            *s_ok = ok;
+        }
+        __syncthreads();
+        const bool ok = *s_ok;
+        const float* src = p.carry + (grp * CH + ch) * N + g * S;
+#pragma unroll
+        for (int j = 0; j < S; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
+    }
+
+    for (int64_t tile = tb; tile < te; tile++) {
+        const int slot = (int)((tile - tb) & 1);
+        if (tile + 1 < te) load_tile(tile + 1, slot ^ 1);
+        cp_async_commit();
+        cp_async_wait_1();
+        __syncthreads();
+
+        const unsigned char* buf = smem + slot * Sh::RAW_BUF;
+        const int64_t t0 = tile * kTL;
+        const int tvalid = (int)(L - t0 < kTL ? L - t0 : kTL);
+
+        // ---- prologue: (Delta, Delta u) pairs, B/C to fp32 ----
+#pragma unroll
+        for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
+            int r, q;
+            chunk_of<CH>(it, r, q);
+            float uv[8], dv[8];
+            unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            unpack8<T>(buf + Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, dv);
+            float dt[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                if constexpr (SOFTPLUS) dt[e] = softplus_log2(fmaf(dv[e], kLog2e, bias_r[it]));
+                else dt[e] = dv[e] + bias_r[it];
+            }
+            if (tvalid < kTL) {   // tokens past the end leave the state untouched
+#pragma unroll
+                for (int e = 0; e < 8; e++)
+                    if (q * 8 + e >= tvalid) dt[e] = 0.0f;
+            }
+            float4* w = reinterpret_cast<float4*>(smem + Sh::OFF_W + r * Sh::W_ROW + q * 64);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+                w[e / 2] = make_float4(dt[e], dt[e] * uv[e], dt[e + 1], dt[e + 1] * uv[e + 1]);
+        }
+        {
+            const unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
+            float* bcf = reinterpret_cast<float*>(smem + Sh::OFF_BC);
+            if constexpr (N % 4 == 0 && S % 4 == 0) {
+                // 4 consecutive n of one token lie in one thread group: one 16-byte store
+                for (int i = threadIdx.x; i < 2 * kTL * N / 4; i += kThreads) {
+                    const int which = i / (kTL * N / 4);           // 0: B, 1: C
+                    const int e0 = (i % (kTL * N / 4)) * 4;
+                    const int t = e0 / N, n = e0 % N;
+                    const T* src = reinterpret_cast<const T*>(bcraw + which * Sh::BC_RAW) + e0;
+                    float4 v;
+                    v.x = io<T>::to_f32(src[0]); v.y = io<T>::to_f32(src[1]);
+                    v.z = io<T>::to_f32(src[2]); v.w = io<T>::to_f32(src[3]);
+                    *reinterpret_cast<float4*>(bcf + (t * G + n / S) * 2 * S + which * S + n % S) = v;
+                }
+            } else {
+                const T* rb = reinterpret_cast<const T*>(bcraw);
+                const T* rc = reinterpret_cast<const T*>(bcraw + Sh::BC_RAW);
+                for (int i = threadIdx.x; i < kTL * N; i += kThreads) {
+                    const int t = i / N, n = i % N;
+                    float* o = bcf + (t * G + n / S) * 2 * S + n % S;
+                    o[0] = io<T>::to_f32(rb[i]);
+                    o[S] = io<T>::to_f32(rc[i]);
+                }
+            }
         }
         __syncthreads();
 
-        T* my_u = s_u + r * Layout<T>::kRow;
-        const T* my_dl = s_dl + r * Layout<T>::kRow;
-        const T* my_z = s_z + r * Layout<T>::kRow;
-        for (int t = 0; t < tl; t++) {
-            const float x = io<T>::to_f32(my_u[t]);
-            const float v = io<T>::to_f32(my_dl[t]) + bias;
-            const float dt = SOFTPLUS ? softplus(v) : v;
-            const float dtx = dt * x;
-            const float* Bt = s_B + t * N;
-            const float* Ct = s_C + t * N;
-            float y0 = 0.0f, y1 = 0.0f;
-            if constexpr (N == 1) {
-                h[0] = fmaf(ex2(dt * A2[0]), h[0], dtx * Bt[0]);
-                y0 = Ct[0] * h[0];
-            } else {
-                const float2 dt2 = make_float2(dt, dt);
-                const float2 dtx2 = make_float2(dtx, dtx);
-                float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int n = 0; n < N; n += 2) {
-                    const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
-                    const float2 a = make_float2(ex2(e.x), ex2(e.y));
-                    const float2 bb = __fmul2_rn(dtx2, *reinterpret_cast<const float2*>(Bt + n));
-                    const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
-                    h[n] = hn.x;
-                    h[n + 1] = hn.y;
-                    acc = __ffma2_rn(*reinterpret_cast<const float2*>(Ct + n), hn, acc);
-                }
-                y0 = acc.x;
-                y1 = acc.y;
+        // ---- recurrence over the tile ----
+        {
+            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
+            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
+            float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
+#pragma unroll 2
+            for (int t = 0; t < kTL; t += 4) {
+                const float4 w01 = wrow[t / 2];
+                const float4 w23 = wrow[t / 2 + 1];
+                float4 out;
+                out.x = token_step<S>(w01.x, w01.y, bcf + (t + 0) * G * 2 * S, h, A2);
+                out.y = token_step<S>(w01.z, w01.w, bcf + (t + 1) * G * 2 * S, h, A2);
+                out.z = token_step<S>(w23.x, w23.y, bcf + (t + 2) * G * 2 * S, h, A2);
+                out.w = token_step<S>(w23.z, w23.w, bcf + (t + 3) * G * 2 * S, h, A2);
+                *reinterpret_cast<float4*>(yrow + t) = out;
             }
-            float yv = fmaf(Dv, x, y0 + y1);
-            if constexpr (HAS_Z) yv *= silu(io<T>::to_f32(my_z[t]));
-            my_u[t] = io<T>::from_f32(yv);   // y overwrites u in place: same thread, same slot
         }
         __syncthreads();
-        store_plane<T, VEC>(gy, s_u, row0, rows, L, t0);
+
+        // ---- epilogue: y = (sum of partials + D u) * silu(z) ----
+#pragma unroll
+        for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
+            int r, q;
+            chunk_of<CH>(it, r, q);
+            float ys[8];
+#pragma unroll
+            for (int gg = 0; gg < G; gg++) {
+                const float4* yp = reinterpret_cast<const float4*>(
+                    smem + Sh::OFF_Y + (gg * CH + r) * Sh::Y_ROW + q * 32);
+                const float4 a = yp[0], c = yp[1];
+                const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int e = 0; e < 8; e++) ys[e] = gg == 0 ? v[e] : ys[e] + v[e];
+            }
+            float uv[8];
+            unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+#pragma unroll
+            for (int e = 0; e < 8; e++) ys[e] = fmaf(D_r[it], uv[e], ys[e]);
+            if constexpr (HAS_Z) {
+                float zv[8];
+                unpack8<T>(buf + 2 * Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, zv);
+#pragma unroll
+                for (int e = 0; e < 8; e++) ys[e] *= gate<T>(zv[e]);
+            }
+            if (r < rows && q * 8 < tvalid) {
+                T* dst = gy + (row0 + r) * L + t0 + q * 8;
+                if (VEC && q * 8 + 8 <= tvalid) {
+                    store8<T>(dst, ys);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; e++)
+                        if (q * 8 + e < tvalid) dst[e] = io<T>::from_f32(ys[e]);
+                }
+            }
+        }
         __syncthreads();
     }
 
-    if (active && p.last_state) {
+    if (te == p.ntiles) {
+        if (active && p.last_state) {
+            float* dst = p.last_state + (row0 + ch) * N + g * S;
 #pragma unroll
-        for (int n = 0; n < N; n++) p.last_state[(row0 + r) * N + n] = h[n];
+            for (int j = 0; j < S; j++) dst[j] = h[j];
+        }
+    } else {
+        // hand the state over to the CTA that scans the rest of this group
+        float* dst = p.carry + (grp * CH + ch) * N + g * S;
+#pragma unroll
+        for (int j = 0; j < S; j++) __stcg(dst + j, h[j]);
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + grp), "r"(1u) : "memory");
     }
 }
 
-}  // namespace v1
+// Persistent, balanced schedule.  The work is ngroups x ntiles tiles (a
+// group is CH channels of one batch row); CTA c takes the contiguous range
+// [c W / P, (c+1) W / P) of the group-major order, so every CTA gets the same
+// number of tiles to within one.  A range that starts inside a group
+// continues the state of the CTA before it: each CTA scans its last group's
+// head first (publishing that state), then its whole groups, and the
+// continuation of its first group last, so the state it needs has long been
+// published when it gets there.  With P <= ngroups no group is split twice.
+template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC>
+__global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_ok;
+    const int64_t W = p.ngroups * p.ntiles;
+    const int64_t s = W * blockIdx.x / gridDim.x;
+    const int64_t e = W * (blockIdx.x + 1) / gridDim.x;
+    if (s >= e) {   // empty sequence (or more CTAs than tiles): only last_state remains
+        if (p.ntiles == 0 && p.last_state) {
+            using Sh = Shape<T, N, S, HAS_Z>;
+            for (int64_t grp = blockIdx.x; grp < p.ngroups; grp += gridDim.x) {
+                const int64_t b = grp / p.groups_per_row;
+                const int64_t d0 = (grp % p.groups_per_row) * Sh::CH;
+                const int rows = (int)(p.dim - d0 < Sh::CH ? p.dim - d0 : Sh::CH);
+                for (int i = threadIdx.x; i < rows * N; i += kThreads)
+                    p.last_state[(b * p.dim + d0) * N + i] = 0.0f;
+            }
+        }
+        return;
+    }
+    const int64_t g_first = s / p.ntiles, g_last = (e - 1) / p.ntiles;
+    for (int64_t grp = g_last; grp >= g_first; grp--) {
+        const int64_t lo = grp * p.ntiles;
+        const int64_t tb = (s > lo ? s : lo) - lo;
+        const int64_t te = (e < lo + p.ntiles ? e : lo + p.ntiles) - lo;
+        scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok);
+    }
+}
+
+}  // namespace seq
 }  // namespace ssm

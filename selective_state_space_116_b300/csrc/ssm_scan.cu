@@ -57,7 +57,7 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
     if (dims->batch < 1 || dims->dim < 1 || dims->dstate < 1) return SSM_ERR_BAD_DIMS;
     if (scan && dims->seqlen < 0) return SSM_ERR_BAD_DIMS;
     if (!valid_n(dims->dstate)) return SSM_ERR_UNSUPPORTED_N;
-    if (scan && dims->chunk != 0 && (dims->chunk < 0 || dims->chunk % 64 != 0))
+    if (scan && (dims->chunk < 0 || (dims->chunk > 0 && dims->chunk < dims->seqlen)))
         return SSM_ERR_BAD_DIMS;
     if (scan && dims->batch > 65535) return SSM_ERR_BAD_DIMS;  // grid.y limit of the scan launch
     const int64_t L = scan ? dims->seqlen : 1;
@@ -70,23 +70,98 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
     return SSM_OK;
 }
 
+// Build-time tuning knobs.  States per thread for N = 16 (8: two thread
+// groups per channel), and a cap on resident scan CTAs per SM (0: as many as
+// fit).
+#ifndef SSM_N16_SPLIT
+#define SSM_N16_SPLIT 8
+#endif
+#ifndef SSM_SCAN_CTAS_PER_SM
+#define SSM_SCAN_CTAS_PER_SM 0
+#endif
+
+template <int N> struct Split { static constexpr int S = N <= 8 ? N : SSM_N16_SPLIT; };
+
+// Workspace of the scan: a 256-byte header (status word), one flag per
+// channel group, one carried state (CH x N fp32) per channel group.
+struct ScanWorkspace {
+    size_t flags_off, carry_off, clear_bytes, total;
+};
+
+template <int N> constexpr int scan_channels_per_cta() {
+    return ssm::seq::kThreads / (N / Split<N>::S);
+}
+
+int scan_channels_per_cta(int64_t n) {
+    switch (n) {
+        case 1: return scan_channels_per_cta<1>();
+        case 2: return scan_channels_per_cta<2>();
+        case 4: return scan_channels_per_cta<4>();
+        case 8: return scan_channels_per_cta<8>();
+        case 16: return scan_channels_per_cta<16>();
+    }
+    return 0;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+ScanWorkspace scan_workspace(const ssm_dims* d) {
+    ScanWorkspace w{};
+    if (d->seqlen == 0) return w;
+    const int ch = scan_channels_per_cta(d->dstate);
+    const int64_t groups = d->batch * ((d->dim + ch - 1) / ch);
+    w.flags_off = 256;
+    w.carry_off = w.flags_off + round256((size_t)groups * 4);
+    w.clear_bytes = w.carry_off;
+    w.total = w.carry_off + round256((size_t)groups * ch * d->dstate * 4);
+    return w;
+}
+
 template <typename T, int N, bool Z, bool SP, bool VEC>
-int launch_scan(const ssm::ScanParams& p, cudaStream_t stream) {
-    using namespace ssm::v1;
-    auto kern = scan_fwd_kernel<T, N, Z, SP, VEC>;
-    const size_t smem = smem_bytes<T, N>(Z);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, const ScanWorkspace& wl,
+                cudaStream_t stream) {
+    using namespace ssm::seq;
+    constexpr int S = Split<N>::S;
+    using Sh = Shape<T, N, S, Z>;
+    auto kern = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
-    const dim3 grid((unsigned)((p.dim + kChannels - 1) / kChannels), (unsigned)p.batch);
-    kern<<<grid, kChannels, smem, stream>>>(p);
+    p.groups_per_row = (p.dim + Sh::CH - 1) / Sh::CH;
+    p.ngroups = p.batch * p.groups_per_row;
+    p.ntiles = (p.L + kTL - 1) / kTL;
+    // one resident wave of persistent CTAs, never more CTAs than groups
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, Sh::SMEM) !=
+            cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (occ < 1) return SSM_ERR_CUDA;
+    if (SSM_SCAN_CTAS_PER_SM > 0 && SSM_SCAN_CTAS_PER_SM < occ) occ = SSM_SCAN_CTAS_PER_SM;
+    int64_t ctas = (int64_t)occ * sms;
+    if (ctas > p.ngroups) ctas = p.ngroups;
+    if (chunk > 0 && p.ntiles > 0) {   // caller-chosen work per CTA (>= one group's tokens)
+        const int64_t per = (chunk + kTL - 1) / kTL;
+        const int64_t want = (p.ngroups * p.ntiles + per - 1) / per;
+        if (want < ctas) ctas = want;
+    }
+    if (ctas < 1) ctas = 1;
+    if (p.ntiles > 0) {
+        p.status = reinterpret_cast<int*>(ws);
+        p.flags = reinterpret_cast<unsigned*>(ws + wl.flags_off);
+        p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
+        if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    kern<<<(unsigned)ctas, kThreads, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 template <typename T, int N>
-int dispatch_scan_n(const ssm::ScanParams& p, bool z, bool sp, bool vec, cudaStream_t s) {
+int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+                    unsigned char* ws, const ScanWorkspace& wl, cudaStream_t s) {
 #define SSM_SCAN_CASE(Z, SP, V) \
-    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, Z, SP, V>(p, s);
+    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, Z, SP, V>(p, chunk, ws, wl, s);
     SSM_SCAN_CASE(false, false, false)
     SSM_SCAN_CASE(false, false, true)
     SSM_SCAN_CASE(false, true, false)
@@ -100,13 +175,14 @@ int dispatch_scan_n(const ssm::ScanParams& p, bool z, bool sp, bool vec, cudaStr
 }
 
 template <typename T>
-int dispatch_scan(const ssm::ScanParams& p, int64_t n, bool z, bool sp, bool vec, cudaStream_t s) {
+int dispatch_scan(const ssm::ScanParams& p, int64_t n, int64_t chunk, bool z, bool sp, bool vec,
+                  unsigned char* ws, const ScanWorkspace& wl, cudaStream_t s) {
     switch (n) {
-        case 1: return dispatch_scan_n<T, 1>(p, z, sp, vec, s);
-        case 2: return dispatch_scan_n<T, 2>(p, z, sp, vec, s);
-        case 4: return dispatch_scan_n<T, 4>(p, z, sp, vec, s);
-        case 8: return dispatch_scan_n<T, 8>(p, z, sp, vec, s);
-        case 16: return dispatch_scan_n<T, 16>(p, z, sp, vec, s);
+        case 1: return dispatch_scan_n<T, 1>(p, chunk, z, sp, vec, ws, wl, s);
+        case 2: return dispatch_scan_n<T, 2>(p, chunk, z, sp, vec, ws, wl, s);
+        case 4: return dispatch_scan_n<T, 4>(p, chunk, z, sp, vec, ws, wl, s);
+        case 8: return dispatch_scan_n<T, 8>(p, chunk, z, sp, vec, ws, wl, s);
+        case 16: return dispatch_scan_n<T, 16>(p, chunk, z, sp, vec, ws, wl, s);
     }
     return SSM_ERR_UNSUPPORTED_N;
 }
@@ -184,7 +260,7 @@ int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
     const int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
     if (!bytes) return SSM_ERR_NULL_ARG;
-    *bytes = 0;
+    *bytes = scan_workspace(dims).total;
     return SSM_OK;
 }
 
@@ -192,8 +268,6 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus, void* y, float* last_state,
                  void* workspace, size_t workspace_bytes, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
@@ -217,15 +291,29 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
         if (overlap(r, out_y) || overlap(r, out_h)) return SSM_ERR_ALIAS;
     if (overlap(out_y, out_h)) return SSM_ERR_ALIAS;
 
-    ssm::ScanParams p{u, delta, A, B, C, D, z, delta_bias, y, last_state,
-                      dims->batch, dims->dim, dims->seqlen};
+    const ScanWorkspace wl = scan_workspace(dims);
+    if (wl.total > 0) {
+        if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+            return SSM_ERR_WORKSPACE;
+        const Range ws{workspace, (int64_t)wl.total};
+        for (const Range& r : in)
+            if (overlap(r, ws)) return SSM_ERR_ALIAS;
+        if (overlap(out_y, ws) || overlap(out_h, ws)) return SSM_ERR_ALIAS;
+    }
+    ssm::ScanParams p{};
+    p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.bias = delta_bias; p.y = y; p.last_state = last_state;
+    p.batch = dims->batch; p.dim = dims->dim; p.L = dims->seqlen;
     // 16-byte vector path: every row of u/delta/z/y starts on a 16-byte boundary
     const bool vec = (dims->seqlen * (int64_t)es) % 16 == 0 && aligned(u, 16) &&
-                     aligned(delta, 16) && aligned(y, 16) && (!z || aligned(z, 16));
+                     aligned(delta, 16) && aligned(y, 16) && (!z || aligned(z, 16)) &&
+                     aligned(B, 16) && aligned(C, 16);
     const bool sp = delta_softplus != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dims->io == SSM_IO_BF16) return dispatch_scan<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
-    return dispatch_scan<float>(p, dims->dstate, z != nullptr, sp, vec, st);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    if (dims->io == SSM_IO_BF16)
+        return dispatch_scan<bf16>(p, dims->dstate, dims->chunk, z != nullptr, sp, vec, ws, wl, st);
+    return dispatch_scan<float>(p, dims->dstate, dims->chunk, z != nullptr, sp, vec, ws, wl, st);
 }
 
 int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void* delta,

@@ -75,7 +75,7 @@ def step(lib, d, state=P[0], x=P[1], delta=P[2], A=P[3], B=P[4], C=P[5], D=P[6],
     (dict(dstate=32), _lib.SSM_ERR_UNSUPPORTED_N),
     (dict(dstate=0), _lib.SSM_ERR_BAD_DIMS),
     (dict(io=7), _lib.SSM_ERR_BAD_DTYPE),
-    (dict(chunk=100), _lib.SSM_ERR_BAD_DIMS),
+    (dict(chunk=63), _lib.SSM_ERR_BAD_DIMS),     # below seqlen
     (dict(chunk=-64), _lib.SSM_ERR_BAD_DIMS),
     (dict(batch=1 << 40, dim=1 << 40), _lib.SSM_ERR_BAD_DIMS),
     (dict(batch=70000), _lib.SSM_ERR_BAD_DIMS),
@@ -129,3 +129,35 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _lib.load(missing)
     finally:
         _lib._lib = saved
+
+
+def test_scan_workspace_checks(lib):
+    """The scan needs the workspace it reports; a missing, short, misaligned or
+    overlapping one is refused before anything is enqueued."""
+    d = dims(batch=2, dim=8, dstate=16, seqlen=64)
+    need = ctypes.c_size_t(0)
+    assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(need)) == _lib.SSM_OK
+    assert need.value >= 256
+    ws = P[10]
+    assert scan(lib, d) == _lib.SSM_ERR_WORKSPACE                               # none
+    assert scan(lib, d, ws=ws, ws_bytes=need.value - 1) == _lib.SSM_ERR_WORKSPACE
+    assert scan(lib, d, ws=ws + 16, ws_bytes=need.value) == _lib.SSM_ERR_WORKSPACE
+    assert scan(lib, d, ws=P[0], ws_bytes=need.value) == _lib.SSM_ERR_ALIAS     # == u
+    assert scan(lib, d, ws=P[8] + 256, ws_bytes=need.value) == _lib.SSM_ERR_ALIAS  # inside y
+    # an empty sequence needs none
+    d0 = dims(batch=2, dim=8, dstate=16, seqlen=0)
+    assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(d0), ctypes.byref(need)) == _lib.SSM_OK
+    assert need.value == 0
+
+
+@pytest.mark.parametrize("N,ch", [(1, 128), (2, 128), (4, 128), (8, 128), (16, 64)])
+def test_scan_workspace_size_formula(lib, N, ch):
+    """256-byte header, one flag per channel group, one carried state per group
+    (a group is the channels one CTA scans together)."""
+    batch, dim = 3, 200
+    d = dims(batch=batch, dim=dim, dstate=N, seqlen=10)
+    need = ctypes.c_size_t(0)
+    assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(need)) == _lib.SSM_OK
+    groups = batch * -(-dim // ch)
+    r256 = lambda x: -(-x // 256) * 256
+    assert need.value == 256 + r256(groups * 4) + r256(groups * ch * N * 4)

@@ -162,3 +162,61 @@ def test_dna_workload_sampled_channels():
     hv = as64(h.reshape(-1, w.dstate)[torch.from_numpy(chans).cuda()])
     assert_close(yv, y_ref, torch.float32, "dna y")
     assert_close(hv, h_ref, torch.float32, "dna last_state")
+
+
+# -- the persistent schedule: a channel group's tokens split between two CTAs --
+SPLIT = Workload("split", 3, 130, 16, 1000, "bf16", bias_range=(-4.0, -2.0),
+                 a_kind="neg_exp_uniform", gate=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [4, 16])
+@pytest.mark.parametrize("frac", [1.0, 1.3, 2.5, 7.0])
+def test_split_groups_match_oracle(io, N, frac):
+    """chunk caps the tokens one CTA scans; ranges that end inside a channel
+    group hand the state over to the next CTA through the workspace."""
+    w = SPLIT.scaled(io=io, dstate=N)
+    inp = make_scan_inputs(w, seed=3)
+    y, h = gpu_scan(inp, chunk=int(w.seqlen * frac))
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, w.torch_io, "y")
+    assert_close(as64(h), h_ref, w.torch_io, "last_state")
+
+
+def test_schedule_is_bitwise_invariant():
+    """Every channel's arithmetic is the same whichever CTA scans which tokens."""
+    w = SPLIT.scaled(io="bf16", seqlen=777)
+    inp = make_scan_inputs(w, seed=8)
+    y0, h0 = gpu_scan(inp)
+    for chunk in (777, 900, 1500, 2333, 5000):
+        y1, h1 = gpu_scan(inp, chunk=chunk)
+        assert torch.equal(y0, y1) and torch.equal(h0, h1), chunk
+
+
+def test_workspace_status_word():
+    """After the work finishes the workspace's first int32 reads SSM_OK."""
+    import selective_state_space_116_b300 as ssm
+    from parity import to_cuda
+    w = SPLIT.scaled(io="f32")
+    g = to_cuda(make_scan_inputs(w, seed=1))
+    nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, torch.float32)
+    ws = torch.full((nbytes,), 0x55, dtype=torch.uint8, device="cuda")   # stale contents
+    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                     delta_bias=g["delta_bias"], delta_softplus=True, workspace=ws,
+                     chunk=2 * w.seqlen)
+    torch.cuda.synchronize()
+    assert ws[:4].view(torch.int32).item() == 0
+
+
+def test_default_schedule_splits_large_problem():
+    """More channel groups than resident CTAs: the default schedule splits
+    groups between CTAs (8 x 3840 channels, N = 16 -> 480 groups)."""
+    w = Workload("wide", 8, 3840, 16, 200, "bf16", bias_range=(-4.0, -2.0),
+                 a_kind="neg_index", gate=True)
+    inp = make_scan_inputs(w, seed=2)
+    y, h = gpu_scan(inp)
+    chans = sample_channels(w.batch, w.dim, 256)
+    y_ref, h_ref = oracle_scan(inp, channels=chans)
+    idx = torch.from_numpy(chans).cuda()
+    assert_close(as64(y.reshape(-1, w.seqlen)[idx]), y_ref, torch.bfloat16, "y")
+    assert_close(as64(h.reshape(-1, w.dstate)[idx]), h_ref, torch.bfloat16, "last_state")
