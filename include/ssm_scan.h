@@ -73,7 +73,8 @@ typedef enum ssm_status {
     SSM_ERR_CUDA = -6,          /* the CUDA runtime refused the launch */
     SSM_ERR_WORKSPACE = -7,     /* workspace missing, too small or misaligned */
     SSM_ERR_ALIAS = -8,         /* an output overlaps an input */
-    SSM_ERR_TIMEOUT = -9        /* a bounded on-device wait gave up */
+    SSM_ERR_TIMEOUT = -9,       /* a bounded on-device wait gave up */
+    SSM_ERR_TOO_LARGE = -10     /* needs more scratch than ssm_scan_fwd_noalloc holds */
 } ssm_status;
 
 typedef enum ssm_io_dtype { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
@@ -138,6 +139,40 @@ SSM_API int ssm_scan_fwd(const ssm_dims* dims,
 /* Bytes of device workspace ssm_scan_fwd needs for these sizes (may be 0).
  * Returns SSM_OK or a negative ssm_status (bad dims). */
 SSM_API int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes);
+
+/*
+ * ssm_scan_fwd without a workspace argument, for callers that cannot allocate
+ * device memory when they call the scan (for example an inference engine's
+ * plugin confined to a memory plan fixed in advance, or a real-time path
+ * where allocation is forbidden).  The source pages have no counterpart to
+ * this entry point; it exists only for such callers.
+ *
+ * The scratch the scan needs lives in one fixed buffer inside the library,
+ * ssm_scan_fwd_noalloc_max_scratch() bytes (4 MiB) on every device that loads
+ * the library, held until the process exits.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.  Problems whose
+ * ssm_scan_fwd_workspace_size() exceeds the buffer are refused with
+ * SSM_ERR_TOO_LARGE before anything is enqueued (at N = 16 the buffer holds
+ * about 1000 groups of 64 channels, e.g. batch 4 x 16000 channels).
+ *
+ * The first call on a device looks up the buffer's device address on that
+ * device (cudaGetSymbolAddress, with the device current); make that first
+ * call before any stream capture.  Every call shares the one buffer: calls
+ * whose work overlaps on the GPU (different streams, or host threads racing)
+ * race on it and give wrong results, so serialise them, e.g. on one stream.
+ * The call clears the part of the buffer that must start at zero, on
+ * `stream`, before the scan reads it; the status word left there is not
+ * readable from the host.  Arguments, outputs and errors are otherwise those
+ * of ssm_scan_fwd.
+ */
+SSM_API int ssm_scan_fwd_noalloc(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 void* y, float* last_state, void* stream);
+
+/* Size in bytes of ssm_scan_fwd_noalloc's built-in scratch buffer. */
+SSM_API size_t ssm_scan_fwd_noalloc_max_scratch(void);
 
 /*
  * One token of recurrent (generation) mode: the same update with L = 1,

@@ -22,12 +22,14 @@ SSM_ERR_CUDA = -6
 SSM_ERR_WORKSPACE = -7
 SSM_ERR_ALIAS = -8
 SSM_ERR_TIMEOUT = -9
+SSM_ERR_TOO_LARGE = -10
 
 SSM_IO_F32 = 0
 SSM_IO_BF16 = 1
 
 # every symbol include/ssm_scan.h declares
-EXPORTS = ("ssm_probe_ex2", "ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_state_step",
+EXPORTS = ("ssm_probe_ex2", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
+           "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_workspace_size", "ssm_state_step",
            "ssm_status_string", "ssm_version")
 
 
@@ -60,6 +62,10 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     dims_p = ctypes.POINTER(ssm_dims)
     lib.ssm_scan_fwd.restype = i32
     lib.ssm_scan_fwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.ssm_scan_fwd_noalloc.restype = i32
+    lib.ssm_scan_fwd_noalloc.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+    lib.ssm_scan_fwd_noalloc_max_scratch.restype = sz
+    lib.ssm_scan_fwd_noalloc_max_scratch.argtypes = []
     lib.ssm_scan_fwd_workspace_size.restype = i32
     lib.ssm_scan_fwd_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
     lib.ssm_state_step.restype = i32

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "probe.cuh"
@@ -243,6 +244,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
         case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
+        case SSM_ERR_TOO_LARGE:
+            return "the problem needs more scratch than the library's built-in buffer holds";
     }
     return "unknown status";
 }
@@ -345,5 +348,61 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
     if (dims->io == SSM_IO_BF16) return dispatch_step<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
     return dispatch_step<float>(p, dims->dstate, z != nullptr, sp, vec, st);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward scan.
+//
+// Some callers cannot allocate device memory when they call the scan: an
+// inference engine's plugin that must live inside a memory plan fixed before
+// it runs, or code on a real-time or safety-critical path where allocation is
+// forbidden.  For them the scan's scratch (the status word, hand-over flags
+// and carried states) lives in this fixed device buffer instead of a
+// caller-supplied workspace.  Every device that loads the library holds the
+// buffer until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;   // 4 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+
+// The buffer's device address on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SSM_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SSM_OK;
+}
+
+}  // namespace
+
+int ssm_scan_fwd_noalloc(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                         const void* B, const void* C, const float* D, const void* z,
+                         const float* delta_bias, int delta_softplus, void* y,
+                         float* last_state, void* stream) {
+    size_t need = 0;
+    const int rc = ssm_scan_fwd_workspace_size(dims, &need);
+    if (rc != SSM_OK) return rc;
+    if (need > kNoAllocScratchBytes) return SSM_ERR_TOO_LARGE;
+    void* scratch = nullptr;
+    if (need > 0) {
+        const int rs = noalloc_scratch(&scratch);
+        if (rs != SSM_OK) return rs;
+    }
+    return ssm_scan_fwd(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                        scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
+
+size_t ssm_scan_fwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
 
 }  // extern "C"

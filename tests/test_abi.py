@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.ssm_version() >= 100
-    for code in range(0, -10, -1):
+    for code in range(0, -11, -1):
         s = _lib.status_string(code)
         assert s and s != "unknown status", code
     assert _lib.status_string(-99) == "unknown status"
@@ -161,3 +161,22 @@ def test_scan_workspace_size_formula(lib, N, ch):
     groups = batch * -(-dim // ch)
     r256 = lambda x: -(-x // 256) * 256
     assert need.value == 256 + r256(groups * 4) + r256(groups * ch * N * 4)
+
+
+def test_noalloc_refuses_problems_beyond_its_buffer(lib):
+    """The allocation-free scan rejects, on the host, any problem whose scratch
+    would not fit its built-in buffer; bad sizes get the usual errors."""
+    cap = lib.ssm_scan_fwd_noalloc_max_scratch()
+    assert cap == 4 << 20
+    big = dims(batch=4, dim=64 * 2000, dstate=16, seqlen=128)   # 8000 groups x 4 KiB of state
+    need = ctypes.c_size_t(0)
+    assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(big), ctypes.byref(need)) == _lib.SSM_OK
+    assert need.value > cap
+
+    def noalloc(d):
+        return lib.ssm_scan_fwd_noalloc(ctypes.byref(d) if d is not None else None, P[0], P[1],
+                                        P[2], P[3], P[4], P[5], P[6], P[7], 1, P[8], P[9], None)
+    assert noalloc(big) == _lib.SSM_ERR_TOO_LARGE
+    assert noalloc(None) == _lib.SSM_ERR_NULL_ARG
+    assert noalloc(dims(dstate=3)) == _lib.SSM_ERR_UNSUPPORTED_N
+    assert noalloc(dims(batch=0)) == _lib.SSM_ERR_BAD_DIMS
