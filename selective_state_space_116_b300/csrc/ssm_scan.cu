@@ -3,6 +3,7 @@
 // alignment) on the caller's stream.  See include/ssm_scan.h for the contract.
 #include "ssm_scan.h"
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -10,6 +11,7 @@
 #include "common.cuh"
 #include "probe.cuh"
 #include "scan_fwd.cuh"
+#include "scan_fwd_tc.cuh"
 #include "state_step.cuh"
 
 namespace {
@@ -71,17 +73,16 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
     return SSM_OK;
 }
 
-// Build-time tuning knobs.  States per thread for N = 16 (8: two thread
-// groups per channel), and a cap on resident scan CTAs per SM (0: as many as
-// fit).
-#ifndef SSM_N16_SPLIT
-#define SSM_N16_SPLIT 8
-#endif
+// Build-time tuning knobs: a cap on resident scan CTAs per SM (0: as many as
+// fit), and whether bf16 / N = 16 scans take the tensor-core kernel of
+// scan_fwd_tc.cuh (off: its synchronous 8-token pipeline is still slower
+// than the state-split kernel).
 #ifndef SSM_SCAN_CTAS_PER_SM
 #define SSM_SCAN_CTAS_PER_SM 0
 #endif
-
-template <int N> struct Split { static constexpr int S = N <= 8 ? N : SSM_N16_SPLIT; };
+#ifndef SSM_SCAN_TC
+#define SSM_SCAN_TC 0
+#endif
 
 // Workspace of the scan: a 256-byte header (status word), one flag per
 // channel group, one carried state (CH x N fp32) per channel group.
@@ -89,27 +90,42 @@ struct ScanWorkspace {
     size_t flags_off, carry_off, clear_bytes, total;
 };
 
-template <int N> constexpr int scan_channels_per_cta() {
-    return ssm::seq::kThreads / (N / Split<N>::S);
+// SM count of the current device, looked up once per device.
+int device_sms(int* sms) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && cache[dev].load() > 0) {
+        *sms = cache[dev].load();
+        return SSM_OK;
+    }
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        *sms < 1)
+        return SSM_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cache[dev].store(*sms);
+    return SSM_OK;
 }
 
-int scan_channels_per_cta(int64_t n) {
-    switch (n) {
-        case 1: return scan_channels_per_cta<1>();
-        case 2: return scan_channels_per_cta<2>();
-        case 4: return scan_channels_per_cta<4>();
-        case 8: return scan_channels_per_cta<8>();
-        case 16: return scan_channels_per_cta<16>();
-    }
-    return 0;
+// Channels one CTA of the state-split kernel scans with S states per thread.
+constexpr int seq_channels(int n, int s) { return ssm::seq::kThreads / (n / s); }
+
+// States per thread for N = 16: 8 (two thread groups per channel, less
+// shared-memory traffic per element) when the problem has enough 64-channel
+// groups to give every SM two of them, else 4 (twice the CTAs).
+int n16_split(const ssm_dims* d, int sms) {
+    const int64_t groups8 = d->batch * ((d->dim + 63) / 64);
+    return groups8 >= 2 * (int64_t)sms ? 8 : 4;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-ScanWorkspace scan_workspace(const ssm_dims* d) {
+ssm_dims wl_dims(const ssm::ScanParams& p, int n) {
+    return ssm_dims{p.batch, p.dim, n, p.L, SSM_IO_F32, 0};
+}
+
+ScanWorkspace scan_workspace_for(const ssm_dims* d, int ch) {
     ScanWorkspace w{};
     if (d->seqlen == 0) return w;
-    const int ch = scan_channels_per_cta(d->dstate);
     const int64_t groups = d->batch * ((d->dim + ch - 1) / ch);
     w.flags_off = 256;
     w.carry_off = w.flags_off + round256((size_t)groups * 4);
@@ -118,51 +134,111 @@ ScanWorkspace scan_workspace(const ssm_dims* d) {
     return w;
 }
 
-template <typename T, int N, bool Z, bool SP, bool VEC>
-int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, const ScanWorkspace& wl,
-                cudaStream_t stream) {
-    using namespace ssm::seq;
-    constexpr int S = Split<N>::S;
-    using Sh = Shape<T, N, S, Z>;
-    auto kern = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
+// The tensor-core kernel serves bf16 I/O with N = 16 when every row of the
+// (batch, dim, L) tensors is 16-byte aligned and L is a whole number of its
+// 8-token blocks; it groups 128 channels, the other kernel 64.
+bool tc_shape(const ssm_dims* d) {
+    return SSM_SCAN_TC && d->io == SSM_IO_BF16 && d->dstate == 16 && d->seqlen > 0 && d->seqlen % 8 == 0;
+}
+
+// The workspace covers whichever kernel and split the call selects.
+ScanWorkspace scan_workspace(const ssm_dims* d) {
+    const int n = (int)d->dstate;
+    ScanWorkspace w = scan_workspace_for(d, seq_channels(n, n <= 8 ? n : 8));
+    if (n == 16) {
+        const ScanWorkspace w4 = scan_workspace_for(d, seq_channels(16, 4));
+        if (w4.total > w.total) w = w4;
+    }
+    if (tc_shape(d)) {
+        const ScanWorkspace t = scan_workspace_for(d, ssm::tc::kCH);
+        if (t.total > w.total) w = t;
+    }
+    return w;
+}
+
+template <bool Z, bool SP>
+int launch_scan_tc(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStream_t stream) {
+    using namespace ssm::tc;
+    auto kern = scan_fwd_tc_kernel<Z, SP>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
+    ssm_dims d{p.batch, p.dim, 16, p.L, SSM_IO_BF16, 0};
+    const ScanWorkspace wl = scan_workspace_for(&d, kCH);
+    p.groups_per_row = (p.dim + kCH - 1) / kCH;
+    p.ngroups = p.batch * p.groups_per_row;
+    p.ntiles = p.L / kTB;   // in 8-token blocks
+    int sms = 0;
+    if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
+    int64_t ctas = sms;   // one CTA per SM: each holds all of its tensor memory
+    if (ctas > p.ngroups) ctas = p.ngroups;
+    if (chunk > 0) {
+        const int64_t per = (chunk + kTB - 1) / kTB;
+        const int64_t want = (p.ngroups * p.ntiles + per - 1) / per;
+        if (want < ctas) ctas = want;
+    }
+    if (ctas < 1) ctas = 1;
+    p.status = reinterpret_cast<int*>(ws);
+    p.flags = reinterpret_cast<unsigned*>(ws + wl.flags_off);
+    p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
+    if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    kern<<<(unsigned)ctas, kThreads, kSmem, stream>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int N, int S, bool Z, bool SP, bool VEC>
+int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
+                cudaStream_t stream) {
+    using namespace ssm::seq;
+    using Sh = Shape<T, N, S, Z>;
+    auto kern = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
+    // per kernel instance: raise its shared-memory limit and ask how many
+    // CTAs fit on an SM, once
+    static std::atomic<int> occ_cache[64];   // per device: the attribute is per context
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSM_ERR_CUDA;
+    int occ = occ_cache[dev].load();
+    if (occ == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, Sh::SMEM) !=
+                cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (occ < 1) return SSM_ERR_CUDA;
+        occ_cache[dev].store(occ);
+    }
     p.groups_per_row = (p.dim + Sh::CH - 1) / Sh::CH;
     p.ngroups = p.batch * p.groups_per_row;
     p.ntiles = (p.L + kTL - 1) / kTL;
-    // one resident wave of persistent CTAs, never more CTAs than groups
-    int dev = 0, sms = 0, occ = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, Sh::SMEM) !=
-            cudaSuccess)
-        return SSM_ERR_CUDA;
-    if (occ < 1) return SSM_ERR_CUDA;
+    // One resident wave of persistent CTAs, the same number on every SM, and
+    // never more CTAs than channel groups (so that no group is split twice).
     if (SSM_SCAN_CTAS_PER_SM > 0 && SSM_SCAN_CTAS_PER_SM < occ) occ = SSM_SCAN_CTAS_PER_SM;
-    int64_t ctas = (int64_t)occ * sms;
-    if (ctas > p.ngroups) ctas = p.ngroups;
+    int64_t per_sm = p.ngroups / sms;
+    if (per_sm > occ) per_sm = occ;
+    int64_t ctas = per_sm >= 1 ? per_sm * sms : p.ngroups;
     if (chunk > 0 && p.ntiles > 0) {   // caller-chosen work per CTA (>= one group's tokens)
         const int64_t per = (chunk + kTL - 1) / kTL;
         const int64_t want = (p.ngroups * p.ntiles + per - 1) / per;
         if (want < ctas) ctas = want;
     }
     if (ctas < 1) ctas = 1;
+    const ssm_dims own_dims = wl_dims(p, N);
+    const ScanWorkspace own = scan_workspace_for(&own_dims, Sh::CH);
     if (p.ntiles > 0) {
         p.status = reinterpret_cast<int*>(ws);
-        p.flags = reinterpret_cast<unsigned*>(ws + wl.flags_off);
-        p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
-        if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
+        p.flags = reinterpret_cast<unsigned*>(ws + own.flags_off);
+        p.carry = reinterpret_cast<float*>(ws + own.carry_off);
+        if (cudaMemsetAsync(ws, 0, own.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     }
     kern<<<(unsigned)ctas, kThreads, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename T, int N>
+template <typename T, int N, int S>
 int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
-                    unsigned char* ws, const ScanWorkspace& wl, cudaStream_t s) {
+                    unsigned char* ws, int sms, cudaStream_t s) {
 #define SSM_SCAN_CASE(Z, SP, V) \
-    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, Z, SP, V>(p, chunk, ws, wl, s);
+    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, S, Z, SP, V>(p, chunk, ws, sms, s);
     SSM_SCAN_CASE(false, false, false)
     SSM_SCAN_CASE(false, false, true)
     SSM_SCAN_CASE(false, true, false)
@@ -176,14 +252,17 @@ int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bo
 }
 
 template <typename T>
-int dispatch_scan(const ssm::ScanParams& p, int64_t n, int64_t chunk, bool z, bool sp, bool vec,
-                  unsigned char* ws, const ScanWorkspace& wl, cudaStream_t s) {
-    switch (n) {
-        case 1: return dispatch_scan_n<T, 1>(p, chunk, z, sp, vec, ws, wl, s);
-        case 2: return dispatch_scan_n<T, 2>(p, chunk, z, sp, vec, ws, wl, s);
-        case 4: return dispatch_scan_n<T, 4>(p, chunk, z, sp, vec, ws, wl, s);
-        case 8: return dispatch_scan_n<T, 8>(p, chunk, z, sp, vec, ws, wl, s);
-        case 16: return dispatch_scan_n<T, 16>(p, chunk, z, sp, vec, ws, wl, s);
+int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool z, bool sp, bool vec,
+                  unsigned char* ws, int sms, cudaStream_t s) {
+    const int64_t chunk = d->chunk;
+    switch (d->dstate) {
+        case 1: return dispatch_scan_n<T, 1, 1>(p, chunk, z, sp, vec, ws, sms, s);
+        case 2: return dispatch_scan_n<T, 2, 2>(p, chunk, z, sp, vec, ws, sms, s);
+        case 4: return dispatch_scan_n<T, 4, 4>(p, chunk, z, sp, vec, ws, sms, s);
+        case 8: return dispatch_scan_n<T, 8, 8>(p, chunk, z, sp, vec, ws, sms, s);
+        case 16:
+            if (n16_split(d, sms) == 8) return dispatch_scan_n<T, 16, 8>(p, chunk, z, sp, vec, ws, sms, s);
+            return dispatch_scan_n<T, 16, 4>(p, chunk, z, sp, vec, ws, sms, s);
     }
     return SSM_ERR_UNSUPPORTED_N;
 }
@@ -314,9 +393,18 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
     const bool sp = delta_softplus != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
+    int sms = 0;
+    if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
+    if (vec && tc_shape(dims)) {
+        const bool zz = z != nullptr;
+        if (zz && sp) return launch_scan_tc<true, true>(p, dims->chunk, ws, st);
+        if (zz) return launch_scan_tc<true, false>(p, dims->chunk, ws, st);
+        if (sp) return launch_scan_tc<false, true>(p, dims->chunk, ws, st);
+        return launch_scan_tc<false, false>(p, dims->chunk, ws, st);
+    }
     if (dims->io == SSM_IO_BF16)
-        return dispatch_scan<bf16>(p, dims->dstate, dims->chunk, z != nullptr, sp, vec, ws, wl, st);
-    return dispatch_scan<float>(p, dims->dstate, dims->chunk, z != nullptr, sp, vec, ws, wl, st);
+        return dispatch_scan<bf16>(dims, p, z != nullptr, sp, vec, ws, sms, st);
+    return dispatch_scan<float>(dims, p, z != nullptr, sp, vec, ws, sms, st);
 }
 
 int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void* delta,

@@ -220,3 +220,70 @@ def test_default_schedule_splits_large_problem():
     idx = torch.from_numpy(chans).cuda()
     assert_close(as64(y.reshape(-1, w.seqlen)[idx]), y_ref, torch.bfloat16, "y")
     assert_close(as64(h.reshape(-1, w.dstate)[idx]), h_ref, torch.bfloat16, "last_state")
+
+
+# -- bf16 I/O, N = 16, L a multiple of 8: the shapes the tensor-core kernel takes --
+TC = Workload("tc", 2, 200, 16, 256, "bf16", bias_range=(-4.0, -2.0),
+              a_kind="neg_exp_uniform", gate=True)
+
+
+@pytest.mark.parametrize("L", [8, 16, 40, 256, 808])
+@pytest.mark.parametrize("dim", [1, 127, 128, 129, 300])
+def test_tc_shapes(L, dim):
+    check_full(TC.scaled(seqlen=L, dim=dim, batch=1 if dim > 128 else 3), seed=L * 7 + dim)
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("softplus", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+@pytest.mark.parametrize("skip", [False, True])
+def test_tc_options(gate, softplus, bias, skip):
+    w = TC.scaled(gate=gate, softplus=softplus, skip=skip,
+                  bias_range=(-4.0, -2.0) if bias else None)
+    inp = make_scan_inputs(w, seed=13)
+    if not softplus:
+        inp["delta"] = (inp["delta"].float().abs() * 0.1).to(torch.bfloat16)
+        if inp["delta_bias"] is not None:
+            inp["delta_bias"] = inp["delta_bias"].abs() * 0.01
+    y, h = gpu_scan(inp)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.bfloat16, "y")
+    assert_close(as64(h), h_ref, torch.bfloat16, "last_state")
+
+
+@pytest.mark.parametrize("frac", [1.0, 1.4, 3.0])
+def test_tc_split_groups(frac):
+    """Channel groups of 128 split between CTAs (chunk caps the tokens per CTA)."""
+    w = TC.scaled(batch=3, dim=300, seqlen=800)
+    inp = make_scan_inputs(w, seed=17)
+    y, h = gpu_scan(inp, chunk=int(frac * w.seqlen))
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.bfloat16, "y")
+    assert_close(as64(h), h_ref, torch.bfloat16, "last_state")
+
+
+def test_tc_schedule_bitwise_invariant():
+    w = TC.scaled(batch=2, dim=256, seqlen=512)
+    inp = make_scan_inputs(w, seed=19)
+    y0, h0 = gpu_scan(inp)
+    for chunk in (512, 700, 1100, 2048):
+        y1, h1 = gpu_scan(inp, chunk=chunk)
+        assert torch.equal(y0, y1) and torch.equal(h0, h1), chunk
+
+
+def test_tc_causality_bitwise():
+    w = TC.scaled(seqlen=320)
+    inp = make_scan_inputs(w, seed=23)
+    y0, _ = gpu_scan(inp)
+    t0 = 168
+    pert = dict(inp)
+    for k in ("u", "delta", "z"):
+        t = inp[k].clone()
+        t[..., t0:] = t[..., t0:] * -3.0 + 1.0
+        pert[k] = t
+    B = inp["B"].clone()
+    B[:, t0:] += 1.0
+    pert["B"] = B
+    y1, _ = gpu_scan(pert)
+    assert torch.equal(y0[..., :t0], y1[..., :t0])
+    assert not torch.equal(y0[..., t0:], y1[..., t0:])
