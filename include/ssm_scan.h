@@ -86,13 +86,20 @@ typedef struct ssm_dims {
     int64_t dstate;  /* N in {1, 2, 4, 8, 16}: state entries per channel */
     int64_t seqlen;  /* L >= 0: tokens */
     int32_t io;      /* ssm_io_dtype of u, delta, z, B, C, y */
-    int32_t chunk;   /* ssm_scan_fwd only.  0: library default schedule.
-                        Otherwise a cap on the work of one CTA, in tokens of a
-                        channel group, at least seqlen: the scan then runs on
-                        at most ceil(groups * seqlen / chunk) CTAs, splitting a
-                        group's tokens between two CTAs where the ranges fall.
-                        It changes only the schedule: the arithmetic of every
-                        channel is the same, so outputs are bitwise equal. */
+    int32_t chunk;   /* ssm_scan_fwd only; >= 0.  0: library default schedule.
+                        chunk >= seqlen: a cap on the work of one CTA, in
+                        tokens of a channel group: the scan then runs on at most
+                        ceil(groups * seqlen / chunk) CTAs, splitting a group's
+                        tokens between two CTAs where the ranges fall.  Every
+                        channel's arithmetic is unchanged: outputs are bitwise
+                        equal to the default schedule's.
+                        0 < chunk < seqlen: the chunked schedule, with chunks of
+                        chunk tokens (rounded up to 32): the chunks of a
+                        sequence are scanned in parallel from zero, their affine
+                        maps composed into carry-ins, and scanned again from
+                        those; outputs agree up to fp32 rounding order.  The
+                        default schedule takes it by itself for long sequences
+                        over few channels. */
 } ssm_dims;
 
 /*

@@ -51,6 +51,21 @@ struct ScanParams {
     int* status;
     unsigned* flags;
     float* carry;
+    // chunked (L-parallel) schedule: chunks of tiles_per_chunk tiles; per
+    // (group, chunk) unit the aggregate state / carry-in [CH][N] and the sum
+    // of Delta per channel [CH]
+    int64_t nchunks, tiles_per_chunk;
+    float* agg;
+    float* dsum;
+};
+
+// How one part of a channel group starts and ends.
+struct PartIO {
+    int init;            // 0: zero state, 1: handed over (flag + carry), 2: from h0
+    const float* h0;     // [CH][N] initial state when init == 2
+    float* hout;         // [CH][N] final state (chunk aggregate), or null
+    float* dsum;         // [CH] sum of Delta over the part, or null
+    bool handoff;        // a part ending inside its group hands the state on (flag + carry)
 };
 
 // Value a kernel leaves in the workspace status word when a bounded wait
@@ -263,9 +278,45 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag) {
     return false;
 }
 
-template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC>
+// One token for one thread without the output sum (the aggregate pass of the
+// chunked schedule needs only the final state).
+template <int S>
+__device__ __forceinline__ void token_state(float dt, float dtx, const float* __restrict__ bc,
+                                            float (&h)[S], const float (&A2)[S]) {
+    float Bv[S];
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int n = 0; n < S; n += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
+            Bv[n] = b4.x; Bv[n + 1] = b4.y; Bv[n + 2] = b4.z; Bv[n + 3] = b4.w;
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < S; n++) Bv[n] = bc[n];
+    }
+    if constexpr (S == 1) {
+        h[0] = fmaf(ex2(dt * A2[0]), h[0], dtx * Bv[0]);
+    } else {
+        const float2 dt2 = make_float2(dt, dt);
+        const float2 dtx2 = make_float2(dtx, dtx);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
+            const float2 a = make_float2(ex2(e.x), ex2(e.y));
+            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+        }
+    }
+}
+
+// Tiles [tb, te) of channel group `grp`.  AGG: the aggregate pass of the
+// chunked schedule (no output; the final state and the sum of Delta go to
+// part.hout / part.dsum).
+template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC, bool AGG = false>
 __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* smem, int64_t grp,
-                                          int64_t tb, int64_t te, int* s_ok) {
+                                          int64_t tb, int64_t te, int* s_ok, const PartIO& part) {
     using Sh = Shape<T, N, S, HAS_Z>;
     constexpr int G = Sh::G, CH = Sh::CH;
 
@@ -306,7 +357,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         const int64_t t0 = tile * kTL;
         load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0);
         load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0);
-        if constexpr (HAS_Z)
+        if constexpr (HAS_Z && !AGG)
             load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0);
         unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
         load_bc<T, N, VEC>(bcraw, gB, L, t0);
@@ -317,10 +368,14 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     load_tile(tb, 0);
     cp_async_commit();
 
-    // initial state: zero at the sequence start, else the carry handed over
-    if (tb == 0) {
+    // initial state: zero, given, or the carry handed over by another CTA
+    if (part.init == 0) {
 #pragma unroll
         for (int j = 0; j < S; j++) h[j] = 0.0f;
+    } else if (part.init == 2) {
+        const float* src = part.h0 + ch * N + g * S;
+#pragma unroll
+        for (int j = 0; j < S; j++) h[j] = __ldcg(src + j);
     } else {
         if (threadIdx.x == 0) {
             const bool ok = wait_flag(p.flags + grp);
@@ -335,6 +390,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         for (int j = 0; j < S; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
     }
 
+    float dsum = 0.0f, dcomp = 0.0f;   // sum of Delta over the part (compensated)
     for (int64_t tile = tb; tile < te; tile++) {
         const int slot = (int)((tile - tb) & 1);
         if (tile + 1 < te) load_tile(tile + 1, slot ^ 1);
@@ -399,7 +455,21 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         __syncthreads();
 
         // ---- recurrence over the tile ----
-        {
+        if constexpr (AGG) {
+            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
+            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
+            float tsum = 0.0f;
+#pragma unroll 2
+            for (int t = 0; t < kTL; t += 2) {
+                const float4 w = wrow[t / 2];
+                token_state<S>(w.x, w.y, bcf + (t + 0) * G * 2 * S, h, A2);
+                token_state<S>(w.z, w.w, bcf + (t + 1) * G * 2 * S, h, A2);
+                tsum += w.x + w.z;
+            }
+            const float yk = tsum - dcomp, tk = dsum + yk;
+            dcomp = (tk - dsum) - yk;
+            dsum = tk;
+        } else {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
             float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
@@ -419,7 +489,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 
         // ---- epilogue: y = (sum of partials + D u) * silu(z) ----
 #pragma unroll
-        for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
+        for (int it = 0; it < (AGG ? 0 : Sh::CHUNK_ITERS); it++) {
             int r, q;
             chunk_of<CH>(it, r, q);
             float ys[8];
@@ -456,13 +526,18 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         __syncthreads();
     }
 
-    if (te == p.ntiles) {
+    if (part.hout) {   // chunk aggregate: final state from zero and the Delta sum
+        float* dst = part.hout + ch * N + g * S;
+#pragma unroll
+        for (int j = 0; j < S; j++) dst[j] = h[j];
+        if (g == 0) part.dsum[ch] = dsum;
+    } else if (te == p.ntiles) {
         if (active && p.last_state) {
             float* dst = p.last_state + (row0 + ch) * N + g * S;
 #pragma unroll
             for (int j = 0; j < S; j++) dst[j] = h[j];
         }
-    } else {
+    } else if (part.handoff) {
         // hand the state over to the CTA that scans the rest of this group
         float* dst = p.carry + (grp * CH + ch) * N + g * S;
 #pragma unroll
@@ -486,6 +561,19 @@ template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC>
 __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
+    if (p.nchunks > 0) {   // pass 3 of the chunked schedule (see scan_chunk_agg_kernel)
+        using Sh = Shape<T, N, S, HAS_Z>;
+        const int64_t units = p.ngroups * p.nchunks;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            const int64_t grp = u / p.nchunks, ck = u % p.nchunks;
+            const int64_t tb = ck * p.tiles_per_chunk;
+            const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
+            const PartIO io{ck == 0 ? 0 : 2, p.agg + u * Sh::CH * N, nullptr, nullptr, false};
+            scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok, io);
+            __syncthreads();
+        }
+        return;
+    }
     const int64_t W = p.ngroups * p.ntiles;
     const int64_t s = W * blockIdx.x / gridDim.x;
     const int64_t e = W * (blockIdx.x + 1) / gridDim.x;
@@ -507,7 +595,59 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
         const int64_t lo = grp * p.ntiles;
         const int64_t tb = (s > lo ? s : lo) - lo;
         const int64_t te = (e < lo + p.ntiles ? e : lo + p.ntiles) - lo;
-        scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok);
+        const PartIO io{tb == 0 ? 0 : 1, nullptr, nullptr, nullptr, true};
+        scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok, io);
+    }
+}
+
+// Chunked (L-parallel) schedule for problems with too few channel groups to
+// fill the GPU (a long sequence over few channels).  The token range of every
+// group is cut into chunks, and the affine maps h -> a h + b of the steps
+// compose associatively ((a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2)), so:
+//   pass 1  every (group, chunk) unit scans its chunk from a zero state: the
+//           final state is the chunk's b; its a is exp(A sum Delta)
+//           (scan_chunk_agg_kernel)
+//   pass 2  per (channel, state) a sequential scan over the chunks composes
+//           them into each chunk's carry-in (scan_chunk_carry_kernel)
+//   pass 3  every unit scans its chunk again from its carry-in and writes y
+//           and, for the last chunk, last_state (scan_fwd_kernel with
+//           p.nchunks > 0).
+// Passes 1 and 3 are independent over units: grid-stride loops of
+// persistent CTAs.  The price is a second pass over the inputs (no z, no y).
+template <typename T, int N, int S, bool SOFTPLUS, bool VEC>
+__global__ void __launch_bounds__(kThreads, 2) scan_chunk_agg_kernel(ScanParams p) {
+    using Sh = Shape<T, N, S, false>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_ok;
+    const int64_t units = p.ngroups * p.nchunks;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int64_t grp = u / p.nchunks, ck = u % p.nchunks;
+        const int64_t tb = ck * p.tiles_per_chunk;
+        const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
+        const PartIO io{0, nullptr, p.agg + u * Sh::CH * N, p.dsum + u * Sh::CH, false};
+        scan_part<T, N, S, false, SOFTPLUS, VEC, true>(p, smem, grp, tb, te, &s_ok, io);
+        __syncthreads();
+    }
+}
+
+// Pass 2: one thread per (group, channel, state) walks the chunks in order,
+// replacing each chunk's aggregate state by its carry-in.
+template <int N, int CH>
+__global__ void scan_chunk_carry_kernel(ScanParams p) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= p.ngroups * CH * N) return;
+    const int64_t grp = idx / (CH * N);
+    const int rem = (int)(idx % (CH * N)), ch = rem / N, n = rem % N;
+    const int64_t d = (grp % p.groups_per_row) * CH + ch;
+    const float A2 = d < p.dim ? p.A[d * N + n] * kLog2e : 0.0f;
+    float carry = 0.0f;
+    for (int64_t ck = 0; ck < p.nchunks; ck++) {
+        const int64_t u = grp * p.nchunks + ck;
+        float* st = p.agg + (u * CH + ch) * N + n;
+        const float b = *st;                          // the chunk's state from zero
+        const float a = ex2(A2 * p.dsum[u * CH + ch]);   // prod of exp(Delta A) over the chunk
+        *st = carry;                                  // the state entering the chunk
+        carry = fmaf(a, carry, b);
     }
 }
 

@@ -49,13 +49,13 @@
 namespace ssm {
 namespace tc {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 state quarters x 4 tensor-memory lane quarters
 constexpr int kCH = 128;        // channels per group = tensor-memory lanes = MMA M
 constexpr int kN = 16;          // states
-constexpr int kTB = 8;          // tokens per block
+constexpr int kTB = 8;          // tokens per block (one MMA pair, one pipeline step)
+constexpr int kTT = 32;         // tokens per raw input tile (4 blocks)
 constexpr int kNSLOT = 4;       // operand slots (A1, W, Bexp, Cexp)
-constexpr int kNRAW = 8;        // raw input blocks in flight
-constexpr int kLeadRaw = 6;     // the raw inputs of block k + 6 are requested at step k
+constexpr int kNTILE = 3;       // raw input tiles in flight
 constexpr int kTmemCols = 512;  // 2 buffers x (128 bb + 128 Cb) columns
 
 // Operands are K-major without swizzle: 8 x 16-byte core matrices, the next
@@ -63,19 +63,23 @@ constexpr int kTmemCols = 512;  // 2 buffers x (128 bb + 128 Cb) columns
 __host__ __device__ constexpr int kmaj(int row, int k) {
     return (row >> 3) * 256 + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4;
 }
+// Column (= Bexp / Cexp row) of token t, state n within a block: each thread's
+// 4 states x 8 tokens are 32 consecutive columns.
+__host__ __device__ constexpr int bcol(int t, int n) { return (n >> 2) * 32 + t * 4 + (n & 3); }
 constexpr int kOpBytes = 128 * kTB * 4;     // one 128 x 8 tf32 operand
 constexpr int kSlotBytes = 4 * kOpBytes;    // A1 = Delta u, W = Delta, Bexp, Cexp
 constexpr int kOffW = kOpBytes, kOffBexp = 2 * kOpBytes, kOffCexp = 3 * kOpBytes;
 constexpr int kYRow = 48;                   // 8 fp32 partial sums + 16 bytes of padding
-constexpr int kYBytes = 2 * kCH * kYRow;    // both state halves
-constexpr int kRawPlane = kCH * 16;         // 128 channels x 8 bf16
-constexpr int kRawBC = kTB * kN * 2;        // 8 tokens x 16 states bf16
-constexpr int kRawBytes = 3 * kRawPlane + 2 * kRawBC;
+constexpr int kYBytes = 4 * kCH * kYRow;    // the four state quarters
+constexpr int kRawRow = kTT * 2 + 16;       // one channel's 32 bf16 tokens, padded
+constexpr int kRawPlane = kCH * kRawRow;
+constexpr int kRawBC = kTT * kN * 2;        // 32 tokens x 16 states bf16
+constexpr int kTileBytes = 3 * kRawPlane + 2 * kRawBC;
 constexpr int kOffOnes = kNSLOT * kSlotBytes;
 constexpr int kOffY = kOffOnes + kOpBytes;
 constexpr int kOffRaw = kOffY + 2 * kYBytes;
-constexpr int kSmem = kOffRaw + kNRAW * kRawBytes;
-static_assert(kSmem <= 227 * 1024, "shared memory");
+constexpr int kSmem = kOffRaw + kNTILE * kTileBytes;
+static_assert(kSmem <= 226 * 1024, "shared memory");
 
 // instruction descriptor, kind::tf32, fp32 accumulate, both operands K-major
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -186,7 +190,7 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
                                         int64_t grp, int64_t b0, int64_t b1, uint32_t& S) {
     using bf16 = __nv_bfloat16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, g = warp >> 2;
+    const int q = warp & 3, s4 = warp >> 2;
     const int c = q * 32 + lane;                       // this thread's channel in the group
     const int64_t b = grp / p.groups_per_row;
     const int64_t d0 = (grp % p.groups_per_row) * kCH;
@@ -203,29 +207,36 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
     const bf16* gC = static_cast<const bf16*>(p.C) + b * L * kN;
     bf16* gy = static_cast<bf16*>(p.y);
 
-    float A2[8], h[8];
+    float A2[4], h[4];
 #pragma unroll
-    for (int j = 0; j < 8; j++)   // exp(Delta A) = 2^(Delta A log2 e)
-        A2[j] = active ? p.A[(d0 + c) * kN + g * 8 + j] * kLog2e : 0.0f;
+    for (int j = 0; j < 4; j++)   // exp(Delta A) = 2^(Delta A log2 e)
+        A2[j] = active ? p.A[(d0 + c) * kN + s4 * 4 + j] * kLog2e : 0.0f;
     float bias = (active && p.bias) ? p.bias[d0 + c] : 0.0f;
     if (SOFTPLUS) bias *= kLog2e;
     const float Dv = (active && p.D) ? p.D[d0 + c] : 0.0f;
 
-    // raw inputs of block kb into ring slot kb % kNRAW (zero past the last channel)
-    auto load_raw = [&](int kb) {
-        unsigned char* r = smem + kOffRaw + (kb % kNRAW) * kRawBytes;
-        const int64_t t0 = (b0 + kb) * kTB;
+    // raw inputs of tile j (blocks 4j .. 4j+3) into ring slot j % kNTILE,
+    // 64 bytes per channel row; zero past the last channel
+    auto load_tile = [&](int j) {
+        unsigned char* r = smem + kOffRaw + (j % kNTILE) * kTileBytes;
+        const int kb0 = 4 * j;
+        const int nblk = nb - kb0 < 4 ? nb - kb0 : 4;     // blocks of this tile in the part
+        const int64_t t0 = (b0 + kb0) * kTB;
         const int nplanes = HAS_Z ? 3 : 2;
-        for (int i = tid; i < nplanes * kCH; i += kThreads) {
-            const int pl = i / kCH, ch = i % kCH;
+        // one 16-byte chunk (8 bf16 tokens) per block: chunk ck of a row is
+        // block 4j + ck, present only for ck < nblk
+        for (int i = tid; i < nplanes * kCH * 4; i += kThreads) {
+            const int pl = i / (kCH * 4), rem = i % (kCH * 4), ch = rem >> 2, ck = rem & 3;
+            if (ck >= nblk) continue;
             const bf16* src = pl == 0 ? gu : (pl == 1 ? gdl : gz);
             const bool ok = ch < rows;
-            ssm::seq::cp_async16(r + pl * kRawPlane + ch * 16,
-                                 ok ? static_cast<const void*>(src + (row0 + ch) * L + t0) : src,
+            ssm::seq::cp_async16(r + pl * kRawPlane + ch * kRawRow + ck * 16,
+                                 ok ? static_cast<const void*>(src + (row0 + ch) * L + t0 + ck * 8)
+                                    : src,
                                  ok ? 16 : 0);
         }
-        if (tid < 32) {   // B, C: 8 tokens x 16 states each = 16 chunks of 16 bytes
-            const int which = tid / 16, e = (tid % 16) * 8;
+        for (int i = tid; i < 2 * nblk * 16; i += kThreads) {   // B, C: 16 chunks per block
+            const int which = i / (nblk * 16), e = (i % (nblk * 16)) * 8;
             const bf16* src = (which == 0 ? gB : gC) + t0 * kN + e;
             ssm::seq::cp_async16(r + 3 * kRawPlane + which * kRawBC + e * 2, src, 16);
         }
@@ -234,7 +245,7 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
     // initial state: zero, or the state handed over by the CTA before
     if (b0 == 0) {
 #pragma unroll
-        for (int j = 0; j < 8; j++) h[j] = 0.0f;
+        for (int j = 0; j < 4; j++) h[j] = 0.0f;
     } else {
         if (tid == 0) {
             const bool ok = ssm::seq::wait_flag(p.flags + grp);
@@ -244,32 +255,30 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
         }
         __syncthreads();
         const bool ok = sh.ok;
-        const float* src = p.carry + (grp * kCH + c) * kN + g * 8;
+        const float* src = p.carry + (grp * kCH + c) * kN + s4 * 4;
 #pragma unroll
-        for (int j = 0; j < 8; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
+        for (int j = 0; j < 4; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
     }
 
-    // raw inputs of blocks 0..2 (step k requests block k + 6; blocks 0..2
-    // belong to the steps before the first one); one cp.async group per block
-    for (int kb = 0; kb < kLeadRaw - 3; kb++) {
-        if (kb < nb) load_raw(kb);
-        ssm::seq::cp_async_commit();
-    }
+    // Tile j is requested at step 4j - 7 (tile 0 before the first step) and
+    // first read at step 4j - 3; one cp.async group per step, so at every
+    // step all but the three newest groups must be complete.
+    load_tile(0);
+    ssm::seq::cp_async_commit();
+    for (int i = 0; i < 3; i++) ssm::seq::cp_async_commit();
 
     const uint32_t tbase = sh.taddr;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
     for (int k = -3; k < nb; k++, S++) {
-        asm volatile("cp.async.wait_group 2;\n" ::: "memory");
+        asm volatile("cp.async.wait_group 3;\n" ::: "memory");
 
-        // ---- recurrence of block k ----
+        // ---- recurrence of block k: states 4 s4 .. 4 s4 + 3 ----
         if (k >= 0) {
-            const uint32_t col = tbase + lane_base + (uint32_t)((k & 1) * 256 + g * 64);
-            uint32_t v[64], cv[64];
+            const uint32_t col = tbase + lane_base + (uint32_t)((k & 1) * 256 + s4 * 32);
+            uint32_t v[32], cv[32];
             SSM_TMEM_LD32(col, v, 0);
-            SSM_TMEM_LD32(col + 32, v, 32);
             SSM_TMEM_LD32(col + 128, cv, 0);
-            SSM_TMEM_LD32(col + 160, cv, 32);
             const unsigned char* wsl = smem + (k % kNSLOT) * kSlotBytes + kOffW;
             const float4 dA = *reinterpret_cast<const float4*>(wsl + kmaj(c, 0));
             const float4 dB = *reinterpret_cast<const float4*>(wsl + kmaj(c, 4));
@@ -279,37 +288,38 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
 #pragma unroll
             for (int t = 0; t < kTB; t++) {
                 const float2 dt2 = make_float2(dts[t], dts[t]);
-                float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    const float2 e = __fmul2_rn(dt2, make_float2(A2[j], A2[j + 1]));
-                    const float2 a = make_float2(ex2(e.x), ex2(e.y));
-                    const float2 bb = make_float2(__uint_as_float(v[t * 8 + j]),
-                                                  __uint_as_float(v[t * 8 + j + 1]));
-                    const float2 hn = __ffma2_rn(a, make_float2(h[j], h[j + 1]), bb);
-                    h[j] = hn.x;
-                    h[j + 1] = hn.y;
-                    acc = __ffma2_rn(make_float2(__uint_as_float(cv[t * 8 + j]),
-                                                 __uint_as_float(cv[t * 8 + j + 1])),
-                                     hn, acc);
-                }
+                const float2 e0 = __fmul2_rn(dt2, make_float2(A2[0], A2[1]));
+                const float2 e1 = __fmul2_rn(dt2, make_float2(A2[2], A2[3]));
+                const float2 a0 = make_float2(ex2(e0.x), ex2(e0.y));
+                const float2 a1 = make_float2(ex2(e1.x), ex2(e1.y));
+                const float2 h0 = __ffma2_rn(a0, make_float2(h[0], h[1]),
+                                             make_float2(__uint_as_float(v[t * 4]),
+                                                         __uint_as_float(v[t * 4 + 1])));
+                const float2 h1 = __ffma2_rn(a1, make_float2(h[2], h[3]),
+                                             make_float2(__uint_as_float(v[t * 4 + 2]),
+                                                         __uint_as_float(v[t * 4 + 3])));
+                h[0] = h0.x; h[1] = h0.y; h[2] = h1.x; h[3] = h1.y;
+                float2 acc = __fmul2_rn(make_float2(__uint_as_float(cv[t * 4]),
+                                                    __uint_as_float(cv[t * 4 + 1])), h0);
+                acc = __ffma2_rn(make_float2(__uint_as_float(cv[t * 4 + 2]),
+                                             __uint_as_float(cv[t * 4 + 3])), h1, acc);
                 yp[t] = acc.x + acc.y;
             }
             float4* ydst = reinterpret_cast<float4*>(smem + kOffY + (k & 1) * kYBytes +
-                                                     (g * kCH + c) * kYRow);
+                                                     (s4 * kCH + c) * kYRow);
             ydst[0] = make_float4(yp[0], yp[1], yp[2], yp[3]);
             ydst[1] = make_float4(yp[4], yp[5], yp[6], yp[7]);
             if (k == nb - 1) {   // the part's final state
                 if (b1 * kTB == L) {
                     if (active && p.last_state) {
-                        float* dst = p.last_state + (row0 + c) * kN + g * 8;
+                        float* dst = p.last_state + (row0 + c) * kN + s4 * 4;
 #pragma unroll
-                        for (int j = 0; j < 8; j++) dst[j] = h[j];
+                        for (int j = 0; j < 4; j++) dst[j] = h[j];
                     }
                 } else {
-                    float* dst = p.carry + (grp * kCH + c) * kN + g * 8;
+                    float* dst = p.carry + (grp * kCH + c) * kN + s4 * 4;
 #pragma unroll
-                    for (int j = 0; j < 8; j++) __stcg(dst + j, h[j]);
+                    for (int j = 0; j < 4; j++) __stcg(dst + j, h[j]);
                     __threadfence();
                 }
             }
@@ -341,13 +351,14 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
         }
 
         const int k3 = k + 3;
-        if (g == 0) {
+        if (s4 == 0) {
             // ---- prologue of block k+3: Delta and Delta u ----
             if (k3 < nb) {
-                const unsigned char* r = smem + kOffRaw + (k3 % kNRAW) * kRawBytes;
+                const unsigned char* r = smem + kOffRaw + ((k3 >> 2) % kNTILE) * kTileBytes +
+                                         c * kRawRow + (k3 & 3) * 16;
                 float uv[8], dv[8];
-                ssm::seq::unpack8<bf16>(r + c * 16, uv);
-                ssm::seq::unpack8<bf16>(r + kRawPlane + c * 16, dv);
+                ssm::seq::unpack8<bf16>(r, uv);
+                ssm::seq::unpack8<bf16>(r + kRawPlane, dv);
                 float dt[8], du[8];
 #pragma unroll
                 for (int t = 0; t < 8; t++) {
@@ -361,53 +372,65 @@ __device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem
                 *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 0)) = make_float4(dt[0], dt[1], dt[2], dt[3]);
                 *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 4)) = make_float4(dt[4], dt[5], dt[6], dt[7]);
             }
-        } else {
+        } else if (s4 == 1) {
             // ---- B and C of block k+3 onto their block diagonals ----
             if (k3 < nb) {
-                const unsigned char* r = smem + kOffRaw + (k3 % kNRAW) * kRawBytes + 3 * kRawPlane;
+                const unsigned char* r = smem + kOffRaw + ((k3 >> 2) % kNTILE) * kTileBytes +
+                                         3 * kRawPlane + (k3 & 3) * 256;
                 unsigned char* sl = smem + (k3 % kNSLOT) * kSlotBytes;
                 const int i = c;                   // one B and one C value per thread
-                const int t = i >> 4, n = i & 15, gg = n >> 3, j = n & 7;
-                const int row = gg * 64 + t * 8 + j;
+                const int t = i >> 4, n = i & 15;
+                const int row = bcol(t, n);
                 const float bv = __bfloat162float(reinterpret_cast<const bf16*>(r)[i]);
                 const float cv = __bfloat162float(reinterpret_cast<const bf16*>(r + kRawBC)[i]);
                 *reinterpret_cast<float*>(sl + kOffBexp + kmaj(row, t)) = bv;
                 *reinterpret_cast<float*>(sl + kOffCexp + kmaj(row, 0)) = cv;
             }
-            // ---- output of block k ----
-            if (k >= 0) {
-                const unsigned char* yb = smem + kOffY + (k & 1) * kYBytes;
-                const float4 a0 = *reinterpret_cast<const float4*>(yb + c * kYRow);
-                const float4 a1 = *reinterpret_cast<const float4*>(yb + c * kYRow + 16);
-                const float4 c0 = *reinterpret_cast<const float4*>(yb + (kCH + c) * kYRow);
-                const float4 c1 = *reinterpret_cast<const float4*>(yb + (kCH + c) * kYRow + 16);
-                float ys[8] = {a0.x + c0.x, a0.y + c0.y, a0.z + c0.z, a0.w + c0.w,
-                               a1.x + c1.x, a1.y + c1.y, a1.z + c1.z, a1.w + c1.w};
-                const unsigned char* r = smem + kOffRaw + (k % kNRAW) * kRawBytes;
-                float uv[8];
-                ssm::seq::unpack8<bf16>(r + c * 16, uv);
+        } else if (k >= 0) {
+            // ---- output of block k: tokens 4 (s4 - 2) .. + 3 of channel c ----
+            const int half = s4 - 2;
+            const unsigned char* yb = smem + kOffY + (k & 1) * kYBytes + c * kYRow + half * 16;
+            float4 acc = *reinterpret_cast<const float4*>(yb);
 #pragma unroll
-                for (int t = 0; t < 8; t++) ys[t] = fmaf(Dv, uv[t], ys[t]);
-                if constexpr (HAS_Z) {
-                    float zv[8];
-                    ssm::seq::unpack8<bf16>(r + 2 * kRawPlane + c * 16, zv);
+            for (int qq = 1; qq < 4; qq++) {
+                const float4 a = *reinterpret_cast<const float4*>(yb + qq * kCH * kYRow);
+                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+            }
+            float ys[4] = {acc.x, acc.y, acc.z, acc.w};
+            const unsigned char* r = smem + kOffRaw + ((k >> 2) % kNTILE) * kTileBytes +
+                                     c * kRawRow + (k & 3) * 16 + half * 8;
+            const uint2 uq = *reinterpret_cast<const uint2*>(r);
+            const float uv[4] = {__uint_as_float(uq.x << 16), __uint_as_float(uq.x & 0xffff0000u),
+                                 __uint_as_float(uq.y << 16), __uint_as_float(uq.y & 0xffff0000u)};
 #pragma unroll
-                    for (int t = 0; t < 8; t++) ys[t] *= ssm::seq::gate<bf16>(zv[t]);
-                }
-                if (active)
-                    ssm::seq::store8<bf16>(gy + (row0 + c) * L + (b0 + k) * kTB, ys);
+            for (int t = 0; t < 4; t++) ys[t] = fmaf(Dv, uv[t], ys[t]);
+            if constexpr (HAS_Z) {
+                const uint2 zq = *reinterpret_cast<const uint2*>(r + 2 * kRawPlane);
+                const float zv[4] = {__uint_as_float(zq.x << 16), __uint_as_float(zq.x & 0xffff0000u),
+                                     __uint_as_float(zq.y << 16), __uint_as_float(zq.y & 0xffff0000u)};
+#pragma unroll
+                for (int t = 0; t < 4; t++) ys[t] *= ssm::seq::gate<bf16>(zv[t]);
+            }
+            if (active) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(ys[0], ys[1]);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(ys[2], ys[3]);
+                uint2 o;
+                o.x = *reinterpret_cast<const unsigned*>(&lo);
+                o.y = *reinterpret_cast<const unsigned*>(&hi);
+                *reinterpret_cast<uint2*>(gy + (row0 + c) * L + (b0 + k) * kTB + half * 4) = o;
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
-        // ---- raw inputs of block k+6 ----
-        const int k6 = k + kLeadRaw;
-        if (k6 >= 0 && k6 < nb) load_raw(k6);
+        // ---- raw inputs of tile (k+7)/4 ----
+        if (((k + 7) & 3) == 0) {
+            const int j = (k + 7) >> 2;
+            if (j >= 1 && 4 * j < nb) load_tile(j);
+        }
         ssm::seq::cp_async_commit();
     }
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    // the last MMAs of the part (issued at steps nb-3, nb-2) were waited for
-    // at steps nb-2, nb-1
+    // the last MMAs of the part (issued at step nb-3) were waited for at step nb-2
     __syncthreads();
 }
 

@@ -60,7 +60,7 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
     if (dims->batch < 1 || dims->dim < 1 || dims->dstate < 1) return SSM_ERR_BAD_DIMS;
     if (scan && dims->seqlen < 0) return SSM_ERR_BAD_DIMS;
     if (!valid_n(dims->dstate)) return SSM_ERR_UNSUPPORTED_N;
-    if (scan && (dims->chunk < 0 || (dims->chunk > 0 && dims->chunk < dims->seqlen)))
+    if (scan && dims->chunk < 0)
         return SSM_ERR_BAD_DIMS;
     if (scan && dims->batch > 65535) return SSM_ERR_BAD_DIMS;  // grid.y limit of the scan launch
     const int64_t L = scan ? dims->seqlen : 1;
@@ -134,6 +134,51 @@ ScanWorkspace scan_workspace_for(const ssm_dims* d, int ch) {
     return w;
 }
 
+// The chunked (L-parallel) schedule: for problems with fewer than 64 groups
+// of the state-split kernel and at least 64 tiles per group, or whenever the
+// caller's `chunk` is below seqlen.  The plan depends only on the sizes, so
+// that the workspace size does too.  N = 16 uses 8 states per thread here
+// (the chunks supply the parallelism).
+struct ChunkPlan {
+    bool on = false;
+    int ch = 0;                     // channels per group
+    int64_t groups = 0, ntiles = 0, tpc = 0, nchunks = 0;
+};
+
+ChunkPlan chunk_plan(const ssm_dims* d) {
+    ChunkPlan c;
+    if (d->seqlen <= 0) return c;
+    const int n = (int)d->dstate;
+    c.ch = seq_channels(n, n <= 8 ? n : 8);
+    c.groups = d->batch * ((d->dim + c.ch - 1) / c.ch);
+    c.ntiles = (d->seqlen + ssm::seq::kTL - 1) / ssm::seq::kTL;
+    if (d->chunk > 0 && d->chunk < d->seqlen) {
+        c.tpc = (d->chunk + ssm::seq::kTL - 1) / ssm::seq::kTL;
+    } else if (d->chunk == 0 && c.groups < 64 && c.ntiles >= 64) {
+        const int64_t want_units = 2048;
+        c.tpc = (c.ntiles * c.groups + want_units - 1) / want_units;
+        if (c.tpc < 8) c.tpc = 8;
+    } else {
+        return c;
+    }
+    c.nchunks = (c.ntiles + c.tpc - 1) / c.tpc;
+    c.on = c.nchunks >= 2;
+    return c;
+}
+
+// workspace of the chunked schedule: header, per unit the aggregate state
+// (overwritten by the carry-in) and the Delta sums
+ScanWorkspace chunk_workspace(const ChunkPlan& c, int n) {
+    ScanWorkspace w{};
+    if (!c.on) return w;
+    const size_t units = (size_t)(c.groups * c.nchunks);
+    w.flags_off = 256;                                        // (no flags: the Delta sums)
+    w.carry_off = w.flags_off + round256(units * c.ch * 4);   // aggregate states
+    w.clear_bytes = 256;
+    w.total = w.carry_off + round256(units * c.ch * n * 4);
+    return w;
+}
+
 // The tensor-core kernel serves bf16 I/O with N = 16 when every row of the
 // (batch, dim, L) tensors is 16-byte aligned and L is a whole number of its
 // 8-token blocks; it groups 128 channels, the other kernel 64.
@@ -153,6 +198,8 @@ ScanWorkspace scan_workspace(const ssm_dims* d) {
         const ScanWorkspace t = scan_workspace_for(d, ssm::tc::kCH);
         if (t.total > w.total) w = t;
     }
+    const ScanWorkspace cw = chunk_workspace(chunk_plan(d), n);
+    if (cw.total > w.total) w = cw;
     return w;
 }
 
@@ -183,6 +230,56 @@ int launch_scan_tc(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStre
     p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
     if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     kern<<<(unsigned)ctas, kThreads, kSmem, stream>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// Number of CTAs of `kern` that fit on one SM (queried once per device).
+template <typename K>
+int occupancy(K kern, int smem, std::atomic<int>* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    int occ = cache[dev].load();
+    if (occ == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, ssm::seq::kThreads, smem) !=
+                cudaSuccess || occ < 1)
+            return -1;
+        cache[dev].store(occ);
+    }
+    return occ;
+}
+
+// Chunked schedule: the three passes on `stream`.
+template <typename T, int N, int S, bool Z, bool SP, bool VEC>
+int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int sms,
+                   cudaStream_t stream) {
+    using namespace ssm::seq;
+    using Sh = Shape<T, N, S, Z>;
+    using ShA = Shape<T, N, S, false>;
+    static_assert(Sh::CH == ShA::CH, "same channel groups in both passes");
+    auto agg = scan_chunk_agg_kernel<T, N, S, SP, VEC>;
+    auto full = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
+    static std::atomic<int> occ_agg[64], occ_full[64];
+    const int oa = occupancy(agg, ShA::SMEM, occ_agg), of = occupancy(full, Sh::SMEM, occ_full);
+    if (oa < 1 || of < 1) return SSM_ERR_CUDA;
+    p.groups_per_row = (p.dim + Sh::CH - 1) / Sh::CH;
+    p.ngroups = p.batch * p.groups_per_row;
+    p.ntiles = c.ntiles;
+    p.nchunks = c.nchunks;
+    p.tiles_per_chunk = c.tpc;
+    const ScanWorkspace wl = chunk_workspace(c, N);
+    p.status = reinterpret_cast<int*>(ws);
+    p.dsum = reinterpret_cast<float*>(ws + wl.flags_off);
+    p.agg = reinterpret_cast<float*>(ws + wl.carry_off);
+    const int64_t units = p.ngroups * p.nchunks;
+    if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    const int64_t ga = units < (int64_t)oa * sms ? units : (int64_t)oa * sms;
+    agg<<<(unsigned)ga, kThreads, ShA::SMEM, stream>>>(p);
+    const int64_t nthr = p.ngroups * Sh::CH * N;
+    scan_chunk_carry_kernel<N, Sh::CH><<<(unsigned)((nthr + 255) / 256), 256, 0, stream>>>(p);
+    const int64_t gf = units < (int64_t)of * sms ? units : (int64_t)of * sms;
+    full<<<(unsigned)gf, kThreads, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -251,10 +348,38 @@ int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bo
     return SSM_ERR_BAD_DIMS;
 }
 
+template <typename T, int N, int S>
+int dispatch_chunked_n(const ssm::ScanParams& p, const ChunkPlan& c, bool z, bool sp, bool vec,
+                       unsigned char* ws, int sms, cudaStream_t s) {
+#define SSM_CHUNK_CASE(Z, SP, V) \
+    if (z == Z && sp == SP && vec == V) return launch_chunked<T, N, S, Z, SP, V>(p, c, ws, sms, s);
+    SSM_CHUNK_CASE(false, false, false)
+    SSM_CHUNK_CASE(false, false, true)
+    SSM_CHUNK_CASE(false, true, false)
+    SSM_CHUNK_CASE(false, true, true)
+    SSM_CHUNK_CASE(true, false, false)
+    SSM_CHUNK_CASE(true, false, true)
+    SSM_CHUNK_CASE(true, true, false)
+    SSM_CHUNK_CASE(true, true, true)
+#undef SSM_CHUNK_CASE
+    return SSM_ERR_BAD_DIMS;
+}
+
 template <typename T>
 int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool z, bool sp, bool vec,
                   unsigned char* ws, int sms, cudaStream_t s) {
     const int64_t chunk = d->chunk;
+    const ChunkPlan cp = chunk_plan(d);
+    if (cp.on) {
+        switch (d->dstate) {
+            case 1: return dispatch_chunked_n<T, 1, 1>(p, cp, z, sp, vec, ws, sms, s);
+            case 2: return dispatch_chunked_n<T, 2, 2>(p, cp, z, sp, vec, ws, sms, s);
+            case 4: return dispatch_chunked_n<T, 4, 4>(p, cp, z, sp, vec, ws, sms, s);
+            case 8: return dispatch_chunked_n<T, 8, 8>(p, cp, z, sp, vec, ws, sms, s);
+            case 16: return dispatch_chunked_n<T, 16, 8>(p, cp, z, sp, vec, ws, sms, s);
+        }
+        return SSM_ERR_UNSUPPORTED_N;
+    }
     switch (d->dstate) {
         case 1: return dispatch_scan_n<T, 1, 1>(p, chunk, z, sp, vec, ws, sms, s);
         case 2: return dispatch_scan_n<T, 2, 2>(p, chunk, z, sp, vec, ws, sms, s);

@@ -75,8 +75,8 @@ def step(lib, d, state=P[0], x=P[1], delta=P[2], A=P[3], B=P[4], C=P[5], D=P[6],
     (dict(dstate=32), _lib.SSM_ERR_UNSUPPORTED_N),
     (dict(dstate=0), _lib.SSM_ERR_BAD_DIMS),
     (dict(io=7), _lib.SSM_ERR_BAD_DTYPE),
-    (dict(chunk=63), _lib.SSM_ERR_BAD_DIMS),     # below seqlen
     (dict(chunk=-64), _lib.SSM_ERR_BAD_DIMS),
+    (dict(chunk=-1), _lib.SSM_ERR_BAD_DIMS),
     (dict(batch=1 << 40, dim=1 << 40), _lib.SSM_ERR_BAD_DIMS),
     (dict(batch=70000), _lib.SSM_ERR_BAD_DIMS),
 ])

@@ -287,3 +287,50 @@ def test_tc_causality_bitwise():
     y1, _ = gpu_scan(pert)
     assert torch.equal(y0[..., :t0], y1[..., :t0])
     assert not torch.equal(y0[..., t0:], y1[..., t0:])
+
+
+# -- the chunked (L-parallel) schedule -----------------------------------------
+CHUNKED = Workload("chunked", 2, 70, 16, 1000, "f32", bias_range=(-4.0, -2.0),
+                   a_kind="neg_exp_uniform", gate=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("chunk", [32, 96, 300])
+def test_chunked_matches_oracle(io, N, chunk):
+    """chunk < L: the chunks are scanned from zero in parallel, composed into
+    carry-ins by a sequential pass over the chunks, and scanned again."""
+    w = CHUNKED.scaled(io=io, dstate=N)
+    inp = make_scan_inputs(w, seed=N + chunk)
+    y, h = gpu_scan(inp, chunk=chunk)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, w.torch_io, "y")
+    assert_close(as64(h), h_ref, w.torch_io, "last_state")
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("softplus", [False, True])
+@pytest.mark.parametrize("skip", [False, True])
+def test_chunked_options(gate, softplus, skip):
+    w = CHUNKED.scaled(gate=gate, softplus=softplus, skip=skip, seqlen=777)
+    inp = make_scan_inputs(w, seed=31)
+    if not softplus:
+        inp["delta"] = inp["delta"].abs() * 0.1
+        inp["delta_bias"] = inp["delta_bias"].abs() * 0.01
+    y, h = gpu_scan(inp, chunk=64)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.float32, "y")
+    assert_close(as64(h), h_ref, torch.float32, "last_state")
+
+
+def test_chunked_by_default_for_long_sequences():
+    """Few channels, long sequence: the default schedule takes the chunked path
+    (128 channels, L = 20000, DNA-like one-hot input)."""
+    w = WORKLOADS["dna"].scaled(dim=128, seqlen=20000)
+    inp = make_scan_inputs(w, seed=3)
+    y, h = gpu_scan(inp)
+    y_ref, h_ref = oracle_scan(inp)
+    assert_close(as64(y), y_ref, torch.float32, "y")
+    assert_close(as64(h), h_ref, torch.float32, "last_state")
+    y1, h1 = gpu_scan(inp, chunk=w.seqlen)   # one CTA range per group: no chunks
+    assert_close(as64(y1), y_ref, torch.float32, "y (unchunked)")
