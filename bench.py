@@ -255,7 +255,76 @@ def time_scan(w, steps, warmup, world, rank, local):
     total_ms = t0.elapsed_time(t1)
     per_launch_ms = [a.elapsed_time(b) for a, b in launches]
     return {"total_ms": total_ms, "launch_ms": per_launch_ms, "clocks": clk,
-            "launches_per_step": 1, "host_inputs": inp}
+            "launches_per_step": launches_per_scan(w), "host_inputs": inp}
+
+
+def launches_per_scan(w) -> int:
+    """Kernels one scan launches: three for the chunked schedule the library
+    picks for long sequences over few channels (fewer than 64 groups of the
+    state-split kernel and at least 64 tiles of 32 tokens), else one."""
+    ch = 128 // (w.dstate // min(w.dstate, 8))
+    groups = w.batch * -(-w.dim // ch)
+    tiles = -(-w.seqlen // 32)
+    return 3 if groups < 64 and tiles >= 64 else 1
+
+
+def time_other(name, reps=20):
+    """Kernel time of one scan of another workload: `reps` scans captured in
+    one CUDA graph (so that host-side call overhead, which dominates the tiny
+    workload, is not counted), L2 flushed before each scan."""
+    import selective_state_space_116_b300 as ssm
+    w = WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = make_scan_inputs(w, seed=0)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(g["u"])
+    last = torch.empty(w.batch, w.dim, w.dstate, device=dev) if w.last_state else None
+    nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, g["u"].dtype)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def scan():
+        ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                         delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
+                         return_last_state=w.last_state, y=y, last_state=last, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            scan()
+    torch.cuda.synchronize(dev)
+    # a graph of flush + scan pairs and a graph of the flushes alone: the
+    # scans' time is the difference
+    both, flushes = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(both, stream=stream):
+        for _ in range(reps):
+            flush.zero_()
+            scan()
+    with torch.cuda.graph(flushes, stream=stream):
+        for _ in range(reps):
+            flush.zero_()
+    both.replay()
+    flushes.replay()
+    torch.cuda.synchronize(dev)
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    cur = torch.cuda.current_stream(dev)
+    a.record(cur)
+    both.replay()
+    b.record(cur)
+    flushes.replay()
+    c.record(cur)
+    torch.cuda.synchronize(dev)
+    t = max(a.elapsed_time(b) - b.elapsed_time(c), 1e-6) * 1e-3 / reps
+    elems, io_bytes, exps = scan_work(w)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    t_sfu = exps / (EX2_PER_CLK_PER_SM * sms * pk["sm_max_mhz"] * 1e6)
+    t_hbm = io_bytes / (pk["hbm_gbs"] * 1e9)
+    return {"workload": f"{w.name}: batch={w.batch}, D={w.dim}, N={w.dstate}, L={w.seqlen}, "
+                        f"{w.io} I/O", "kernel_time_us": t * 1e6, "elements_per_s": elems / t,
+            "roofline_time_us": max(t_sfu, t_hbm) * 1e6, "bound": "alu" if t_sfu >= t_hbm else "hbm",
+            "frac": max(t_sfu, t_hbm) / t, "launches_per_scan": launches_per_scan(w),
+            "timing": f"{reps} scans in a CUDA graph, L2 flushed before each; flush time subtracted"}
 
 
 def time_e2e(w, inp, steps, warmup, local):
@@ -501,6 +570,7 @@ def run_ours(args, world, rank, local):
                       "ms_per_step": sec * 1e3}
     if not args.no_step and rank == 0:
         out["state_step"] = time_state_step(local)
+        out["other_workloads"] = [time_other("m130"), time_other("tiny")]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_rate(w, res["host_inputs"])
     if rank == 0:

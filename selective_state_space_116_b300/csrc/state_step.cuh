@@ -1,10 +1,13 @@
 // Single-token state update (recurrent / generation mode).
 //
-// Mapping: kS = min(N, 4) state entries per thread, kG = N / kS threads per
-// channel, so a warp reads and writes whole 16-byte pieces of consecutive
-// state rows (fully coalesced).  The kG partial sums of C.h are combined with
-// warp shuffles inside the group; the group's first lane writes y.  The
-// kernel streams the state once in and once out: it is bound by HBM.
+// The kernel streams the fp32 state once in and once out (128 of the ~136
+// bytes it moves per channel at N = 16), so it is bound by HBM bandwidth, and
+// what matters is how many bytes each SM keeps in flight.  Mapping: kS =
+// min(N, 8) state entries per thread and kG = N / kS threads per channel; a
+// thread issues all of its state loads (two 16-byte loads at N = 16) before
+// any arithmetic, and the per-channel inputs (x, delta, z) and per-batch-row
+// B, C rows are loaded alongside.  The kG partial sums of C.h are combined
+// with warp shuffles inside the group; the group's first lane writes y.
 // VEC: the state rows are 16-byte aligned, so 4 entries move as one float4.
 #pragma once
 
@@ -29,14 +32,14 @@ struct StepParams {
 constexpr int kStepThreads = 256;
 
 template <int N> struct StepShape {
-    static constexpr int kS = N < 4 ? N : 4;   // state entries per thread
+    static constexpr int kS = N < 8 ? N : 8;   // state entries per thread
     static constexpr int kG = N / kS;          // threads per channel
 };
 
+// One kS-slice of one channel: load, update, store.
 template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool VEC>
-__global__ void __launch_bounds__(kStepThreads) state_step_kernel(StepParams p) {
+__device__ __forceinline__ void step_item(const StepParams& p, int64_t gid) {
     constexpr int kS = StepShape<N>::kS, kG = StepShape<N>::kG;
-    const int64_t gid = (int64_t)blockIdx.x * kStepThreads + threadIdx.x;
     const int64_t c = gid / kG;                  // flat channel b*dim + d
     const int j = (int)(gid % kG);               // which kS-slice of the state
     const int64_t nch = p.batch * p.dim;
@@ -44,48 +47,72 @@ __global__ void __launch_bounds__(kStepThreads) state_step_kernel(StepParams p) 
     const int64_t cc = active ? c : 0;           // keep loads in bounds for idle lanes
     const int64_t b = cc / p.dim, d = cc % p.dim;
     const int n0 = j * kS;
+    float* st = p.state + cc * N + n0;
 
-    const float bias = p.bias ? p.bias[d] : 0.0f;
-    const float v = io<T>::load(static_cast<const T*>(p.delta), cc) + bias;
-    const float dt = SOFTPLUS ? softplus(v) : v;
+    // the state first: the long-latency loads go out before anything else
+    float h[kS];
+    if constexpr (VEC && kS % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < kS; k += 4) {
+            const float4 v4 = __ldcs(reinterpret_cast<const float4*>(st + k));
+            h[k] = v4.x; h[k + 1] = v4.y; h[k + 2] = v4.z; h[k + 3] = v4.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kS; k++) h[k] = __ldcs(st + k);
+    }
     const float xv = io<T>::load(static_cast<const T*>(p.x), cc);
-    const float dtx = dt * xv;
+    const float dl = io<T>::load(static_cast<const T*>(p.delta), cc);
+    const float zv = HAS_Z ? io<T>::load(static_cast<const T*>(p.z), cc) : 0.0f;
+    const float bias = p.bias ? p.bias[d] : 0.0f;
+    const float Dv = p.D ? p.D[d] : 0.0f;
     const T* Bb = static_cast<const T*>(p.B) + b * N + n0;
     const T* Cb = static_cast<const T*>(p.C) + b * N + n0;
     const float* Ad = p.A + d * N + n0;
-    float* st = p.state + cc * N + n0;
-
-    float h[kS];
-    if constexpr (kS == 4 && VEC) {
-        const float4 v4 = *reinterpret_cast<const float4*>(st);
-        h[0] = v4.x; h[1] = v4.y; h[2] = v4.z; h[3] = v4.w;
-    } else {
+    // (scalar loads: 16-byte vector loads of these small rows measured slower)
+    float Bv[kS], Cv[kS], Av[kS];
 #pragma unroll
-        for (int k = 0; k < kS; k++) h[k] = st[k];
+    for (int k = 0; k < kS; k++) {
+        Bv[k] = io<T>::load(Bb, k);
+        Cv[k] = io<T>::load(Cb, k);
+        Av[k] = Ad[k];
     }
+
+    const float v = dl + bias;
+    const float dt = SOFTPLUS ? softplus(v) : v;
+    const float dtx = dt * xv;
     float part = 0.0f;
 #pragma unroll
     for (int k = 0; k < kS; k++) {
-        const float a = ex2(dt * (Ad[k] * kLog2e));
-        h[k] = fmaf(a, h[k], dtx * io<T>::load(Bb, k));
-        part = fmaf(io<T>::load(Cb, k), h[k], part);
+        const float a = ex2(dt * (Av[k] * kLog2e));
+        h[k] = fmaf(a, h[k], dtx * Bv[k]);
+        part = fmaf(Cv[k], h[k], part);
     }
     if (active) {
-        if constexpr (kS == 4 && VEC) {
-            *reinterpret_cast<float4*>(st) = make_float4(h[0], h[1], h[2], h[3]);
+        if constexpr (VEC && kS % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < kS; k += 4)
+                __stcs(reinterpret_cast<float4*>(st + k), make_float4(h[k], h[k + 1], h[k + 2], h[k + 3]));
         } else {
 #pragma unroll
-            for (int k = 0; k < kS; k++) st[k] = h[k];
+            for (int k = 0; k < kS; k++) __stcs(st + k, h[k]);
         }
     }
     // combine the kG partial dot products of one channel (adjacent lanes)
 #pragma unroll
     for (int off = kG / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     if (active && j == 0) {
-        float yv = fmaf(p.D ? p.D[d] : 0.0f, xv, part);
-        if constexpr (HAS_Z) yv *= silu(io<T>::load(static_cast<const T*>(p.z), cc));
+        float yv = fmaf(Dv, xv, part);
+        if constexpr (HAS_Z) yv *= silu(zv);
         static_cast<T*>(p.y)[cc] = io<T>::from_f32(yv);
     }
+}
+
+// One (channel, slice) item per thread.  (A persistent grid-stride variant
+// measured slower: it serialises each thread's items.)
+template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool VEC>
+__global__ void __launch_bounds__(kStepThreads) state_step_kernel(StepParams p) {
+    step_item<T, N, HAS_Z, SOFTPLUS, VEC>(p, (int64_t)blockIdx.x * kStepThreads + threadIdx.x);
 }
 
 }  // namespace ssm
