@@ -1,5 +1,5 @@
 // Forward selective scan with the tensor cores distributing B and C (bf16
-// I/O, N = 16).
+// I/O, N = 16): an asynchronous, warp-specialised pipeline.
 //
 // The state-split kernel in scan_fwd.cuh is bound by shared-memory
 // bandwidth: every thread reads the token's B and C rows (64 bytes per thread
@@ -8,9 +8,9 @@
 // in tensor memory, where each thread reads its own lane:
 //
 //   input term   bb[c, (t, n)] = (Delta u)[c, t] * B[t, n]: over a block of 8
-//                tokens this is the GEMM  A1 x Bexp^T  with A1[c, t] =
-//                (Delta u)[c, t] and the block-diagonal Bexp[(t, n), t'] =
-//                B[t, n] [t = t']  (M = 128 channels, N = 128, K = 8)
+//                tokens the GEMM  A1 x Bexp^T  with A1[c, t] = (Delta u)[c, t]
+//                and the block-diagonal Bexp[(t, n), t'] = B[t, n] [t = t']
+//                (M = 128 channels, N = 128, K = 8)
 //   C broadcast  Cb[c, (t, n)] = C[t, n] for every channel c: the GEMM
 //                ones x Cexp^T with ones[c, k] = [k = 0] and Cexp[(t, n), k]
 //                = C[t, n] [k = 0]  (same shape)
@@ -19,29 +19,36 @@
 // to tf32's 10-bit mantissa, a relative error of 2^-11 on the input term that
 // the bf16 output then rounds at 2^-9).  The recurrence h = exp(Delta A) h +
 // bb and the output sum y = sum_n C h + D u stay on the CUDA cores in fp32,
-// with the state in registers.  The output contraction is not put on the
+// with the state in registers.  (The output contraction is not put on the
 // tensor cores: per token it is a dot product of 16, and as an MMA it needs
-// K = (tokens x states) against a block-diagonal C, i.e. 16 small MMAs per
-// block, which cost more tensor-core time than the recurrence takes.
+// K = tokens x states against a block-diagonal C, 16 small MMAs per block,
+// which cost more tensor-core time than the recurrence takes.)
 //
-// Thread mapping: 256 threads, 8 warps.  Warp w serves tensor-memory lanes
-// 32 (w % 4) .. + 31, i.e. channels 32 (w % 4) + lane of the CTA's 128, and
-// state half g = w / 4 (states 8g .. 8g + 7).  Warps 0-3 also compute the
-// prologue (Delta = softplus(delta + bias), Delta u) of the block three
-// steps ahead; warps 4-7 place B and C on the block diagonals and finish the
-// output (sum of the two halves, D u skip term, silu(z) gate, bf16 store) of
-// the block just scanned.  One elected thread issues the MMAs.
-//
-// Pipeline, per step k (one block of 8 tokens):
-//   recurrence(k)   tcgen05.ld bb, Cb -> registers; partial C.h -> smem
-//   the MMA thread waits for the commit of step k-1 (the MMAs of block k+1)
-//   barrier
-//   MMAs of block k+2 -> tensor-memory buffer (k+2) % 2; commit
-//   prologue(k+3) | B/C diagonals(k+3) and output(k)
-//   cp.async of the raw u, delta, z, B, C of block k+6
-// Rings: 2 x 256 tensor-memory columns, 4 operand slots, 2 partial-sum
-// buffers, 8 raw blocks.  Every wait is bounded.
+// Roles (512 threads, 16 warps, one CTA per SM holding all 512 columns of
+// tensor memory); every hand-off is an mbarrier ring, with one arrival per
+// warp, and no CTA-wide barrier runs inside the loop:
+//   warp 0        producer: one thread issues the TMA copies of 16-token
+//                 tiles (u, delta, z as 128-channel x 16-token boxes with
+//                 32-byte swizzle; the B and C rows as bulk copies) into a
+//                 ring of tiles
+//   warp 1        one thread issues the two MMAs of every 8-token block into
+//                 a ring of 2 tensor-memory buffers (256 columns each)
+//   warps 2-3     epilogue: the sum of the two state halves' partial outputs,
+//                 D u skip term, silu(z) gate, bf16 store (2 channels a thread)
+//   warps 4-7     prologue, thread c for channel c: Delta = softplus(delta +
+//                 bias), Delta u into the A1 operand, Delta for the
+//                 recurrence, B and C onto their block diagonals (ring of
+//                 operand slots)
+//   warps 8-15    recurrence: warp w serves tensor-memory lanes 32 (w % 4) ..
+//                 + 31 (channels) and state half (w - 8) / 4; each thread
+//                 loads its bb and C values with tcgen05.ld (the next two
+//                 tokens' load in flight while it computes the current two),
+//                 advances its 8 states and writes its partial C.h
+// Every wait is bounded; a wait that gives up marks the CTA failed, later
+// waits return at once, and the workspace status word reports it.
 #pragma once
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "scan_fwd.cuh"
@@ -49,13 +56,16 @@
 namespace ssm {
 namespace tc {
 
-constexpr int kThreads = 512;  // 16 warps: 4 state quarters x 4 tensor-memory lane quarters
+constexpr int kThreads = 512;
 constexpr int kCH = 128;        // channels per group = tensor-memory lanes = MMA M
 constexpr int kN = 16;          // states
-constexpr int kTB = 8;          // tokens per block (one MMA pair, one pipeline step)
-constexpr int kTT = 32;         // tokens per raw input tile (4 blocks)
-constexpr int kNSLOT = 4;       // operand slots (A1, W, Bexp, Cexp)
-constexpr int kNTILE = 3;       // raw input tiles in flight
+constexpr int kTB = 8;          // tokens per block (one MMA pair)
+constexpr int kBPT = 2;         // blocks per raw tile
+constexpr int kTT = kTB * kBPT; // tokens per raw tile
+constexpr int kRawSlots = 7;    // raw tiles in flight
+constexpr int kOpSlots = 4;     // operand slots in flight
+constexpr int kYSlots = 4;      // partial-output slots in flight
+constexpr int kRecWarps = 8;
 constexpr int kTmemCols = 512;  // 2 buffers x (128 bb + 128 Cb) columns
 
 // Operands are K-major without swizzle: 8 x 16-byte core matrices, the next
@@ -63,23 +73,35 @@ constexpr int kTmemCols = 512;  // 2 buffers x (128 bb + 128 Cb) columns
 __host__ __device__ constexpr int kmaj(int row, int k) {
     return (row >> 3) * 256 + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4;
 }
-// Column (= Bexp / Cexp row) of token t, state n within a block: each thread's
-// 4 states x 8 tokens are 32 consecutive columns.
-__host__ __device__ constexpr int bcol(int t, int n) { return (n >> 2) * 32 + t * 4 + (n & 3); }
+// Column (= Bexp / Cexp row) of token t, state n within a block: the 8 states
+// x 8 tokens of each state half are 64 consecutive columns.
+__host__ __device__ constexpr int bcol(int t, int n) { return (n >> 3) * 64 + t * 8 + (n & 7); }
 constexpr int kOpBytes = 128 * kTB * 4;     // one 128 x 8 tf32 operand
 constexpr int kSlotBytes = 4 * kOpBytes;    // A1 = Delta u, W = Delta, Bexp, Cexp
 constexpr int kOffW = kOpBytes, kOffBexp = 2 * kOpBytes, kOffCexp = 3 * kOpBytes;
 constexpr int kYRow = 48;                   // 8 fp32 partial sums + 16 bytes of padding
-constexpr int kYBytes = 4 * kCH * kYRow;    // the four state quarters
-constexpr int kRawRow = kTT * 2 + 16;       // one channel's 32 bf16 tokens, padded
-constexpr int kRawPlane = kCH * kRawRow;
-constexpr int kRawBC = kTT * kN * 2;        // 32 tokens x 16 states bf16
-constexpr int kTileBytes = 3 * kRawPlane + 2 * kRawBC;
-constexpr int kOffOnes = kNSLOT * kSlotBytes;
+constexpr int kYBytes = 2 * kCH * kYRow;    // both state halves of one block
+// Raw tile: the u, delta, z planes as TMA writes a 16-token x 128-channel box
+// (32-byte rows, the two 16-byte halves of row r swapped when bit 2 of r is
+// set: the 32-byte swizzle, which keeps 8 consecutive rows' reads of one
+// half on distinct banks), then the B and C rows of the 16 tokens.
+constexpr int kPlaneBytes = kCH * kTT * 2;
+constexpr int kRawBC = kTT * kN * 2;        // 16 tokens x 16 states bf16
+constexpr int kOffTileB = 3 * kPlaneBytes, kOffTileC = kOffTileB + kRawBC;
+constexpr int kTileBytes = (kOffTileC + kRawBC + 1023) / 1024 * 1024;
+__host__ __device__ constexpr int raw_off(int c, int blk) { return c * 32 + ((blk ^ (c >> 2)) & 1) * 16; }
+constexpr int kOffOnes = kOpSlots * kSlotBytes;
 constexpr int kOffY = kOffOnes + kOpBytes;
-constexpr int kOffRaw = kOffY + 2 * kYBytes;
-constexpr int kSmem = kOffRaw + kNTILE * kTileBytes;
+constexpr int kOffRaw = kOffY + kYSlots * kYBytes;
+constexpr int kSmemUsed = kOffRaw + kRawSlots * kTileBytes;
+constexpr int kSmem = kSmemUsed + 1024;   // room to align the base to 1 KB
 static_assert(kSmem <= 226 * 1024, "shared memory");
+static_assert(kOffRaw % 1024 == 0 && kTileBytes % 1024 == 0, "swizzled planes need 1 KB alignment");
+
+// tensor maps of u, delta, z: (L, dim, batch) bf16, box (16, 128, 1), 32-byte swizzle
+struct TmaMaps {
+    CUtensorMap u, delta, z;
+};
 
 // instruction descriptor, kind::tf32, fp32 accumulate, both operands K-major
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -156,292 +178,144 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, volatile
           "=r"(v[o + 26]), "=r"(v[o + 27]), "=r"(v[o + 28]), "=r"(v[o + 29]),                  \
           "=r"(v[o + 30]), "=r"(v[o + 31])                                                     \
         : "r"(addr))
-#define SSM_TMEM_ST32(addr, v, o)                                                              \
+#define SSM_TMEM_LD16(addr, v)                                                                 \
     asm volatile(                                                                              \
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"    \
-        "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"     \
-        "%32};" ::"r"(addr),                                                                   \
-        "r"(v[o + 0]), "r"(v[o + 1]), "r"(v[o + 2]), "r"(v[o + 3]), "r"(v[o + 4]),             \
-        "r"(v[o + 5]), "r"(v[o + 6]), "r"(v[o + 7]), "r"(v[o + 8]), "r"(v[o + 9]),             \
-        "r"(v[o + 10]), "r"(v[o + 11]), "r"(v[o + 12]), "r"(v[o + 13]), "r"(v[o + 14]),        \
-        "r"(v[o + 15]), "r"(v[o + 16]), "r"(v[o + 17]), "r"(v[o + 18]), "r"(v[o + 19]),        \
-        "r"(v[o + 20]), "r"(v[o + 21]), "r"(v[o + 22]), "r"(v[o + 23]), "r"(v[o + 24]),        \
-        "r"(v[o + 25]), "r"(v[o + 26]), "r"(v[o + 27]), "r"(v[o + 28]), "r"(v[o + 29]),        \
-        "r"(v[o + 30]), "r"(v[o + 31])                                                         \
-        : "memory")
-
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
+        "%13,%14,%15}, [%16];"                                                                 \
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),  \
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),           \
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])                                                \
+        : "r"(addr))
 __device__ __forceinline__ float to_tf32(float x) {   // round to nearest, ties away
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return __uint_as_float(r);
 }
 
-struct Shared {
-    uint64_t mbar[4];
-    uint32_t taddr;
-    int ok;
-    int failed;   // a bounded wait of this CTA gave up
-};
 
-// One part: channel group `grp`, blocks [b0, b1) of its 8-token blocks.
-// `S` is the CTA's running step counter (mbarrier slot and phase).
-template <bool HAS_Z, bool SOFTPLUS>
-__device__ __forceinline__ void tc_part(const ScanParams& p, unsigned char* smem, Shared& sh,
-                                        int64_t grp, int64_t b0, int64_t b1, uint32_t& S) {
-    using bf16 = __nv_bfloat16;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, s4 = warp >> 2;
-    const int c = q * 32 + lane;                       // this thread's channel in the group
-    const int64_t b = grp / p.groups_per_row;
-    const int64_t d0 = (grp % p.groups_per_row) * kCH;
-    const int rows = (int)(p.dim - d0 < kCH ? p.dim - d0 : kCH);
-    const int64_t row0 = b * p.dim + d0;
-    const int64_t L = p.L;
-    const int nb = (int)(b1 - b0);
-    const bool active = c < rows;
-
-    const bf16* gu = static_cast<const bf16*>(p.u);
-    const bf16* gdl = static_cast<const bf16*>(p.delta);
-    const bf16* gz = static_cast<const bf16*>(p.z);
-    const bf16* gB = static_cast<const bf16*>(p.B) + b * L * kN;
-    const bf16* gC = static_cast<const bf16*>(p.C) + b * L * kN;
-    bf16* gy = static_cast<bf16*>(p.y);
-
-    float A2[4], h[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++)   // exp(Delta A) = 2^(Delta A log2 e)
-        A2[j] = active ? p.A[(d0 + c) * kN + s4 * 4 + j] * kLog2e : 0.0f;
-    float bias = (active && p.bias) ? p.bias[d0 + c] : 0.0f;
-    if (SOFTPLUS) bias *= kLog2e;
-    const float Dv = (active && p.D) ? p.D[d0 + c] : 0.0f;
-
-    // raw inputs of tile j (blocks 4j .. 4j+3) into ring slot j % kNTILE,
-    // 64 bytes per channel row; zero past the last channel
-    auto load_tile = [&](int j) {
-        unsigned char* r = smem + kOffRaw + (j % kNTILE) * kTileBytes;
-        const int kb0 = 4 * j;
-        const int nblk = nb - kb0 < 4 ? nb - kb0 : 4;     // blocks of this tile in the part
-        const int64_t t0 = (b0 + kb0) * kTB;
-        const int nplanes = HAS_Z ? 3 : 2;
-        // one 16-byte chunk (8 bf16 tokens) per block: chunk ck of a row is
-        // block 4j + ck, present only for ck < nblk
-        for (int i = tid; i < nplanes * kCH * 4; i += kThreads) {
-            const int pl = i / (kCH * 4), rem = i % (kCH * 4), ch = rem >> 2, ck = rem & 3;
-            if (ck >= nblk) continue;
-            const bf16* src = pl == 0 ? gu : (pl == 1 ? gdl : gz);
-            const bool ok = ch < rows;
-            ssm::seq::cp_async16(r + pl * kRawPlane + ch * kRawRow + ck * 16,
-                                 ok ? static_cast<const void*>(src + (row0 + ch) * L + t0 + ck * 8)
-                                    : src,
-                                 ok ? 16 : 0);
-        }
-        for (int i = tid; i < 2 * nblk * 16; i += kThreads) {   // B, C: 16 chunks per block
-            const int which = i / (nblk * 16), e = (i % (nblk * 16)) * 8;
-            const bf16* src = (which == 0 ? gB : gC) + t0 * kN + e;
-            ssm::seq::cp_async16(r + 3 * kRawPlane + which * kRawBC + e * 2, src, 16);
-        }
-    };
-
-    // initial state: zero, or the state handed over by the CTA before
-    if (b0 == 0) {
-#pragma unroll
-        for (int j = 0; j < 4; j++) h[j] = 0.0f;
-    } else {
-        if (tid == 0) {
-            const bool ok = ssm::seq::wait_flag(p.flags + grp);
-            if (!ok) atomicExch(p.status, kStatusTimeout);
-            __threadfence();
-            sh.ok = ok;
-        }
-        __syncthreads();
-        const bool ok = sh.ok;
-        const float* src = p.carry + (grp * kCH + c) * kN + s4 * 4;
-#pragma unroll
-        for (int j = 0; j < 4; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
-    }
-
-    // Tile j is requested at step 4j - 7 (tile 0 before the first step) and
-    // first read at step 4j - 3; one cp.async group per step, so at every
-    // step all but the three newest groups must be complete.
-    load_tile(0);
-    ssm::seq::cp_async_commit();
-    for (int i = 0; i < 3; i++) ssm::seq::cp_async_commit();
-
-    const uint32_t tbase = sh.taddr;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-
-    for (int k = -3; k < nb; k++, S++) {
-        asm volatile("cp.async.wait_group 3;\n" ::: "memory");
-
-        // ---- recurrence of block k: states 4 s4 .. 4 s4 + 3 ----
-        if (k >= 0) {
-            const uint32_t col = tbase + lane_base + (uint32_t)((k & 1) * 256 + s4 * 32);
-            uint32_t v[32], cv[32];
-            SSM_TMEM_LD32(col, v, 0);
-            SSM_TMEM_LD32(col + 128, cv, 0);
-            const unsigned char* wsl = smem + (k % kNSLOT) * kSlotBytes + kOffW;
-            const float4 dA = *reinterpret_cast<const float4*>(wsl + kmaj(c, 0));
-            const float4 dB = *reinterpret_cast<const float4*>(wsl + kmaj(c, 4));
-            const float dts[8] = {dA.x, dA.y, dA.z, dA.w, dB.x, dB.y, dB.z, dB.w};
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            float yp[8];
-#pragma unroll
-            for (int t = 0; t < kTB; t++) {
-                const float2 dt2 = make_float2(dts[t], dts[t]);
-                const float2 e0 = __fmul2_rn(dt2, make_float2(A2[0], A2[1]));
-                const float2 e1 = __fmul2_rn(dt2, make_float2(A2[2], A2[3]));
-                const float2 a0 = make_float2(ex2(e0.x), ex2(e0.y));
-                const float2 a1 = make_float2(ex2(e1.x), ex2(e1.y));
-                const float2 h0 = __ffma2_rn(a0, make_float2(h[0], h[1]),
-                                             make_float2(__uint_as_float(v[t * 4]),
-                                                         __uint_as_float(v[t * 4 + 1])));
-                const float2 h1 = __ffma2_rn(a1, make_float2(h[2], h[3]),
-                                             make_float2(__uint_as_float(v[t * 4 + 2]),
-                                                         __uint_as_float(v[t * 4 + 3])));
-                h[0] = h0.x; h[1] = h0.y; h[2] = h1.x; h[3] = h1.y;
-                float2 acc = __fmul2_rn(make_float2(__uint_as_float(cv[t * 4]),
-                                                    __uint_as_float(cv[t * 4 + 1])), h0);
-                acc = __ffma2_rn(make_float2(__uint_as_float(cv[t * 4 + 2]),
-                                             __uint_as_float(cv[t * 4 + 3])), h1, acc);
-                yp[t] = acc.x + acc.y;
-            }
-            float4* ydst = reinterpret_cast<float4*>(smem + kOffY + (k & 1) * kYBytes +
-                                                     (s4 * kCH + c) * kYRow);
-            ydst[0] = make_float4(yp[0], yp[1], yp[2], yp[3]);
-            ydst[1] = make_float4(yp[4], yp[5], yp[6], yp[7]);
-            if (k == nb - 1) {   // the part's final state
-                if (b1 * kTB == L) {
-                    if (active && p.last_state) {
-                        float* dst = p.last_state + (row0 + c) * kN + s4 * 4;
-#pragma unroll
-                        for (int j = 0; j < 4; j++) dst[j] = h[j];
-                    }
-                } else {
-                    float* dst = p.carry + (grp * kCH + c) * kN + s4 * 4;
-#pragma unroll
-                    for (int j = 0; j < 4; j++) __stcg(dst + j, h[j]);
-                    __threadfence();
-                }
-            }
-        }
-        // step k-1's MMAs (block k+1, read from the next step on): only the
-        // issuing thread waits, and the barrier passes the completion on
-        if (tid == 0 && S >= 1 &&
-            !mbar_wait(&sh.mbar[(S - 1) & 3], ((S - 1) >> 2) & 1, &sh.failed))
-            atomicExch(p.status, kStatusTimeout);
-        fence_before();
-        __syncthreads();
-        fence_after();
-
-        // ---- MMAs of block k+2 (one thread) ----
-        if (tid == 0) {
-            if (k == nb - 1 && b1 * kTB != L)
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + grp), "r"(1u)
-                             : "memory");
-            const int k2 = k + 2;
-            if (k2 >= 0 && k2 < nb) {
-                const unsigned char* sl = smem + (k2 % kNSLOT) * kSlotBytes;
-                const uint32_t d = tbase + (uint32_t)((k2 & 1) * 256);
-                mma_ss(d, sdesc(smem_u32(sl), 128, 256), sdesc(smem_u32(sl + kOffBexp), 128, 256),
-                       idesc_tf32(128, 128), 0);
-                mma_ss(d + 128, sdesc(smem_u32(smem + kOffOnes), 128, 256),
-                       sdesc(smem_u32(sl + kOffCexp), 128, 256), idesc_tf32(128, 128), 0);
-            }
-            mma_commit(&sh.mbar[S & 3]);
-        }
-
-        const int k3 = k + 3;
-        if (s4 == 0) {
-            // ---- prologue of block k+3: Delta and Delta u ----
-            if (k3 < nb) {
-                const unsigned char* r = smem + kOffRaw + ((k3 >> 2) % kNTILE) * kTileBytes +
-                                         c * kRawRow + (k3 & 3) * 16;
-                float uv[8], dv[8];
-                ssm::seq::unpack8<bf16>(r, uv);
-                ssm::seq::unpack8<bf16>(r + kRawPlane, dv);
-                float dt[8], du[8];
-#pragma unroll
-                for (int t = 0; t < 8; t++) {
-                    if constexpr (SOFTPLUS) dt[t] = ssm::seq::softplus_log2(fmaf(dv[t], kLog2e, bias));
-                    else dt[t] = dv[t] + bias;
-                    du[t] = to_tf32(dt[t] * uv[t]);
-                }
-                unsigned char* sl = smem + (k3 % kNSLOT) * kSlotBytes;
-                *reinterpret_cast<float4*>(sl + kmaj(c, 0)) = make_float4(du[0], du[1], du[2], du[3]);
-                *reinterpret_cast<float4*>(sl + kmaj(c, 4)) = make_float4(du[4], du[5], du[6], du[7]);
-                *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 0)) = make_float4(dt[0], dt[1], dt[2], dt[3]);
-                *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 4)) = make_float4(dt[4], dt[5], dt[6], dt[7]);
-            }
-        } else if (s4 == 1) {
-            // ---- B and C of block k+3 onto their block diagonals ----
-            if (k3 < nb) {
-                const unsigned char* r = smem + kOffRaw + ((k3 >> 2) % kNTILE) * kTileBytes +
-                                         3 * kRawPlane + (k3 & 3) * 256;
-                unsigned char* sl = smem + (k3 % kNSLOT) * kSlotBytes;
-                const int i = c;                   // one B and one C value per thread
-                const int t = i >> 4, n = i & 15;
-                const int row = bcol(t, n);
-                const float bv = __bfloat162float(reinterpret_cast<const bf16*>(r)[i]);
-                const float cv = __bfloat162float(reinterpret_cast<const bf16*>(r + kRawBC)[i]);
-                *reinterpret_cast<float*>(sl + kOffBexp + kmaj(row, t)) = bv;
-                *reinterpret_cast<float*>(sl + kOffCexp + kmaj(row, 0)) = cv;
-            }
-        } else if (k >= 0) {
-            // ---- output of block k: tokens 4 (s4 - 2) .. + 3 of channel c ----
-            const int half = s4 - 2;
-            const unsigned char* yb = smem + kOffY + (k & 1) * kYBytes + c * kYRow + half * 16;
-            float4 acc = *reinterpret_cast<const float4*>(yb);
-#pragma unroll
-            for (int qq = 1; qq < 4; qq++) {
-                const float4 a = *reinterpret_cast<const float4*>(yb + qq * kCH * kYRow);
-                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-            }
-            float ys[4] = {acc.x, acc.y, acc.z, acc.w};
-            const unsigned char* r = smem + kOffRaw + ((k >> 2) % kNTILE) * kTileBytes +
-                                     c * kRawRow + (k & 3) * 16 + half * 8;
-            const uint2 uq = *reinterpret_cast<const uint2*>(r);
-            const float uv[4] = {__uint_as_float(uq.x << 16), __uint_as_float(uq.x & 0xffff0000u),
-                                 __uint_as_float(uq.y << 16), __uint_as_float(uq.y & 0xffff0000u)};
-#pragma unroll
-            for (int t = 0; t < 4; t++) ys[t] = fmaf(Dv, uv[t], ys[t]);
-            if constexpr (HAS_Z) {
-                const uint2 zq = *reinterpret_cast<const uint2*>(r + 2 * kRawPlane);
-                const float zv[4] = {__uint_as_float(zq.x << 16), __uint_as_float(zq.x & 0xffff0000u),
-                                     __uint_as_float(zq.y << 16), __uint_as_float(zq.y & 0xffff0000u)};
-#pragma unroll
-                for (int t = 0; t < 4; t++) ys[t] *= ssm::seq::gate<bf16>(zv[t]);
-            }
-            if (active) {
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(ys[0], ys[1]);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(ys[2], ys[3]);
-                uint2 o;
-                o.x = *reinterpret_cast<const unsigned*>(&lo);
-                o.y = *reinterpret_cast<const unsigned*>(&hi);
-                *reinterpret_cast<uint2*>(gy + (row0 + c) * L + (b0 + k) * kTB + half * 4) = o;
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-
-        // ---- raw inputs of tile (k+7)/4 ----
-        if (((k + 7) & 3) == 0) {
-            const int j = (k + 7) >> 2;
-            if (j >= 1 && 4 * j < nb) load_tile(j);
-        }
-        ssm::seq::cp_async_commit();
-    }
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    // the last MMAs of the part (issued at step nb-3) were waited for at step nb-2
-    __syncthreads();
+__device__ __forceinline__ void mbar_arrive(uint64_t* m) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes)
+                 : "memory");
+}
+// TMA: box at (x, y, z) of a 3-D tensor map -> shared memory, completion
+// counted in bytes on the mbarrier
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(m))
+        : "memory");
+}
+// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(m))
+        : "memory");
+}
+// barrier over the `count` threads of a role (ids 1.. ; 0 is __syncthreads)
+__device__ __forceinline__ void role_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Persistent, balanced schedule over (channel group, 8-token block) work,
-// as for the state-split kernel; one CTA per SM (it holds all 512 columns
-// of tensor memory).
+struct Bars {
+    uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
+    uint64_t op_full[kOpSlots], op_empty[kOpSlots];
+    uint64_t d_full[2], d_empty[2], yp_full[kYSlots], yp_empty[kYSlots];
+    uint32_t taddr;
+    int failed;   // a bounded wait of this CTA gave up
+    int ok;       // the carry hand-over arrived
+};
+
+// The CTA's share of the (channel group, 8-token block) work, walked by every
+// role in the same order (as in scan_fwd_kernel of scan_fwd.cuh): the head
+// of its last group, its whole groups, the continuation of its first group.
+struct Parts {
+    int64_t s, e, nblk, g_first, g_last;
+    __device__ explicit Parts(const ScanParams& p) {
+        nblk = p.L / kTB;
+        const int64_t W = p.ngroups * nblk;
+        s = W * blockIdx.x / gridDim.x;
+        e = W * (blockIdx.x + 1) / gridDim.x;
+        g_first = s / nblk;
+        g_last = s < e ? (e - 1) / nblk : g_first - 1;
+    }
+    __device__ void range(int64_t grp, int64_t& b0, int64_t& b1) const {
+        const int64_t lo = grp * nblk;
+        b0 = (s > lo ? s : lo) - lo;
+        b1 = (e < lo + nblk ? e : lo + nblk) - lo;
+    }
+};
+
+// Position in that walk: block kb of group grp (part [b0, b1); batch row b,
+// first channel d0), the CTA-wide block counter i and raw-tile counter T.
+struct Cursor {
+    int64_t grp, b0, b1, kb, i, T, b, d0;
+    __device__ Cursor(const Parts& pt, const ScanParams& p) : grp(pt.g_last), i(0), T(0) {
+        enter(pt, p);
+    }
+    __device__ void enter(const Parts& pt, const ScanParams& p) {
+        if (grp >= pt.g_first) {
+            pt.range(grp, b0, b1);
+            b = grp / p.groups_per_row;
+            d0 = (grp - b * p.groups_per_row) * kCH;
+        } else {
+            b0 = b1 = 0;
+        }
+        kb = b0;
+    }
+    __device__ bool valid(const Parts& pt) const { return grp >= pt.g_first; }
+    __device__ int blk() const { return (int)((kb - b0) & (kBPT - 1)); }
+    __device__ bool tile_last() const { return blk() == kBPT - 1 || kb == b1 - 1; }
+    __device__ void next(const Parts& pt, const ScanParams& p) {
+        if (tile_last()) T++;
+        i++;
+        if (++kb == b1) {
+            --grp;
+            enter(pt, p);
+        }
+    }
+};
+static_assert((kBPT & (kBPT - 1)) == 0, "blocks per tile: a power of two");
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t* m, uint32_t parity, Bars& br,
+                                             const ScanParams& p) {
+    if (mbar_wait(m, parity, &br.failed)) return true;
+    atomicExch(p.status, kStatusTimeout);
+    return false;
+}
+// phase parity of the k-th use (k = 0, 1, ...) of a ring slot: the full
+// barrier's phase k, and the empty barrier's phase k - 1 (k >= 1)
+__device__ __forceinline__ uint32_t full_parity(int64_t k) { return (uint32_t)(k & 1); }
+__device__ __forceinline__ uint32_t empty_parity(int64_t k) { return (uint32_t)((k + 1) & 1); }
+
+// wait for this thread's tensor-memory loads; the "+r" operands keep every use
+// of the loaded registers after the wait
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[16], uint32_t (&w)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(w[0]), "+r"(w[1]),
+                   "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7]),
+                   "+r"(w[8]), "+r"(w[9]), "+r"(w[10]), "+r"(w[11]), "+r"(w[12]), "+r"(w[13]),
+                   "+r"(w[14]), "+r"(w[15])
+                 :
+                 : "memory");
+}
+
 template <bool HAS_Z, bool SOFTPLUS>
-__global__ void __launch_bounds__(kThreads, 1) scan_fwd_tc_kernel(ScanParams p) {
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ Shared sh;
-    const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_fwd_tc_kernel(ScanParams p, const __grid_constant__ TmaMaps maps) {
+    using bf16 = __nv_bfloat16;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ Bars br;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // zero the operand slots once (only the block diagonals of Bexp and Cexp
     // are ever written again); the ones operand has a 1 in column 0 of every row
@@ -449,16 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1) scan_fwd_tc_kernel(ScanParams p) 
         *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (tid < kCH) *reinterpret_cast<float*>(smem + kOffOnes + kmaj(tid, 0)) = 1.0f;
-    if (tid < 32) {
+    if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&sh.taddr)),
+                         smem_u32(&br.taddr)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        sh.failed = 0;
-        for (int i = 0; i < 4; i++) mbar_init(&sh.mbar[i], 1);
+        br.failed = 0;
+        for (int i = 0; i < kRawSlots; i++) {
+            mbar_init(&br.raw_full[i], 1);    // the producer's expect_tx
+            mbar_init(&br.raw_empty[i], 6);   // 4 prologue + 2 epilogue warps
+        }
+        for (int i = 0; i < kOpSlots; i++) {
+            mbar_init(&br.op_full[i], 4);                  // prologue warps
+            mbar_init(&br.op_empty[i], 1 + kRecWarps);     // MMA commit + recurrence warps
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&br.d_full[i], 1);                   // MMA commit
+            mbar_init(&br.d_empty[i], kRecWarps);
+        }
+        for (int i = 0; i < kYSlots; i++) {
+            mbar_init(&br.yp_full[i], kRecWarps);
+            mbar_init(&br.yp_empty[i], 2);                 // epilogue warps
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -466,26 +355,278 @@ __global__ void __launch_bounds__(kThreads, 1) scan_fwd_tc_kernel(ScanParams p) 
     __syncthreads();
     fence_after();
 
-    const int64_t nblk = p.L / kTB;
-    const int64_t W = p.ngroups * nblk;
-    const int64_t s = W * blockIdx.x / gridDim.x;
-    const int64_t e = W * (blockIdx.x + 1) / gridDim.x;
-    uint32_t S = 0;
-    if (s < e) {
-        const int64_t g_first = s / nblk, g_last = (e - 1) / nblk;
-        for (int64_t grp = g_last; grp >= g_first; grp--) {
-            const int64_t lo = grp * nblk;
-            const int64_t b0 = (s > lo ? s : lo) - lo;
-            const int64_t b1 = (e < lo + nblk ? e : lo + nblk) - lo;
-            tc_part<HAS_Z, SOFTPLUS>(p, smem, sh, grp, b0, b1, S);
+    const Parts parts(p);
+    const uint32_t tbase = br.taddr;
+    const int64_t L = p.L;
+
+    if (warp == 0) {
+        // ---------------- producer: raw input tiles (one thread) ----------------
+        if (lane == 0) {
+            int64_t T = 0;   // CTA-wide tile counter
+            for (int64_t grp = parts.g_last; grp >= parts.g_first; grp--) {
+                int64_t b0, b1;
+                parts.range(grp, b0, b1);
+                const int64_t b = grp / p.groups_per_row;
+                const int d0 = (int)((grp % p.groups_per_row) * kCH);
+                const bf16* gB = static_cast<const bf16*>(p.B) + b * L * kN;
+                const bf16* gC = static_cast<const bf16*>(p.C) + b * L * kN;
+                const int nb = (int)(b1 - b0);
+                for (int j = 0; j * kBPT < nb; j++, T++) {
+                    const int slot = (int)(T % kRawSlots);
+                    if (T >= kRawSlots) wait_or_fail(&br.raw_empty[slot], empty_parity(T / kRawSlots), br, p);
+                    unsigned char* r = smem + kOffRaw + slot * kTileBytes;
+                    const int nblk = nb - j * kBPT < kBPT ? nb - j * kBPT : kBPT;
+                    const int64_t t0 = (b0 + (int64_t)j * kBPT) * kTB;
+                    const uint32_t bc = (uint32_t)(nblk * kTB * kN * 2);
+                    mbar_expect_tx(&br.raw_full[slot], (HAS_Z ? 3 : 2) * kPlaneBytes + 2 * bc);
+                    tma_load_3d(r, &maps.u, (int)t0, d0, (int)b, &br.raw_full[slot]);
+                    tma_load_3d(r + kPlaneBytes, &maps.delta, (int)t0, d0, (int)b, &br.raw_full[slot]);
+                    if (HAS_Z) tma_load_3d(r + 2 * kPlaneBytes, &maps.z, (int)t0, d0, (int)b, &br.raw_full[slot]);
+                    bulk_load(r + kOffTileB, gB + t0 * kN, bc, &br.raw_full[slot]);
+                    bulk_load(r + kOffTileC, gC + t0 * kN, bc, &br.raw_full[slot]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            int64_t i = 0;   // CTA-wide block counter
+            for (Cursor cu(parts, p); cu.valid(parts); cu.next(parts, p), i++) {
+                const int o = (int)(i % kOpSlots), bf = (int)(i & 1);
+                wait_or_fail(&br.op_full[o], full_parity(i / kOpSlots), br, p);
+                if (i >= 2) wait_or_fail(&br.d_empty[bf], empty_parity(i / 2), br, p);
+                fence_after();
+                const unsigned char* sl = smem + o * kSlotBytes;
+                const uint32_t d = tbase + (uint32_t)(bf * 256);
+                mma_ss(d, sdesc(smem_u32(sl), 128, 256), sdesc(smem_u32(sl + kOffBexp), 128, 256),
+                       idesc_tf32(128, 128), 0);
+                mma_ss(d + 128, sdesc(smem_u32(smem + kOffOnes), 128, 256),
+                       sdesc(smem_u32(sl + kOffCexp), 128, 256), idesc_tf32(128, 128), 0);
+                mma_commit(&br.d_full[bf]);
+                mma_commit(&br.op_empty[o]);
+            }
+            // the tensor memory is freed below: let the last MMAs finish even
+            // if the pipeline gave up
+            if (i > 0) {
+                volatile int never = 0;
+                mbar_wait(&br.d_full[(i - 1) & 1], full_parity((i - 1) / 2), &never);
+            }
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------- epilogue ----------------
+        for (Cursor ec(parts, p); ec.valid(parts); ec.next(parts, p)) {
+            const int64_t b = ec.b, d0 = ec.d0;
+            const int rs = (int)(ec.T % kRawSlots), ys = (int)(ec.i % kYSlots), blk = ec.blk();
+            wait_or_fail(&br.yp_full[ys], full_parity(ec.i / kYSlots), br, p);
+            float y[2][8];
+#pragma unroll
+            for (int k = 0; k < 2; k++) {   // channels tid - 64 and tid
+                const int c = tid - 64 + 64 * k;
+                const unsigned char* yb = smem + kOffY + ys * kYBytes + c * kYRow;
+                const float4 a0 = *reinterpret_cast<const float4*>(yb);
+                const float4 a1 = *reinterpret_cast<const float4*>(yb + 16);
+                const float4 b0v = *reinterpret_cast<const float4*>(yb + kCH * kYRow);
+                const float4 b1v = *reinterpret_cast<const float4*>(yb + kCH * kYRow + 16);
+                y[k][0] = a0.x + b0v.x; y[k][1] = a0.y + b0v.y; y[k][2] = a0.z + b0v.z; y[k][3] = a0.w + b0v.w;
+                y[k][4] = a1.x + b1v.x; y[k][5] = a1.y + b1v.y; y[k][6] = a1.z + b1v.z; y[k][7] = a1.w + b1v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&br.yp_empty[ys]);
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int c = tid - 64 + 64 * k;
+                const bool active = d0 + c < p.dim;
+                const float Dv = (active && p.D) ? p.D[d0 + c] : 0.0f;
+                const unsigned char* r = smem + kOffRaw + rs * kTileBytes + raw_off(c, blk);
+                float uv[8];
+                ssm::seq::unpack8<bf16>(r, uv);
+#pragma unroll
+                for (int t = 0; t < 8; t++) y[k][t] = fmaf(Dv, uv[t], y[k][t]);
+                if constexpr (HAS_Z) {
+                    float zv[8];
+                    ssm::seq::unpack8<bf16>(r + 2 * kPlaneBytes, zv);
+#pragma unroll
+                    for (int t = 0; t < 8; t++) y[k][t] *= ssm::seq::gate<bf16>(zv[t]);
+                }
+                if (active) {
+                    uint4 ov;
+                    unsigned* o32 = reinterpret_cast<unsigned*>(&ov);
+#pragma unroll
+                    for (int t = 0; t < 4; t++) {
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(y[k][2 * t], y[k][2 * t + 1]);
+                        o32[t] = *reinterpret_cast<const unsigned*>(&pr);
+                    }
+                    bf16* gy = static_cast<bf16*>(p.y);
+                    *reinterpret_cast<uint4*>(gy + (b * p.dim + d0 + c) * L + ec.kb * kTB) = ov;
+                }
+            }
+            if (ec.tile_last()) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&br.raw_empty[rs]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- prologue ----------------
+        const int c = tid - 128;   // channel within the group
+        float bias = 0.0f;
+        int64_t bias_grp = -1;
+        for (Cursor pc(parts, p); pc.valid(parts); pc.next(parts, p)) {
+            const int64_t d0 = pc.d0;
+            if (pc.grp != bias_grp) {
+                bias_grp = pc.grp;
+                bias = (d0 + c < p.dim && p.bias) ? p.bias[d0 + c] : 0.0f;
+                if (SOFTPLUS) bias *= kLog2e;
+            }
+            const int rs = (int)(pc.T % kRawSlots), o = (int)(pc.i % kOpSlots), blk = pc.blk();
+            if (blk == 0) wait_or_fail(&br.raw_full[rs], full_parity(pc.T / kRawSlots), br, p);
+            if (pc.i >= kOpSlots) wait_or_fail(&br.op_empty[o], empty_parity(pc.i / kOpSlots), br, p);
+            const unsigned char* r = smem + kOffRaw + rs * kTileBytes;
+            unsigned char* sl = smem + o * kSlotBytes;
+            float uv[8], dv[8];
+            ssm::seq::unpack8<bf16>(r + raw_off(c, blk), uv);
+            ssm::seq::unpack8<bf16>(r + kPlaneBytes + raw_off(c, blk), dv);
+            float dt[8], du[8];
+#pragma unroll
+            for (int t = 0; t < 8; t++) {
+                if constexpr (SOFTPLUS) dt[t] = ssm::seq::softplus_log2(fmaf(dv[t], kLog2e, bias));
+                else dt[t] = dv[t] + bias;
+                du[t] = to_tf32(dt[t] * uv[t]);
+            }
+            *reinterpret_cast<float4*>(sl + kmaj(c, 0)) = make_float4(du[0], du[1], du[2], du[3]);
+            *reinterpret_cast<float4*>(sl + kmaj(c, 4)) = make_float4(du[4], du[5], du[6], du[7]);
+            *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 0)) = make_float4(dt[0], dt[1], dt[2], dt[3]);
+            *reinterpret_cast<float4*>(sl + kOffW + kmaj(c, 4)) = make_float4(dt[4], dt[5], dt[6], dt[7]);
+            {   // B and C element c of the block onto the block diagonals
+                const unsigned char* rb = r + kOffTileB + blk * 256;
+                const int t = c >> 4, n = c & 15, row = bcol(t, n);
+                const float bv = __bfloat162float(reinterpret_cast<const bf16*>(rb)[c]);
+                const float cv = __bfloat162float(reinterpret_cast<const bf16*>(rb + kRawBC)[c]);
+                *reinterpret_cast<float*>(sl + kOffBexp + kmaj(row, t)) = bv;
+                *reinterpret_cast<float*>(sl + kOffCexp + kmaj(row, 0)) = cv;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&br.op_full[o]);
+                if (pc.tile_last()) mbar_arrive(&br.raw_empty[rs]);
+            }
+        }
+    } else if (warp >= 8) {
+        // ---------------- recurrence ----------------
+        const int g = (warp - 8) >> 2, q = warp & 3;
+        const int c = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int64_t i = 0;
+        for (int64_t grp = parts.g_last; grp >= parts.g_first; grp--) {
+            int64_t b0, b1;
+            parts.range(grp, b0, b1);
+            const int64_t b = grp / p.groups_per_row;
+            const int64_t d0 = (grp % p.groups_per_row) * kCH;
+            const int64_t row0 = b * p.dim + d0;
+            const bool active = d0 + c < p.dim;
+            float A2[8], h[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++)   // exp(Delta A) = 2^(Delta A log2 e)
+                A2[j] = active ? p.A[(d0 + c) * kN + g * 8 + j] * kLog2e : 0.0f;
+            if (b0 == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) h[j] = 0.0f;
+            } else {
+                if (tid == 256) {
+                    const bool ok = ssm::seq::wait_flag(p.flags + grp);
+                    if (!ok) atomicExch(p.status, kStatusTimeout);
+                    __threadfence();
+                    br.ok = ok;
+                }
+                role_sync(2, 32 * kRecWarps);
+                const bool ok = br.ok;
+                const float* src = p.carry + (grp * kCH + c) * kN + g * 8;
+#pragma unroll
+                for (int j = 0; j < 8; j++) h[j] = ok ? __ldcg(src + j) : __int_as_float(0x7fc00000);
+            }
+            for (int64_t kb = b0; kb < b1; kb++, i++) {
+                const int o = (int)(i % kOpSlots), bf = (int)(i & 1), ys = (int)(i % kYSlots);
+                wait_or_fail(&br.op_full[o], full_parity(i / kOpSlots), br, p);
+                wait_or_fail(&br.d_full[bf], full_parity(i / 2), br, p);
+                __syncwarp();
+                fence_after();
+                const unsigned char* wsl = smem + o * kSlotBytes + kOffW;
+                const float4 dA = *reinterpret_cast<const float4*>(wsl + kmaj(c, 0));
+                const float4 dB = *reinterpret_cast<const float4*>(wsl + kmaj(c, 4));
+                const float dts[8] = {dA.x, dA.y, dA.z, dA.w, dB.x, dB.y, dB.z, dB.w};
+                const uint32_t col = tbase + lane_base + (uint32_t)(bf * 256 + g * 64);
+                uint32_t v[2][16], cv[2][16];
+                SSM_TMEM_LD16(col, v[0]);
+                SSM_TMEM_LD16(col + 128, cv[0]);
+                float yp[8];
+#pragma unroll
+                for (int qt = 0; qt < 4; qt++) {   // two tokens (16 columns) at a time
+                    const int cur = qt & 1;
+                    tmem_wait_ld(v[cur], cv[cur]);
+                    if (qt < 3) {
+                        SSM_TMEM_LD16(col + (qt + 1) * 16, v[cur ^ 1]);
+                        SSM_TMEM_LD16(col + 128 + (qt + 1) * 16, cv[cur ^ 1]);
+                    } else {   // all of the block's bb, Cb and Delta are in registers
+                        fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&br.d_empty[bf]);
+                            mbar_arrive(&br.op_empty[o]);
+                        }
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < 2; tt++) {
+                        const float2 dt2 = make_float2(dts[qt * 2 + tt], dts[qt * 2 + tt]);
+                        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            const float2 e = __fmul2_rn(dt2, make_float2(A2[j], A2[j + 1]));
+                            const float2 a = make_float2(ex2(e.x), ex2(e.y));
+                            const float2 bb = make_float2(__uint_as_float(v[cur][tt * 8 + j]),
+                                                          __uint_as_float(v[cur][tt * 8 + j + 1]));
+                            const float2 hn = __ffma2_rn(a, make_float2(h[j], h[j + 1]), bb);
+                            h[j] = hn.x;
+                            h[j + 1] = hn.y;
+                            acc = __ffma2_rn(make_float2(__uint_as_float(cv[cur][tt * 8 + j]),
+                                                         __uint_as_float(cv[cur][tt * 8 + j + 1])),
+                                             hn, acc);
+                        }
+                        yp[qt * 2 + tt] = acc.x + acc.y;
+                    }
+                }
+                // this half's partial output sums -> the block's slot
+                if (i >= kYSlots) wait_or_fail(&br.yp_empty[ys], empty_parity(i / kYSlots), br, p);
+                float4* ydst = reinterpret_cast<float4*>(smem + kOffY + ys * kYBytes + (g * kCH + c) * kYRow);
+                ydst[0] = make_float4(yp[0], yp[1], yp[2], yp[3]);
+                ydst[1] = make_float4(yp[4], yp[5], yp[6], yp[7]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&br.yp_full[ys]);
+            }
+            // the part's final state
+            if (b1 * kTB == L) {
+                if (active && p.last_state) {
+                    float* dst = p.last_state + (row0 + c) * kN + g * 8;
+#pragma unroll
+                    for (int j = 0; j < 8; j++) dst[j] = h[j];
+                }
+            } else if (b1 > b0) {
+                float* dst = p.carry + (grp * kCH + c) * kN + g * 8;
+#pragma unroll
+                for (int j = 0; j < 8; j++) __stcg(dst + j, h[j]);
+                __threadfence();
+                role_sync(2, 32 * kRecWarps);
+                if (tid == 256)
+                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + grp), "r"(1u)
+                                 : "memory");
+            }
         }
     }
 
     fence_before();
     __syncthreads();
-    if (tid < 32) {
+    if (warp == 0) {
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(sh.taddr),
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(br.taddr),
                      "r"(kTmemCols)
                      : "memory");
     }

@@ -75,8 +75,9 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
 
 // Build-time tuning knobs: a cap on resident scan CTAs per SM (0: as many as
 // fit), and whether bf16 / N = 16 scans take the tensor-core kernel of
-// scan_fwd_tc.cuh (off: its synchronous 8-token pipeline is still slower
-// than the state-split kernel).
+// scan_fwd_tc.cuh (off: its warp-specialised pipeline runs the Mamba-2.8B
+// layer shape in ~605 us against ~450 us for the state-split kernel; it is
+// bound by hand-off latency, not by any pipe).
 #ifndef SSM_SCAN_CTAS_PER_SM
 #define SSM_SCAN_CTAS_PER_SM 0
 #endif
@@ -203,9 +204,48 @@ ScanWorkspace scan_workspace(const ssm_dims* d) {
     return w;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// A (L, dim, batch) bf16 tensor as 16-token x 128-channel boxes with 32-byte
+// swizzle; rows past `dim` read as zero.
+bool encode_plane(CUtensorMap* m, const void* base, int64_t batch, int64_t dim, int64_t L) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t gdim[3] = {(cuuint64_t)L, (cuuint64_t)dim, (cuuint64_t)batch};
+    const cuuint64_t gstride[2] = {(cuuint64_t)L * 2, (cuuint64_t)(dim * L * 2)};
+    const cuuint32_t box[3] = {(cuuint32_t)ssm::tc::kTT, (cuuint32_t)ssm::tc::kCH, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool Z, bool SP>
 int launch_scan_tc(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStream_t stream) {
     using namespace ssm::tc;
+    TmaMaps maps;
+    if (!encode_plane(&maps.u, p.u, p.batch, p.dim, p.L) ||
+        !encode_plane(&maps.delta, p.delta, p.batch, p.dim, p.L) ||
+        !encode_plane(&maps.z, Z ? p.z : p.u, p.batch, p.dim, p.L))
+        return SSM_ERR_CUDA;
     auto kern = scan_fwd_tc_kernel<Z, SP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
         cudaSuccess)
@@ -229,7 +269,7 @@ int launch_scan_tc(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStre
     p.flags = reinterpret_cast<unsigned*>(ws + wl.flags_off);
     p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
     if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
-    kern<<<(unsigned)ctas, kThreads, kSmem, stream>>>(p);
+    kern<<<(unsigned)ctas, kThreads, kSmem, stream>>>(p, maps);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
