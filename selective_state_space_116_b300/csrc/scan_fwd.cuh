@@ -226,40 +226,99 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// One token for one thread, B and C read as bf16 straight from the raw tile
-// (S = 8: one 16-byte load each; S = 4: one 8-byte load each).  bf16 -> fp32
-// is exact, so this matches token_step bit for bit.
-template <int S>
-__device__ __forceinline__ float token_step_raw(float dt, float dtx, const unsigned char* __restrict__ braw,
-                                                const unsigned char* __restrict__ craw,
-                                                float (&h)[S], const float (&A2)[S]) {
-    static_assert(S == 8 || S == 4, "raw B/C steps take 4 or 8 states");
-    unsigned bw[S / 2], cw[S / 2];
-    if constexpr (S == 8) {
-        const uint4 b4 = *reinterpret_cast<const uint4*>(braw);
-        const uint4 c4 = *reinterpret_cast<const uint4*>(craw);
-        bw[0] = b4.x; bw[1] = b4.y; bw[2] = b4.z; bw[3] = b4.w;
-        cw[0] = c4.x; cw[1] = c4.y; cw[2] = c4.z; cw[3] = c4.w;
-    } else {
-        const uint2 b2 = *reinterpret_cast<const uint2*>(braw);
-        const uint2 c2 = *reinterpret_cast<const uint2*>(craw);
-        bw[0] = b2.x; bw[1] = b2.y;
-        cw[0] = c2.x; cw[1] = c2.y;
-    }
-    const float2 dt2 = make_float2(dt, dt);
-    const float2 dtx2 = make_float2(dtx, dtx);
-    float2 acc = make_float2(0.0f, 0.0f);
+// NT consecutive tokens for one thread, software-pipelined: the B, C loads
+// and the 2^x of token t + 1 are issued before the state update of token t,
+// so the exponentials overlap the FMA chain instead of following it.  Same
+// operations as token_step, in the same order per token: bit-identical.
+// wrow: (Delta, Delta u) pairs, two tokens per float4; bcf: B (S floats) then
+// C (S floats) of this thread's states, BCT floats per token; yrow: NT
+// partial outputs (16-byte aligned).
+// RAW: B and C are bf16 rows of the raw tile instead (bcf then points at this
+// thread's B states, C follows RAW_C bytes on, BCT bytes per token; S = 4 or
+// 8), unpacked exactly in registers.
+template <int S, int BCT, int NT, bool RAW = false, int RAW_C = 0>
+__device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, const void* __restrict__ bcp,
+                                            float (&h)[S], const float (&A2)[S], float* __restrict__ yrow) {
+    static_assert(S % 4 == 0 && NT % 4 == 0, "scan_tokens takes S and NT multiples of 4");
+    static_assert(!RAW || S == 4 || S == 8, "raw B/C rows take 4 or 8 states");
+    float a_n[S], B_n[S], C_n[S];
+    float dt_n, dtx_n;
+    float4 wq = wrow[0];
+    auto fetch = [&](int t) {   // inputs and exponentials of token t
+        if (t % 2 == 0) {
+            wq = wrow[t / 2];
+            dt_n = wq.x;
+            dtx_n = wq.y;
+        } else {
+            dt_n = wq.z;
+            dtx_n = wq.w;
+        }
+        if constexpr (RAW) {
+            const unsigned char* bc = static_cast<const unsigned char*>(bcp) + t * BCT;
+            unsigned bw[S / 2], cw[S / 2];
+            if constexpr (S == 8) {
+                const uint4 b4 = *reinterpret_cast<const uint4*>(bc);
+                const uint4 c4 = *reinterpret_cast<const uint4*>(bc + RAW_C);
+                bw[0] = b4.x; bw[1] = b4.y; bw[2] = b4.z; bw[3] = b4.w;
+                cw[0] = c4.x; cw[1] = c4.y; cw[2] = c4.z; cw[3] = c4.w;
+            } else {
+                const uint2 b2 = *reinterpret_cast<const uint2*>(bc);
+                const uint2 c2 = *reinterpret_cast<const uint2*>(bc + RAW_C);
+                bw[0] = b2.x; bw[1] = b2.y;
+                cw[0] = c2.x; cw[1] = c2.y;
+            }
 #pragma unroll
-    for (int n = 0; n < S; n += 2) {
-        const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
-        const float2 a = make_float2(ex2(e.x), ex2(e.y));
-        const float2 bb = __fmul2_rn(dtx2, bf2_to_f2(bw[n / 2]));
-        const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
-        h[n] = hn.x;
-        h[n + 1] = hn.y;
-        acc = __ffma2_rn(bf2_to_f2(cw[n / 2]), hn, acc);
+            for (int n = 0; n < S; n += 2) {
+                const float2 bf = bf2_to_f2(bw[n / 2]), cf = bf2_to_f2(cw[n / 2]);
+                B_n[n] = bf.x; B_n[n + 1] = bf.y;
+                C_n[n] = cf.x; C_n[n + 1] = cf.y;
+            }
+        } else {
+            const float* bc = static_cast<const float*>(bcp) + t * BCT;
+#pragma unroll
+            for (int n = 0; n < S; n += 4) {
+                const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
+                const float4 c4 = *reinterpret_cast<const float4*>(bc + S + n);
+                B_n[n] = b4.x; B_n[n + 1] = b4.y; B_n[n + 2] = b4.z; B_n[n + 3] = b4.w;
+                C_n[n] = c4.x; C_n[n + 1] = c4.y; C_n[n + 2] = c4.z; C_n[n + 3] = c4.w;
+            }
+        }
+        const float2 dt2 = make_float2(dt_n, dt_n);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
+            a_n[n] = ex2(e.x);
+            a_n[n + 1] = ex2(e.y);
+        }
+    };
+    fetch(0);
+    float4 out;
+#pragma unroll
+    for (int t = 0; t < NT; t++) {
+        float a[S], Bv[S], Cv[S];
+#pragma unroll
+        for (int n = 0; n < S; n++) { a[n] = a_n[n]; Bv[n] = B_n[n]; Cv[n] = C_n[n]; }
+        const float dtx = dtx_n;
+        if (t + 1 < NT) fetch(t + 1);
+        const float2 dtx2 = make_float2(dtx, dtx);
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 hn = __ffma2_rn(make_float2(a[n], a[n + 1]), make_float2(h[n], h[n + 1]), bb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+            acc = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc);
+        }
+        const float yv = acc.x + acc.y;
+        if (t % 4 == 0) out.x = yv;
+        if (t % 4 == 1) out.y = yv;
+        if (t % 4 == 2) out.z = yv;
+        if (t % 4 == 3) {
+            out.w = yv;
+            *reinterpret_cast<float4*>(yrow + t - 3) = out;
+        }
     }
-    return acc.x + acc.y;
 }
 
 // One token for one thread: advance S states, return the partial C.h.
@@ -363,9 +422,9 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     using Sh = Shape<T, N, S, HAS_Z>;
     constexpr int G = Sh::G, CH = Sh::CH;
     // bf16 B and C read by the recurrence straight from the raw tile (S = 4:
-    // one 8-byte load each, no fp32 staging pass; measured 9% faster on the
-    // Mamba-130M layer shape.  At S = 8 the extra unpacking made the Mamba-2.8B
-    // shape 3% slower, so S = 8 keeps the fp32 staging.)
+    // one 8-byte load each, no fp32 staging pass; the Mamba-130M layer shape
+    // runs 168 -> 156 us.  At S = 8 the extra unpacking made the Mamba-2.8B
+    // shape 5% slower, 428 -> 450 us, so S = 8 keeps the fp32 staging.)
     constexpr bool RAW_BC = std::is_same<T, __nv_bfloat16>::value && VEC && S == 4 && !AGG;
 
     const int64_t b = grp / p.groups_per_row;
@@ -506,19 +565,8 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         if constexpr (RAW_BC && !AGG) {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const unsigned char* braw = buf + Sh::NPLANES * Sh::RAW_PLANE + g * S * 2;
-            const unsigned char* craw = braw + Sh::BC_RAW;
             float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
-#pragma unroll 2
-            for (int t = 0; t < kTL; t += 4) {
-                const float4 w01 = wrow[t / 2];
-                const float4 w23 = wrow[t / 2 + 1];
-                float4 out;
-                out.x = token_step_raw<S>(w01.x, w01.y, braw + (t + 0) * N * 2, craw + (t + 0) * N * 2, h, A2);
-                out.y = token_step_raw<S>(w01.z, w01.w, braw + (t + 1) * N * 2, craw + (t + 1) * N * 2, h, A2);
-                out.z = token_step_raw<S>(w23.x, w23.y, braw + (t + 2) * N * 2, craw + (t + 2) * N * 2, h, A2);
-                out.w = token_step_raw<S>(w23.z, w23.w, braw + (t + 3) * N * 2, craw + (t + 3) * N * 2, h, A2);
-                *reinterpret_cast<float4*>(yrow + t) = out;
-            }
+            scan_tokens<S, N * 2, kTL, true, Sh::BC_RAW>(wrow, braw, h, A2, yrow);
         } else if constexpr (AGG) {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
@@ -533,6 +581,11 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             const float yk = tsum - dcomp, tk = dsum + yk;
             dcomp = (tk - dsum) - yk;
             dsum = tk;
+        } else if constexpr (S % 4 == 0) {
+            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
+            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
+            float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
+            scan_tokens<S, G * 2 * S, kTL>(wrow, bcf, h, A2, yrow);
         } else {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;

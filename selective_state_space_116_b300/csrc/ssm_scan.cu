@@ -12,6 +12,7 @@
 #include "probe.cuh"
 #include "scan_fwd.cuh"
 #include "scan_fwd_tc.cuh"
+#include "scan_fwd_ws.cuh"
 #include "state_step.cuh"
 
 namespace {
@@ -83,6 +84,12 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
 #endif
 #ifndef SSM_SCAN_TC
 #define SSM_SCAN_TC 0
+#endif
+// whether bf16 / N = 16 scans with L % 16 == 0 take the warp-specialised
+// state-split kernel of scan_fwd_ws.cuh (off: 423 us against 428 us at the
+// Mamba-2.8B layer shape, but 198 us against 156 us at the Mamba-130M one)
+#ifndef SSM_SCAN_WS
+#define SSM_SCAN_WS 0
 #endif
 
 // Workspace of the scan: a 256-byte header (status word), one flag per
@@ -187,6 +194,13 @@ bool tc_shape(const ssm_dims* d) {
     return SSM_SCAN_TC && d->io == SSM_IO_BF16 && d->dstate == 16 && d->seqlen > 0 && d->seqlen % 8 == 0;
 }
 
+// The warp-specialised kernel serves the same shapes with L a whole number of
+// its 16-token blocks, unless the chunked schedule takes the call.
+bool ws_shape(const ssm_dims* d) {
+    return SSM_SCAN_WS && d->io == SSM_IO_BF16 && d->dstate == 16 && d->seqlen > 0 &&
+           d->seqlen % 16 == 0 && !chunk_plan(d).on;
+}
+
 // The workspace covers whichever kernel and split the call selects.
 ScanWorkspace scan_workspace(const ssm_dims* d) {
     const int n = (int)d->dstate;
@@ -197,6 +211,10 @@ ScanWorkspace scan_workspace(const ssm_dims* d) {
     }
     if (tc_shape(d)) {
         const ScanWorkspace t = scan_workspace_for(d, ssm::tc::kCH);
+        if (t.total > w.total) w = t;
+    }
+    if (ws_shape(d)) {
+        const ScanWorkspace t = scan_workspace_for(d, ssm::ws::kCH);
         if (t.total > w.total) w = t;
     }
     const ScanWorkspace cw = chunk_workspace(chunk_plan(d), n);
@@ -258,6 +276,41 @@ int launch_scan_tc(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStre
     int sms = 0;
     if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
     int64_t ctas = sms;   // one CTA per SM: each holds all of its tensor memory
+    if (ctas > p.ngroups) ctas = p.ngroups;
+    if (chunk > 0) {
+        const int64_t per = (chunk + kTB - 1) / kTB;
+        const int64_t want = (p.ngroups * p.ntiles + per - 1) / per;
+        if (want < ctas) ctas = want;
+    }
+    if (ctas < 1) ctas = 1;
+    p.status = reinterpret_cast<int*>(ws);
+    p.flags = reinterpret_cast<unsigned*>(ws + wl.flags_off);
+    p.carry = reinterpret_cast<float*>(ws + wl.carry_off);
+    if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    kern<<<(unsigned)ctas, kThreads, kSmem, stream>>>(p, maps);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <bool Z, bool SP>
+int launch_scan_ws(ssm::ScanParams p, int64_t chunk, unsigned char* ws, cudaStream_t stream) {
+    using namespace ssm::ws;
+    TmaMaps maps;
+    if (!encode_plane(&maps.u, p.u, p.batch, p.dim, p.L) ||
+        !encode_plane(&maps.delta, p.delta, p.batch, p.dim, p.L) ||
+        !encode_plane(&maps.z, Z ? p.z : p.u, p.batch, p.dim, p.L))
+        return SSM_ERR_CUDA;
+    auto kern = scan_fwd_ws_kernel<Z, SP>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+        return SSM_ERR_CUDA;
+    ssm_dims d{p.batch, p.dim, 16, p.L, SSM_IO_BF16, 0};
+    const ScanWorkspace wl = scan_workspace_for(&d, kCH);
+    p.groups_per_row = (p.dim + kCH - 1) / kCH;
+    p.ngroups = p.batch * p.groups_per_row;
+    p.ntiles = p.L / kTB;   // in 16-token blocks
+    int sms = 0;
+    if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
+    int64_t ctas = sms;   // one CTA per SM (its shared memory)
     if (ctas > p.ngroups) ctas = p.ngroups;
     if (chunk > 0) {
         const int64_t per = (chunk + kTB - 1) / kTB;
@@ -560,6 +613,13 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int sms = 0;
     if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
+    if (vec && ws_shape(dims)) {
+        const bool zz = z != nullptr;
+        if (zz && sp) return launch_scan_ws<true, true>(p, dims->chunk, ws, st);
+        if (zz) return launch_scan_ws<true, false>(p, dims->chunk, ws, st);
+        if (sp) return launch_scan_ws<false, true>(p, dims->chunk, ws, st);
+        return launch_scan_ws<false, false>(p, dims->chunk, ws, st);
+    }
     if (vec && tc_shape(dims)) {
         const bool zz = z != nullptr;
         if (zz && sp) return launch_scan_tc<true, true>(p, dims->chunk, ws, st);
