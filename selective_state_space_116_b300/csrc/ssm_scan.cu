@@ -86,8 +86,7 @@ int check_dims(const ssm_dims* dims, bool scan, Sizes* s) {
 #define SSM_SCAN_TC 0
 #endif
 // whether bf16 / N = 16 scans with L % 16 == 0 take the warp-specialised
-// state-split kernel of scan_fwd_ws.cuh (off: 423 us against 428 us at the
-// Mamba-2.8B layer shape, but 198 us against 156 us at the Mamba-130M one)
+// state-split kernel of scan_fwd_ws.cuh
 #ifndef SSM_SCAN_WS
 #define SSM_SCAN_WS 0
 #endif
