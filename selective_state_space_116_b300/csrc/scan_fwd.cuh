@@ -321,6 +321,63 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
     }
 }
 
+// The aggregate pass's token loop (state only: no C, no output), pipelined
+// like scan_tokens; returns the tile's sum of Delta, added pairwise in token
+// order exactly as the unpipelined loop does.
+template <int S, int BCT, int NT>
+__device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wrow,
+                                                   const float* __restrict__ bcf, float (&h)[S],
+                                                   const float (&A2)[S]) {
+    static_assert(S % 4 == 0 && NT % 2 == 0, "scan_tokens_state takes S % 4 == 0, even NT");
+    float a_n[S], B_n[S];
+    float dtx_n;
+    float4 wq = wrow[0];
+    float tsum = 0.0f;
+    auto fetch = [&](int t) {
+        float dt;
+        if (t % 2 == 0) {
+            wq = wrow[t / 2];
+            dt = wq.x;
+            dtx_n = wq.y;
+            tsum += wq.x + wq.z;
+        } else {
+            dt = wq.z;
+            dtx_n = wq.w;
+        }
+        const float* bc = bcf + t * BCT;
+#pragma unroll
+        for (int n = 0; n < S; n += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
+            B_n[n] = b4.x; B_n[n + 1] = b4.y; B_n[n + 2] = b4.z; B_n[n + 3] = b4.w;
+        }
+        const float2 dt2 = make_float2(dt, dt);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
+            a_n[n] = ex2(e.x);
+            a_n[n + 1] = ex2(e.y);
+        }
+    };
+    fetch(0);
+#pragma unroll
+    for (int t = 0; t < NT; t++) {
+        float a[S], Bv[S];
+#pragma unroll
+        for (int n = 0; n < S; n++) { a[n] = a_n[n]; Bv[n] = B_n[n]; }
+        const float dtx = dtx_n;
+        if (t + 1 < NT) fetch(t + 1);
+        const float2 dtx2 = make_float2(dtx, dtx);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 hn = __ffma2_rn(make_float2(a[n], a[n + 1]), make_float2(h[n], h[n + 1]), bb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+        }
+    }
+    return tsum;
+}
+
 // One token for one thread: advance S states, return the partial C.h.
 template <int S>
 __device__ __forceinline__ float token_step(float dt, float dtx, const float* __restrict__ bc,
@@ -567,6 +624,13 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             const unsigned char* braw = buf + Sh::NPLANES * Sh::RAW_PLANE + g * S * 2;
             float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
             scan_tokens<S, N * 2, kTL, true, Sh::BC_RAW>(wrow, braw, h, A2, yrow);
+        } else if constexpr (AGG && S % 4 == 0) {
+            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
+            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
+            const float tsum = scan_tokens_state<S, G * 2 * S, kTL>(wrow, bcf, h, A2);
+            const float yk = tsum - dcomp, tk = dsum + yk;
+            dcomp = (tk - dsum) - yk;
+            dsum = tk;
         } else if constexpr (AGG) {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
