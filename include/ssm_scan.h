@@ -148,6 +148,32 @@ SSM_API int ssm_scan_fwd(const ssm_dims* dims,
 SSM_API int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes);
 
 /*
+ * ssm_scan_fwd on HOST buffers: every pointer (u, delta, A, B, C, D, z,
+ * delta_bias, y, last_state) is host memory, with the layouts and meanings of
+ * ssm_scan_fwd.  The call takes device memory on the current device with
+ * cudaMallocAsync on `stream` (returned with cudaFreeAsync when the work is
+ * done) and cuts the problem into slices (a batch row, or a range of its
+ * channels) whose copies in, scans and copies out overlap on two internal
+ * streams of the library joined to `stream` by events; one cudaMemcpyAsync
+ * per tensor per slice.  It returns once everything is enqueued: the outputs
+ * are valid, and the host buffers may be reused, when `stream` has completed
+ * (e.g. cudaStreamSynchronize).  Pinned host memory (cudaHostAlloc,
+ * cudaHostRegister) lets the copies run asynchronously and overlap; pageable
+ * memory gives the same results with copies staged by the driver.  Each
+ * slice's scan is ssm_scan_fwd over the slice, so the outputs equal those of
+ * ssm_scan_fwd on device copies of the inputs bit for bit whenever the same
+ * kernel serves both (it does except where the full problem would have taken
+ * the chunked long-sequence schedule).  Returns SSM_OK or a negative
+ * ssm_status; SSM_ERR_CUDA when an allocation or an enqueue fails (after
+ * waiting for what was already enqueued).
+ */
+SSM_API int ssm_scan_fwd_host(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 void* y, float* last_state, void* stream);
+
+/*
  * ssm_scan_fwd without a workspace argument, for callers that cannot allocate
  * device memory when they call the scan (for example an inference engine's
  * plugin confined to a memory plan fixed in advance, or a real-time path

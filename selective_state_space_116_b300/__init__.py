@@ -5,9 +5,10 @@ torch tensors into raw pointers and call the C ABI of include/ssm_scan.h
 with the same names.  Every step of the scan runs in the library's CUDA
 kernels; PyTorch only supplies device memory and the current stream.
 
-Host (CPU) tensors are accepted as well: they are copied to the current CUDA
-device on the current stream, the scan runs there, and the outputs are
-copied back into host tensors (pinned when the inputs were pinned).
+Host (CPU) tensors are accepted as well: they go to ssm_scan_fwd_host, which
+copies them to the current CUDA device slice by slice, overlapping the copies
+with the scans on the current stream, and copies the outputs back into host
+tensors (pinned when the inputs were pinned).
 """
 from __future__ import annotations
 
@@ -57,10 +58,6 @@ def _check(t, name, shape, dtype, device, optional=False):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _to_device(tensors: dict, device):
-    return {k: (None if v is None else v.to(device, non_blocking=True)) for k, v in tensors.items()}
-
-
 def _host_like(t, pinned):
     return torch.empty(t.shape, dtype=t.dtype, pin_memory=pinned)
 
@@ -79,6 +76,47 @@ def ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen, dtype=torch.bfloat16
     return int(out.value)
 
 
+def _scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state,
+                   y, last_state, chunk):
+    """Host tensors: ssm_scan_fwd_host of the library (copies in, scans and
+    copies out overlapped slice by slice) on the current CUDA device and
+    stream; returns once the outputs are in the host tensors."""
+    cpu = torch.device("cpu")
+    if u.dim() != 3 or A.dim() != 2:
+        raise ValueError("u must be (batch, dim, L) and A (dim, N)")
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    if io not in _IO:
+        raise TypeError(f"unsupported I/O dtype {io}; use float32 or bfloat16")
+    _check(u, "u", (batch, dim, L), io, cpu)
+    _check(delta, "delta", (batch, dim, L), io, cpu)
+    _check(A, "A", (dim, N), torch.float32, cpu)
+    _check(B, "B", (batch, L, N), io, cpu)
+    _check(C, "C", (batch, L, N), io, cpu)
+    _check(D, "D", (dim,), torch.float32, cpu, optional=True)
+    _check(z, "z", (batch, dim, L), io, cpu, optional=True)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, cpu, optional=True)
+    pinned = u.is_pinned()
+    if y is None:
+        y = _host_like(u, pinned)
+    _check(y, "y", (batch, dim, L), io, cpu)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((batch, dim, N), dtype=torch.float32, pin_memory=pinned)
+    if last_state is not None:
+        _check(last_state, "last_state", (batch, dim, N), torch.float32, cpu)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream(dev)
+    d = _dims(batch, dim, N, L, _IO[io], chunk)
+    rc = _lib.load().ssm_scan_fwd_host(
+        ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), 1 if delta_softplus else 0, _ptr(y), _ptr(last_state), st.cuda_stream)
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_fwd_host")
+    st.synchronize()
+    return y, last_state
+
+
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
                  return_last_state=True, y=None, last_state=None, workspace=None, chunk=0):
     """Forward selective scan.
@@ -89,20 +127,8 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     ``y``/``last_state``/``workspace`` may be passed preallocated.
     """
     if u.device.type == "cpu":
-        dev = torch.device("cuda", torch.cuda.current_device())
-        pinned = u.is_pinned()
-        g = _to_device(dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=delta_bias), dev)
-        yd, hd = ssm_scan_fwd(**g, delta_softplus=delta_softplus,
-                              return_last_state=return_last_state, chunk=chunk)
-        y_h = _host_like(yd, pinned) if y is None else y
-        y_h.copy_(yd, non_blocking=pinned)
-        h_h = None
-        if hd is not None:
-            h_h = _host_like(hd, pinned) if last_state is None else last_state
-            h_h.copy_(hd, non_blocking=pinned)
-        if pinned:
-            torch.cuda.current_stream(dev).synchronize()
-        return y_h, h_h
+        return _scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus,
+                              return_last_state, y, last_state, chunk)
 
     device = u.device
     if device.type != "cuda":

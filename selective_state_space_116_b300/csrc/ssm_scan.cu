@@ -459,7 +459,7 @@ int dispatch_chunked_n(const ssm::ScanParams& p, const ChunkPlan& c, bool z, boo
 
 template <typename T>
 int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool z, bool sp, bool vec,
-                  unsigned char* ws, int sms, cudaStream_t s) {
+                  unsigned char* ws, int sms, cudaStream_t s, int split) {
     const int64_t chunk = d->chunk;
     const ChunkPlan cp = chunk_plan(d);
     if (cp.on) {
@@ -478,7 +478,8 @@ int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool z, bool sp, 
         case 4: return dispatch_scan_n<T, 4, 4>(p, chunk, z, sp, vec, ws, sms, s);
         case 8: return dispatch_scan_n<T, 8, 8>(p, chunk, z, sp, vec, ws, sms, s);
         case 16:
-            if (n16_split(d, sms) == 8) return dispatch_scan_n<T, 16, 8>(p, chunk, z, sp, vec, ws, sms, s);
+            if ((split ? split : n16_split(d, sms)) == 8)
+                return dispatch_scan_n<T, 16, 8>(p, chunk, z, sp, vec, ws, sms, s);
             return dispatch_scan_n<T, 16, 4>(p, chunk, z, sp, vec, ws, sms, s);
     }
     return SSM_ERR_UNSUPPORTED_N;
@@ -524,49 +525,15 @@ int dispatch_step(const ssm::StepParams& p, int64_t n, bool z, bool sp, bool vec
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int ssm_version(void) { return kVersion; }
-
-const char* ssm_status_string(int status) {
-    switch (status) {
-        case SSM_OK: return "ok";
-        case SSM_ERR_NULL_ARG: return "a required pointer is NULL";
-        case SSM_ERR_BAD_DIMS: return "a size is out of range or overflows";
-        case SSM_ERR_UNSUPPORTED_N: return "dstate must be 1, 2, 4, 8 or 16";
-        case SSM_ERR_BAD_DTYPE: return "unknown I/O element type";
-        case SSM_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
-        case SSM_ERR_CUDA: return "the CUDA runtime refused the launch";
-        case SSM_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
-        case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
-        case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
-        case SSM_ERR_TOO_LARGE:
-            return "the problem needs more scratch than the library's built-in buffer holds";
-    }
-    return "unknown status";
-}
-
-int ssm_probe_ex2(int32_t blocks, int32_t threads, int32_t iters, float* sink, void* stream) {
-    if (!sink) return SSM_ERR_NULL_ARG;
-    if (blocks < 1 || iters < 1 || threads < 32 || threads > 1024 || threads % 32 != 0)
-        return SSM_ERR_BAD_DIMS;
-    ssm::probe_ex2_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, sink);
-    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
-}
-
-int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
-    Sizes s;
-    const int rc = check_dims(dims, true, &s);
-    if (rc != SSM_OK) return rc;
-    if (!bytes) return SSM_ERR_NULL_ARG;
-    *bytes = scan_workspace(dims).total;
-    return SSM_OK;
-}
-
-int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
-                 const void* B, const void* C, const float* D, const void* z,
-                 const float* delta_bias, int delta_softplus, void* y, float* last_state,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+// The scan; split (N = 16 only): 0 picks the state split from the sizes, 4 or
+// 8 forces it (the host entry point keeps its slices on the full problem's
+// choice).
+int scan_fwd_impl(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                  const void* B, const void* C, const float* D, const void* z,
+                  const float* delta_bias, int delta_softplus, void* y, float* last_state,
+                  void* workspace, size_t workspace_bytes, void* stream, int split) {
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
@@ -627,8 +594,57 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
         return launch_scan_tc<false, false>(p, dims->chunk, ws, st);
     }
     if (dims->io == SSM_IO_BF16)
-        return dispatch_scan<bf16>(dims, p, z != nullptr, sp, vec, ws, sms, st);
-    return dispatch_scan<float>(dims, p, z != nullptr, sp, vec, ws, sms, st);
+        return dispatch_scan<bf16>(dims, p, z != nullptr, sp, vec, ws, sms, st, split);
+    return dispatch_scan<float>(dims, p, z != nullptr, sp, vec, ws, sms, st, split);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_version(void) { return kVersion; }
+
+const char* ssm_status_string(int status) {
+    switch (status) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_NULL_ARG: return "a required pointer is NULL";
+        case SSM_ERR_BAD_DIMS: return "a size is out of range or overflows";
+        case SSM_ERR_UNSUPPORTED_N: return "dstate must be 1, 2, 4, 8 or 16";
+        case SSM_ERR_BAD_DTYPE: return "unknown I/O element type";
+        case SSM_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
+        case SSM_ERR_CUDA: return "the CUDA runtime refused the launch";
+        case SSM_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
+        case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
+        case SSM_ERR_TOO_LARGE:
+            return "the problem needs more scratch than the library's built-in buffer holds";
+    }
+    return "unknown status";
+}
+
+int ssm_probe_ex2(int32_t blocks, int32_t threads, int32_t iters, float* sink, void* stream) {
+    if (!sink) return SSM_ERR_NULL_ARG;
+    if (blocks < 1 || iters < 1 || threads < 32 || threads > 1024 || threads % 32 != 0)
+        return SSM_ERR_BAD_DIMS;
+    ssm::probe_ex2_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, sink);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
+    Sizes s;
+    const int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    if (!bytes) return SSM_ERR_NULL_ARG;
+    *bytes = scan_workspace(dims).total;
+    return SSM_OK;
+}
+
+int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus, void* y, float* last_state,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    return scan_fwd_impl(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                         workspace, workspace_bytes, stream, 0);
 }
 
 int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void* delta,
@@ -659,6 +675,189 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dims->io == SSM_IO_BF16) return dispatch_step<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
     return dispatch_step<float>(p, dims->dstate, z != nullptr, sp, vec, st);
+}
+
+// ---------------------------------------------------------------------------
+// Forward scan from host buffers.
+//
+// Batch rows, and channel ranges within a row, are independent scans, so the
+// problem is cut into slices (one batch row, or a range of its channels,
+// each) that pass through three streams: copy in (H2D) on one, the scan on
+// the caller's stream, copy out (D2H) on a third, with two sets of device
+// buffers.  Slice k's copy in overlaps slice k-1's scan and slice k-2's copy
+// out; with pinned host memory the time approaches that of the copies in.
+
+}  // extern "C"
+
+namespace {
+
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+std::mutex g_host_mu;
+HostStreams g_host_streams[64];
+
+int host_streams(HostStreams* hs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostStreams& h = g_host_streams[dev];
+    if (!h.in) {
+        if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaStreamDestroy(h.in);
+            h.in = nullptr;
+            return SSM_ERR_CUDA;
+        }
+    }
+    *hs = h;
+    return SSM_OK;
+}
+
+// Events of one call: the copies in of a buffer set done, its scan done, its
+// copies out done; plus the start fence.
+struct HostEvents {
+    cudaEvent_t ev[7] = {};
+    int n = 0;
+    ~HostEvents() {
+        for (int i = 0; i < n; i++) cudaEventDestroy(ev[i]);
+    }
+    bool make() {
+        for (n = 0; n < 7; n++)
+            if (cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming) != cudaSuccess) return false;
+        return true;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_fwd_host(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                      const void* B, const void* C, const float* D, const void* z,
+                      const float* delta_bias, int delta_softplus, void* y, float* last_state,
+                      void* stream) {
+    Sizes s;
+    int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    const bool empty = dims->seqlen == 0;
+    if (!A || (!empty && (!u || !delta || !B || !C || !y))) return SSM_ERR_NULL_ARG;
+    const size_t es = io_size(dims->io);
+    const int64_t batch = dims->batch, dim = dims->dim, N = dims->dstate, L = dims->seqlen;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // slices: every batch row cut into `parts` channel ranges, at least 16
+    // slices in all when the rows allow it (the pipeline's fill and drain
+    // cost about one slice's copies and scan)
+    int64_t parts = (16 + batch - 1) / batch;
+    if (parts > dim) parts = dim;
+    const int64_t cw = (dim + parts - 1) / parts;   // channels per slice (the last may be fewer)
+    parts = (dim + cw - 1) / cw;
+    const int64_t nslices = batch * parts;
+
+    // the slices take the kernel the whole problem would: its state split and
+    // its chunk boundaries (or no chunking), so the outputs are the same
+    int sms = 0;
+    if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
+    const ChunkPlan full = chunk_plan(dims);
+    int64_t sc = dims->chunk;
+    if (full.on) sc = full.tpc * ssm::seq::kTL;
+    else if (sc == 0) sc = L;
+    const int32_t slice_chunk = (int32_t)(sc > INT32_MAX ? INT32_MAX : sc);
+    const int split = (N == 16 && !full.on) ? n16_split(dims, sms) : 0;
+
+    ssm_dims sd{1, cw, N, L, dims->io, slice_chunk};
+    size_t ws_bytes = 0;
+    if ((rc = ssm_scan_fwd_workspace_size(&sd, &ws_bytes)) != SSM_OK) return rc;
+
+    // device layout: parameters, workspace, then two buffer sets
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t seq_b = (size_t)cw * L * es, bc_b = (size_t)L * N * es, st_b = (size_t)cw * N * 4;
+    const size_t off_A = 0, off_D = up(off_A + (size_t)dim * N * 4), off_bias = up(off_D + (size_t)dim * 4);
+    const size_t off_ws = up(off_bias + (size_t)dim * 4);
+    const size_t off_set = up(off_ws + ws_bytes);
+    const size_t o_u = 0, o_dl = up(seq_b), o_z = o_dl + up(seq_b), o_B = o_z + up(seq_b),
+                 o_C = o_B + up(bc_b), o_y = o_C + up(bc_b), o_h = o_y + up(seq_b);
+    const size_t set_b = o_h + up(st_b);
+    const size_t total = off_set + 2 * set_b;
+
+    HostStreams hs;
+    if ((rc = host_streams(&hs)) != SSM_OK) return rc;
+    HostEvents he;
+    if (!he.make()) return SSM_ERR_CUDA;
+    cudaEvent_t ev_in[2] = {he.ev[0], he.ev[1]}, ev_scan[2] = {he.ev[2], he.ev[3]},
+                ev_out[2] = {he.ev[4], he.ev[5]}, ev_start = he.ev[6];
+
+    unsigned char* dev = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&dev), total, st) != cudaSuccess) return SSM_ERR_CUDA;
+    bool ok = cudaEventRecord(ev_start, st) == cudaSuccess &&
+              cudaStreamWaitEvent(hs.in, ev_start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(hs.out, ev_start, 0) == cudaSuccess;
+    float* dA = reinterpret_cast<float*>(dev + off_A);
+    float* dD = D ? reinterpret_cast<float*>(dev + off_D) : nullptr;
+    float* dbias = delta_bias ? reinterpret_cast<float*>(dev + off_bias) : nullptr;
+    ok = ok && cudaMemcpyAsync(dA, A, (size_t)dim * N * 4, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+    if (D) ok = ok && cudaMemcpyAsync(dD, D, (size_t)dim * 4, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+    if (delta_bias)
+        ok = ok && cudaMemcpyAsync(dbias, delta_bias, (size_t)dim * 4, cudaMemcpyHostToDevice, hs.in) ==
+                       cudaSuccess;
+
+    const unsigned char* hu = static_cast<const unsigned char*>(u);
+    const unsigned char* hdl = static_cast<const unsigned char*>(delta);
+    const unsigned char* hz = static_cast<const unsigned char*>(z);
+    const unsigned char* hB = static_cast<const unsigned char*>(B);
+    const unsigned char* hC = static_cast<const unsigned char*>(C);
+    unsigned char* hy = static_cast<unsigned char*>(y);
+    for (int64_t k = 0; ok && k < nslices; k++) {
+        const int set = (int)(k & 1);
+        const int64_t b = k / parts, d0 = (k % parts) * cw;
+        const int64_t w = dim - d0 < cw ? dim - d0 : cw;   // channels of this slice
+        unsigned char* sb = dev + off_set + set * set_b;
+        const size_t row = (size_t)(b * dim + d0);         // first flat (b, d) row
+        const size_t nseq = (size_t)w * L * es;
+        // copy in, once the set's previous slice has been copied out
+        if (k >= 2) ok = ok && cudaStreamWaitEvent(hs.in, ev_out[set], 0) == cudaSuccess;
+        if (nseq > 0) {
+            ok = ok && cudaMemcpyAsync(sb + o_u, hu + row * L * es, nseq, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+            ok = ok && cudaMemcpyAsync(sb + o_dl, hdl + row * L * es, nseq, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+            if (z) ok = ok && cudaMemcpyAsync(sb + o_z, hz + row * L * es, nseq, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+            ok = ok && cudaMemcpyAsync(sb + o_B, hB + (size_t)b * L * N * es, bc_b, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+            ok = ok && cudaMemcpyAsync(sb + o_C, hC + (size_t)b * L * N * es, bc_b, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
+        }
+        ok = ok && cudaEventRecord(ev_in[set], hs.in) == cudaSuccess;
+        // the scan of the slice
+        ok = ok && cudaStreamWaitEvent(st, ev_in[set], 0) == cudaSuccess;
+        if (ok) {
+            ssm_dims d1{1, w, N, L, dims->io, slice_chunk};
+            rc = scan_fwd_impl(&d1, sb + o_u, sb + o_dl, dA + d0 * N, sb + o_B, sb + o_C,
+                              dD ? dD + d0 : nullptr, z ? sb + o_z : nullptr, dbias ? dbias + d0 : nullptr,
+                              delta_softplus, sb + o_y, last_state ? reinterpret_cast<float*>(sb + o_h) : nullptr,
+                              ws_bytes ? dev + off_ws : nullptr, ws_bytes, st, split);
+            ok = rc == SSM_OK;
+        }
+        ok = ok && cudaEventRecord(ev_scan[set], st) == cudaSuccess;
+        // copy out
+        ok = ok && cudaStreamWaitEvent(hs.out, ev_scan[set], 0) == cudaSuccess;
+        if (nseq > 0)
+            ok = ok && cudaMemcpyAsync(hy + row * L * es, sb + o_y, nseq, cudaMemcpyDeviceToHost, hs.out) == cudaSuccess;
+        if (last_state)
+            ok = ok && cudaMemcpyAsync(last_state + row * N, sb + o_h, (size_t)w * N * 4, cudaMemcpyDeviceToHost, hs.out) ==
+                           cudaSuccess;
+        ok = ok && cudaEventRecord(ev_out[set], hs.out) == cudaSuccess;
+    }
+    // join: the caller's stream waits for the last copies out, then frees
+    if (ok) ok = cudaStreamWaitEvent(st, ev_out[0], 0) == cudaSuccess;
+    if (ok && nslices > 1) ok = cudaStreamWaitEvent(st, ev_out[1], 0) == cudaSuccess;
+    if (ok) ok = cudaStreamWaitEvent(st, ev_in[0], 0) == cudaSuccess;   // (covers the parameter copies)
+    if (!ok) {
+        // an enqueue failed: wait for what was enqueued before freeing
+        cudaStreamSynchronize(hs.in);
+        cudaStreamSynchronize(hs.out);
+        cudaStreamSynchronize(st);
+        cudaFree(dev);
+        return rc != SSM_OK ? rc : SSM_ERR_CUDA;
+    }
+    return cudaFreeAsync(dev, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------
