@@ -386,6 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_load(r + kOffTileC, gC + t0 * kN, bc, &br.raw_full[slot]);
                 }
             }
+            // the shared memory is released when the CTA exits: let the last
+            // copies land even if the pipeline gave up
+            volatile int never = 0;
+            for (int64_t k = T - kRawSlots < 0 ? 0 : T - kRawSlots; k < T; k++)
+                mbar_wait(&br.raw_full[k % kRawSlots], full_parity(k / kRawSlots), &never);
         }
     } else if (warp == 1) {
         // ---------------- MMA issue (one thread) ----------------
