@@ -58,6 +58,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_state_step.restype = i32
         lib.oracle_state_step.argtypes = [i64, i64, i64, i32, i32,
                                           dp, vp, vp, vp, vp, vp, vp, vp, vp, i32, dp]
+        lib.oracle_scan_bwd.restype = i32
+        lib.oracle_scan_bwd.argtypes = [i64, i64, i64, i64, i32, i32,
+                                        vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                        dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, i32]
         _lib_cache[path] = lib
     return _lib_cache[path]
 
@@ -166,3 +170,49 @@ def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
     if rc != 0:
         raise ValueError("oracle_state_step rejected its arguments")
     return y
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
+             dlast=None, nthreads: int = 1, lib: ctypes.CDLL | None = None):
+    """Oracle backward scan: the gradients of a loss with dLoss/dy = ``dy``
+    (batch, dim, L) and dLoss/dlast_state = ``dlast`` (batch, dim, N, or
+    None) with respect to every input of ``scan_fwd`` (zero initial state).
+
+    Returns a dict of fp64 arrays: du, ddelta, dz (batch, dim, L; dz is None
+    without z), dA (dim, N), dD, ddelta_bias (dim,), dB, dC (batch, L, N),
+    dh0 (batch, dim, N: the gradient with respect to the initial state).
+    The per-channel C code leaves the sums over channels (dB, dC) and over
+    the batch (dA, dD, ddelta_bias) to this wrapper.
+    """
+    lib = lib or load()
+    batch, dim, L = (int(s) for s in u.shape)
+    N = int(A.shape[1])
+    arrs = {n: _host(a) for n, a in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z))}
+    io_types = {t for _, t in arrs.values() if t is not None}
+    if len(io_types) != 1:
+        raise TypeError("u, delta, B, C, z must share one element type")
+    io = io_types.pop()
+    parr = {n: _host(a) for n, a in (("A", A), ("D", D), ("bias", delta_bias))}
+    p_types = {t for _, t in parr.values() if t is not None}
+    if len(p_types) != 1 or not p_types <= {F32, F64}:
+        raise TypeError("A, D, delta_bias must share one element type, fp32 or fp64")
+    pio = p_types.pop()
+    dy = np.ascontiguousarray(np.asarray(dy, dtype=np.float64).reshape(batch, dim, L))
+    if dlast is not None:
+        dlast = np.ascontiguousarray(np.asarray(dlast, dtype=np.float64).reshape(batch, dim, N))
+    du = np.empty((batch, dim, L)); ddelta = np.empty((batch, dim, L))
+    dz = np.empty((batch, dim, L)) if z is not None else None
+    dA = np.empty((batch, dim, N)); dD = np.empty((batch, dim)); dbias = np.empty((batch, dim))
+    dBc = np.empty((batch, dim, L, N)); dCc = np.empty((batch, dim, L, N))
+    dh0 = np.empty((batch, dim, N))
+    rc = lib.oracle_scan_bwd(batch, dim, N, L, io, pio,
+                             _ptr(arrs["u"][0]), _ptr(arrs["delta"][0]), _ptr(parr["A"][0]),
+                             _ptr(arrs["B"][0]), _ptr(arrs["C"][0]), _ptr(parr["D"][0]),
+                             _ptr(arrs["z"][0]), _ptr(parr["bias"][0]), int(bool(delta_softplus)),
+                             _ptr(dy), _ptr(dlast), _ptr(du), _ptr(ddelta), _ptr(dz), _ptr(dA),
+                             _ptr(dD), _ptr(dbias), _ptr(dBc), _ptr(dCc), _ptr(dh0), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_scan_bwd rejected its arguments")
+    return {"du": du, "ddelta": ddelta, "dz": dz, "dA": dA.sum(axis=0), "dD": dD.sum(axis=0),
+            "ddelta_bias": dbias.sum(axis=0), "dB": dBc.sum(axis=1), "dC": dCc.sum(axis=1),
+            "dh0": dh0}

@@ -204,3 +204,181 @@ int oracle_state_step(int64_t batch, int64_t dim, int64_t dstate, int io, int pi
     }
     return 0;
 }
+
+/*
+ * Backward pass of the forward scan above (gradients for training): given
+ * dy = dLoss/dy (and optionally dlast = dLoss/dlast_state), the gradients of
+ * the loss with respect to every input.  The pages describe the backward
+ * pass only as the forward recomputed in on-chip memory instead of storing
+ * the expanded state ("State Spaces, Selectively - Mamba", papermap,
+ * "The hardware-aware scan"); this oracle states what that pass must
+ * produce: the reverse-mode derivative of the recurrence, written out
+ * step by step in reverse token order.
+ *
+ * For one channel (b, d), with x_t = u_t, v_t = delta_t + bias,
+ * Delta_t = softplus(v_t) (or v_t), a_tn = exp(Delta_t A_n),
+ * h_tn = a_tn h_(t-1)n + Delta_t B_tn x_t, s_t = sum_n C_tn h_tn + D x_t and
+ * y_t = s_t silu(z_t) (or s_t), let g_n be the adjoint of h_tn.  Going from
+ * t = L-1 down to 0, starting from g = dlast:
+ *
+ *   ds_t   = dy_t silu(z_t)           dz_t = dy_t s_t silu'(z_t)
+ *   dD    += ds_t x_t                 dx_t = ds_t D
+ *   g_n   += ds_t C_tn                dC_tn = ds_t h_tn
+ *   dDelta_t = sum_n g_n (A_n a_tn h_(t-1)n + B_tn x_t)
+ *   dx_t  += sum_n g_n Delta_t B_tn   dB_tn = g_n Delta_t x_t
+ *   dA_n  += g_n Delta_t a_tn h_(t-1)n
+ *   g_n    = g_n a_tn                 (the adjoint of h_(t-1)n)
+ *   ddelta_t = dDelta_t sigmoid(v_t) (softplus' = sigmoid) or dDelta_t
+ *   dbias += ddelta_t
+ *
+ * The forward states h_t are recomputed first and kept for the channel
+ * (L x N doubles), then the loop above runs.  Per-channel outputs: du,
+ * ddelta, dz (nchan x L), dA (nchan x N), dD, dbias (nchan), and the
+ * channel's terms of dB, dC (nchan x L x N; the caller sums them over the
+ * channels of a batch row) and dh0 = g after t = 0 (nchan x N).
+ */
+typedef struct {
+    int64_t batch, dim, dstate, seqlen;
+    int io, pio;
+    const void *u, *delta, *A, *B, *C, *D, *z, *bias;
+    int softplus_on;
+    const double *dy, *dlast;   /* nchan x L, nchan x N (dlast may be NULL) */
+    double *du, *ddelta, *dz, *dA, *dD, *dbias, *dBc, *dCc, *dh0;
+    int64_t nchan, next;
+    pthread_mutex_t mu;
+} bwd_job;
+
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+static void bwd_channel(const bwd_job* j, int64_t c, double* hs, double* g) {
+    const int64_t L = j->seqlen, N = j->dstate;
+    const int64_t b = c / j->dim, d = c % j->dim;
+    const int64_t row = c * L, bc_row = b * L * N;
+    const double bias = j->bias ? load(j->pio, j->bias, d) : 0.0;
+    const double Dskip = j->D ? load(j->pio, j->D, d) : 0.0;
+    /* forward: hs[(t + 1) * N + n] = h_tn, hs[n] = h_(-1)n = 0 */
+    for (int64_t n = 0; n < N; n++) hs[n] = 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        const double v = load(j->io, j->delta, row + t) + bias;
+        const double dt = j->softplus_on ? softplus(v) : v;
+        const double x = load(j->io, j->u, row + t);
+        for (int64_t n = 0; n < N; n++) {
+            const double a = exp(dt * load(j->pio, j->A, d * N + n));
+            hs[(t + 1) * N + n] = a * hs[t * N + n] + dt * load(j->io, j->B, bc_row + t * N + n) * x;
+        }
+    }
+    /* reverse */
+    for (int64_t n = 0; n < N; n++) {
+        g[n] = j->dlast ? j->dlast[c * N + n] : 0.0;
+        j->dA[c * N + n] = 0.0;
+    }
+    double dD = 0.0, dbias = 0.0;
+    for (int64_t t = L - 1; t >= 0; t--) {
+        const double v = load(j->io, j->delta, row + t) + bias;
+        const double dt = j->softplus_on ? softplus(v) : v;
+        const double x = load(j->io, j->u, row + t);
+        const double* h = hs + (t + 1) * N;
+        const double* hp = hs + t * N;
+        double s = Dskip * x;
+        for (int64_t n = 0; n < N; n++) s += load(j->io, j->C, bc_row + t * N + n) * h[n];
+        const double dyv = j->dy[c * L + t];
+        double ds = dyv;
+        if (j->z) {
+            const double zv = load(j->io, j->z, row + t);
+            const double sg = sigmoid(zv);
+            ds = dyv * zv * sg;
+            j->dz[c * L + t] = dyv * s * sg * (1.0 + zv * (1.0 - sg));
+        } else if (j->dz) {
+            j->dz[c * L + t] = 0.0;
+        }
+        dD += ds * x;
+        double dx = ds * Dskip, ddt = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            const double Cv = load(j->io, j->C, bc_row + t * N + n);
+            const double Bv = load(j->io, j->B, bc_row + t * N + n);
+            const double An = load(j->pio, j->A, d * N + n);
+            const double a = exp(dt * An);
+            g[n] += ds * Cv;
+            j->dCc[(c * L + t) * N + n] = ds * h[n];
+            ddt += g[n] * (An * a * hp[n] + Bv * x);
+            dx += g[n] * dt * Bv;
+            j->dBc[(c * L + t) * N + n] = g[n] * dt * x;
+            j->dA[c * N + n] += g[n] * dt * a * hp[n];
+            g[n] *= a;
+        }
+        const double dv = j->softplus_on ? ddt * sigmoid(v) : ddt;
+        j->ddelta[c * L + t] = dv;
+        j->du[c * L + t] = dx;
+        dbias += dv;
+    }
+    j->dD[c] = dD;
+    j->dbias[c] = dbias;
+    if (j->dh0)
+        for (int64_t n = 0; n < N; n++) j->dh0[c * N + n] = g[n];
+}
+
+static void* bwd_worker(void* arg) {
+    bwd_job* j = (bwd_job*)arg;
+    double* hs = (double*)malloc(sizeof(double) * (size_t)((j->seqlen + 1) * j->dstate));
+    double* g = (double*)malloc(sizeof(double) * (size_t)j->dstate);
+    if (!hs || !g) {
+        free(hs);
+        free(g);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&j->mu);
+        const int64_t c = j->next++;
+        pthread_mutex_unlock(&j->mu);
+        if (c >= j->nchan) break;
+        bwd_channel(j, c, hs, g);
+    }
+    free(hs);
+    free(g);
+    return NULL;
+}
+
+/*
+ * Backward selective scan over every channel (see the comment above).
+ * Inputs as for oracle_scan_fwd; dy is (batch, dim, L) fp64 and dlast
+ * (batch, dim, N) fp64 or NULL.  Outputs (fp64, per channel): du, ddelta,
+ * dz (batch, dim, L; dz may be NULL when z is), dA (batch, dim, N: the
+ * channel's share, summed over the batch by the caller), dD, dbias
+ * (batch, dim), dBc, dCc (batch, dim, L, N: per-channel terms) and dh0
+ * (batch, dim, N) or NULL.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io, int pio,
+                    const void* u, const void* delta, const void* A, const void* B,
+                    const void* C, const void* D, const void* z, const void* delta_bias,
+                    int delta_softplus, const double* dy, const double* dlast, double* du,
+                    double* ddelta, double* dz, double* dA, double* dD, double* dbias,
+                    double* dBc, double* dCc, double* dh0, int nthreads) {
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dD || !dbias || !dBc ||
+        !dCc)
+        return -1;
+    if (z && !dz) return -1;
+    if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
+    bwd_job j;
+    memset(&j, 0, sizeof j);
+    j.batch = batch; j.dim = dim; j.dstate = dstate; j.seqlen = seqlen;
+    j.io = io; j.pio = pio;
+    j.u = u; j.delta = delta; j.A = A; j.B = B; j.C = C; j.D = D; j.z = z;
+    j.bias = delta_bias; j.softplus_on = delta_softplus;
+    j.dy = dy; j.dlast = dlast;
+    j.du = du; j.ddelta = ddelta; j.dz = dz; j.dA = dA; j.dD = dD; j.dbias = dbias;
+    j.dBc = dBc; j.dCc = dCc; j.dh0 = dh0;
+    j.nchan = batch * dim;
+    j.next = 0;
+    pthread_mutex_init(&j.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < nthreads; i++)
+        if (pthread_create(&th[started], NULL, bwd_worker, &j) == 0) started++;
+    bwd_worker(&j);
+    for (int i = 0; i < started; i++) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&j.mu);
+    return 0;
+}
