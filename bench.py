@@ -354,6 +354,48 @@ def time_e2e(w, inp, steps, warmup, local):
     return sec, h2d, d2h
 
 
+def time_scan_bwd(w, local, reps=5):
+    """Backward scan (gradients of every input from dy, forward recomputed
+    inside the kernel) at the workload's shape, CUDA events on the current
+    stream.  Roofline: the forward states are computed twice (checkpoint pass
+    and tile recompute) and the decay once more in the adjoint pass, 3 x
+    batch*dim*L*N exps; bytes: the forward inputs twice, dy and the fp32
+    gradients of the (batch, dim, L) tensors once."""
+    import selective_state_space_116_b300 as ssm
+    from selective_state_space_116_b300.workloads import make_scan_inputs
+    dev = torch.device("cuda", local)
+    inp = make_scan_inputs(w, seed=0)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dy = torch.randn(w.batch, w.dim, w.seqlen, device=dev)
+
+    def run():
+        return ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], z=g["z"],
+                                delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"])
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        run()
+    b.record()
+    torch.cuda.synchronize(dev)
+    sec = a.elapsed_time(b) / 1e3 / reps
+    es = 2 if w.io == "bf16" else 4
+    elems = w.batch * w.dim * w.seqlen
+    nseq = 3 if w.gate else 2                                   # u, delta (, z)
+    byts = 2 * (nseq * elems * es + 2 * w.batch * w.seqlen * w.dstate * es)
+    byts += elems * 4 + nseq * elems * 4 + 2 * w.batch * w.seqlen * w.dstate * 4
+    exps = 3 * elems * w.dstate
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    t_roof = max(byts / (pk["hbm_gbs"] * 1e9),
+                 exps / (EX2_PER_CLK_PER_SM * sms * pk["sm_max_mhz"] * 1e6))
+    return {"workload": w.name, "ms": sec * 1e3, "roofline_ms": t_roof * 1e3,
+            "frac": t_roof / sec, "launches": 1,
+            "timing": f"{reps} calls, CUDA events (outputs ~1.4 GB: larger than L2)"}
+
+
 def time_state_step(local, graph_steps=1024, reps=5):
     """Generation: 128 x 5120 channels, N = 16, bf16 inputs, fp32 state, one token
     per launch, 1024 consecutive launches captured in one CUDA graph.  The state
@@ -570,6 +612,7 @@ def run_ours(args, world, rank, local):
                       "ms_per_step": sec * 1e3}
     if not args.no_step and rank == 0:
         out["state_step"] = time_state_step(local)
+        out["scan_bwd"] = time_scan_bwd(w, local)
         out["other_workloads"] = [time_other("m130"), time_other("tiny")]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_rate(w, res["host_inputs"])

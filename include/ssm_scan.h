@@ -148,6 +148,52 @@ SSM_API int ssm_scan_fwd(const ssm_dims* dims,
 SSM_API int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes);
 
 /*
+ * Backward selective scan: the gradients for training.  Given dy =
+ * dLoss/dy (and optionally dlast_state = dLoss/dlast_state) of a forward
+ * scan with the same inputs and a zero initial state, writes the gradients
+ * of the loss with respect to every input.  The forward pass stores nothing
+ * for it; the backward pass recomputes the forward states on chip instead of
+ * reading an expanded state from memory ("State Spaces, Selectively -
+ * Mamba", papermap interactive explainer, "The hardware-aware scan": the
+ * states are recomputed in the backward pass rather than stored).
+ *
+ *   dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus
+ *                  as for ssm_scan_fwd (device pointers)
+ *   dy             (batch, dim, seqlen) fp32; required
+ *   dlast_state    (batch, dim, dstate) fp32, or NULL for zero
+ *   du, ddelta     (batch, dim, seqlen) fp32; required.  ddelta is the
+ *                  gradient with respect to the raw delta (before bias and
+ *                  softplus)
+ *   dz             (batch, dim, seqlen) fp32; required when z is given
+ *   dA             (dim, dstate) fp32; required
+ *   dB, dC         (batch, seqlen, dstate) fp32; required
+ *   dD, ddelta_bias (dim) fp32, or NULL to skip (ignored when D, resp.
+ *                  delta_bias, is NULL)
+ *   dh0            (batch, dim, dstate) fp32 gradient with respect to the
+ *                  initial state, or NULL
+ *   workspace      device scratch of ssm_scan_bwd_workspace_size() bytes
+ *                  (the state at every 8th token), 16-byte aligned
+ *   stream         cudaStream_t to enqueue on
+ *
+ * All gradients are fp32 whatever the I/O type.  dA, dB, dC, dD and
+ * ddelta_bias are sums over channels or over the batch, accumulated with
+ * fp32 atomics: their rounding order, and so their last bits, may vary from
+ * run to run.  The call clears them on `stream` first.  Returns SSM_OK or a
+ * negative ssm_status.
+ */
+SSM_API int ssm_scan_bwd(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 const float* dy, const float* dlast_state,
+                 float* du, float* ddelta, float* dz, float* dA,
+                 float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace ssm_scan_bwd needs for these sizes (may be 0). */
+SSM_API int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes);
+
+/*
  * ssm_scan_fwd on HOST buffers: every pointer (u, delta, A, B, C, D, z,
  * delta_bias, y, last_state) is host memory, with the layouts and meanings of
  * ssm_scan_fwd.  The call takes device memory on the current device with

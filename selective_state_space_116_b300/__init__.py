@@ -19,7 +19,7 @@ import torch
 from . import _lib
 from ._lib import SSMError, ssm_dims
 
-__all__ = ["ssm_scan_fwd", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
+__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
            "library_path", "version"]
 
 _IO = {torch.float32: _lib.SSM_IO_F32, torch.bfloat16: _lib.SSM_IO_BF16}
@@ -205,3 +205,59 @@ def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
     if rc != 0:
         raise SSMError(rc, "ssm_state_step")
     return y
+
+
+def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
+                 dlast_state=None, return_dh0=False, workspace=None):
+    """Backward selective scan (CUDA tensors): the gradients of a loss with
+    dLoss/dy = ``dy`` (and dLoss/dlast_state = ``dlast_state``) with respect
+    to the inputs of ``ssm_scan_fwd`` (zero initial state).  The forward
+    states are recomputed inside the kernel.  Returns a dict of fp32
+    tensors: du, ddelta (gradient of the raw delta), dz (None without z),
+    dA, dB, dC, dD (None without D), ddelta_bias (None without delta_bias)
+    and dh0 (None unless ``return_dh0``).
+    """
+    device = u.device
+    if device.type != "cuda":
+        raise ValueError("ssm_scan_bwd needs CUDA tensors")
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    if io not in _IO:
+        raise TypeError(f"unsupported I/O dtype {io}; use float32 or bfloat16")
+    _check(u, "u", (batch, dim, L), io, device)
+    _check(delta, "delta", (batch, dim, L), io, device)
+    _check(A, "A", (dim, N), torch.float32, device)
+    _check(B, "B", (batch, L, N), io, device)
+    _check(C, "C", (batch, L, N), io, device)
+    _check(D, "D", (dim,), torch.float32, device, optional=True)
+    _check(z, "z", (batch, dim, L), io, device, optional=True)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, device, optional=True)
+    _check(dy, "dy", (batch, dim, L), torch.float32, device)
+    _check(dlast_state, "dlast_state", (batch, dim, N), torch.float32, device, optional=True)
+    f32 = dict(dtype=torch.float32, device=device)
+    g = {"du": torch.empty((batch, dim, L), **f32), "ddelta": torch.empty((batch, dim, L), **f32),
+         "dz": torch.empty((batch, dim, L), **f32) if z is not None else None,
+         "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, L, N), **f32),
+         "dC": torch.empty((batch, L, N), **f32),
+         "dD": torch.empty((dim,), **f32) if D is not None else None,
+         "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+         "dh0": torch.empty((batch, dim, N), **f32) if return_dh0 else None}
+    lib = _lib.load()
+    d = _dims(batch, dim, N, L, _IO[io])
+    need = ctypes.c_size_t(0)
+    rc = lib.ssm_scan_bwd_workspace_size(ctypes.byref(d), ctypes.byref(need))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_bwd_workspace_size")
+    if workspace is None and need.value > 0:
+        workspace = torch.empty(need.value, dtype=torch.uint8, device=device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.ssm_scan_bwd(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                          _ptr(D), _ptr(z), _ptr(delta_bias), 1 if delta_softplus else 0,
+                          _ptr(dy), _ptr(dlast_state), _ptr(g["du"]), _ptr(g["ddelta"]),
+                          _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                          _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+                          _ptr(workspace), ws_bytes, _stream(device))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_bwd")
+    return g

@@ -13,6 +13,7 @@
 #include "scan_fwd.cuh"
 #include "scan_fwd_tc.cuh"
 #include "scan_fwd_ws.cuh"
+#include "scan_bwd.cuh"
 #include "state_step.cuh"
 
 namespace {
@@ -675,6 +676,112 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dims->io == SSM_IO_BF16) return dispatch_step<bf16>(p, dims->dstate, z != nullptr, sp, vec, st);
     return dispatch_step<float>(p, dims->dstate, z != nullptr, sp, vec, st);
+}
+
+// ---------------------------------------------------------------------------
+// Backward scan.
+
+}  // extern "C"
+
+namespace {
+
+size_t bwd_workspace(const ssm_dims* d) {
+    const int64_t ntiles = (d->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT;
+    return (size_t)d->batch * d->dim * ntiles * d->dstate * sizeof(float);
+}
+
+template <typename T, int N, bool Z, bool SP>
+int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
+    using Sh = ssm::bwd::BwdShape<N>;
+    auto kern = ssm::bwd::scan_bwd_kernel<T, N, Z, SP>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    const dim3 grid((unsigned)((p.dim + ssm::bwd::kCH - 1) / ssm::bwd::kCH), (unsigned)p.batch);
+    kern<<<grid, ssm::bwd::kCH, Sh::SMEM, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int N>
+int dispatch_bwd_n(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
+    if (z && sp) return launch_bwd<T, N, true, true>(p, st);
+    if (z) return launch_bwd<T, N, true, false>(p, st);
+    if (sp) return launch_bwd<T, N, false, true>(p, st);
+    return launch_bwd<T, N, false, false>(p, st);
+}
+
+template <typename T>
+int dispatch_bwd(const ssm::bwd::BwdParams& p, int64_t n, bool z, bool sp, cudaStream_t st) {
+    switch (n) {
+        case 1: return dispatch_bwd_n<T, 1>(p, z, sp, st);
+        case 2: return dispatch_bwd_n<T, 2>(p, z, sp, st);
+        case 4: return dispatch_bwd_n<T, 4>(p, z, sp, st);
+        case 8: return dispatch_bwd_n<T, 8>(p, z, sp, st);
+        case 16: return dispatch_bwd_n<T, 16>(p, z, sp, st);
+    }
+    return SSM_ERR_UNSUPPORTED_N;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
+    if (!bytes) return SSM_ERR_NULL_ARG;
+    Sizes s;
+    const int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    *bytes = bwd_workspace(dims);
+    return SSM_OK;
+}
+
+int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus, const float* dy,
+                 const float* dlast_state, float* du, float* ddelta, float* dz, float* dA,
+                 float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    Sizes s;
+    int rc = check_dims(dims, true, &s);
+    if (rc != SSM_OK) return rc;
+    const bool empty = dims->seqlen == 0;
+    if (!A || !dA || (!empty && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)))
+        return SSM_ERR_NULL_ARG;
+    if (z && !empty && !dz) return SSM_ERR_NULL_ARG;
+    const size_t es = io_size(dims->io);
+    for (const void* q : {u, delta, B, C, z})
+        if (!aligned(q, es)) return SSM_ERR_MISALIGNED;
+    for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
+                          static_cast<const void*>(delta_bias), static_cast<const void*>(dy),
+                          static_cast<const void*>(dlast_state), static_cast<const void*>(du),
+                          static_cast<const void*>(ddelta), static_cast<const void*>(dz),
+                          static_cast<const void*>(dA), static_cast<const void*>(dB),
+                          static_cast<const void*>(dC), static_cast<const void*>(dD),
+                          static_cast<const void*>(ddelta_bias), static_cast<const void*>(dh0)})
+        if (!aligned(q, 4)) return SSM_ERR_MISALIGNED;
+    const size_t need = bwd_workspace(dims);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the accumulated gradients start from zero
+    const int64_t N = dims->dstate;
+    if (cudaMemsetAsync(dA, 0, (size_t)dims->dim * N * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (!empty) {
+        if (cudaMemsetAsync(dB, 0, (size_t)s.bc * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(dC, 0, (size_t)s.bc * 4, st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (dD && cudaMemsetAsync(dD, 0, (size_t)dims->dim * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)dims->dim * 4, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    ssm::bwd::BwdParams p{u, delta, A, B, C, D, z && !empty ? z : nullptr, delta_bias, dy,
+                          dlast_state, du, ddelta, z ? dz : nullptr, dA, dB, dC,
+                          D ? dD : nullptr, delta_bias ? ddelta_bias : nullptr, dh0,
+                          static_cast<float*>(workspace), dims->batch, dims->dim, dims->seqlen,
+                          (dims->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT};
+    if (empty) p.z = nullptr;
+    const bool zz = p.z != nullptr, sp = delta_softplus != 0;
+    if (dims->io == SSM_IO_BF16) return dispatch_bwd<bf16>(p, N, zz, sp, st);
+    return dispatch_bwd<float>(p, N, zz, sp, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,94 @@
+"""Backward scan on the GPU (through the C ABI) against the fp64 backward
+oracle (itself pinned by finite differences) on the same seeded inputs.
+
+Tolerance: every gradient is compared in fp64 against the oracle with
+|got - ref| <= 1e-3 * max|ref| + 1e-6.  The kernel works in fp32 with the
+hardware 2^x (relative error ~2^-22); a gradient entry is a sum of up to
+L (or batch * L, for dA, dD, ddelta_bias, or dim, for dB, dC) terms, so
+its rounding error grows like sqrt(terms) * 2^-23 of the largest term:
+below 1e-4 of max|ref| at these sizes, ten times inside the bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_116_b300 as ssm
+from parity import nthreads, to_cuda
+from selective_state_space_116_b300.workloads import WORKLOADS, make_scan_inputs
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"]
+
+
+def run_both(w, seed=0, with_dlast=True):
+    inp = make_scan_inputs(w, seed)
+    rng = np.random.default_rng(seed + 100)
+    b, d, L, N = w.batch, w.dim, w.seqlen, w.dstate
+    dy = torch.from_numpy(rng.standard_normal((b, d, L)).astype(np.float32))
+    dlast = torch.from_numpy(rng.standard_normal((b, d, N)).astype(np.float32)) if with_dlast else None
+    g = to_cuda(inp)
+    got = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+                           delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
+                           dlast_state=None if dlast is None else dlast.cuda(), return_dh0=True)
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy.double().numpy(),
+                          D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
+                          delta_softplus=inp["delta_softplus"],
+                          dlast=None if dlast is None else dlast.double().numpy(), nthreads=nthreads())
+    return got, ref
+
+
+def check(got, ref, what):
+    for name in NAMES:
+        r, gt = ref[name], got[name]
+        if r is None or gt is None:
+            assert (gt is None) == (r is None) or name in ("dD", "ddelta_bias"), (what, name)
+            continue
+        gt = gt.double().cpu().numpy()
+        assert gt.shape == r.shape, (what, name, gt.shape, r.shape)
+        assert np.all(np.isfinite(gt)), (what, name, "non-finite")
+        err = np.abs(gt - r).max()
+        bound = 1e-3 * np.abs(r).max() + 1e-6
+        assert err <= bound, f"{what} {name}: max err {err:.3e} > {bound:.3e}"
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+def test_bwd_state_sizes(io, N):
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=37, dstate=N, io=io, last_state=True)
+    got, ref = run_both(w, seed=N)
+    check(got, ref, f"{io} N={N}")
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("softplus", [False, True])
+@pytest.mark.parametrize("extras", [False, True])
+def test_bwd_options(gate, softplus, extras):
+    w = WORKLOADS["m130"].scaled(batch=2, dim=33, seqlen=50, io="f32", gate=gate,
+                                 softplus=softplus, last_state=True,
+                                 bias_range=(((-4.0, -2.0) if softplus else (0.1, 0.5))
+                                             if extras else None))
+    inp = make_scan_inputs(w, seed=7)
+    if not extras:
+        inp["D"] = None
+    if not softplus:
+        inp["delta"] = inp["delta"].abs()
+    rng = np.random.default_rng(9)
+    dy = torch.from_numpy(rng.standard_normal((2, 33, 50)).astype(np.float32))
+    g = to_cuda(inp)
+    got = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+                           delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
+                           return_dh0=True)
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy.double().numpy(),
+                          D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
+                          delta_softplus=inp["delta_softplus"])
+    check(got, ref, f"gate={gate} softplus={softplus} extras={extras}")
+
+
+@pytest.mark.parametrize("L", [1, 8, 9, 300])
+def test_bwd_lengths_and_ragged_channels(L):
+    w = WORKLOADS["m130"].scaled(batch=3, dim=130, seqlen=L, last_state=True)
+    got, ref = run_both(w, seed=L)
+    check(got, ref, f"L={L}")
