@@ -3,12 +3,15 @@
 // The forward pass keeps no state for the backward pass; the backward pass
 // recomputes the forward states on chip instead of reading an expanded state
 // from memory ("State Spaces, Selectively - Mamba", papermap, "The
-// hardware-aware scan").  Per channel (one thread, all N states in
-// registers):
+// hardware-aware scan").  Per channel, G = N / S adjacent lanes of a warp
+// hold S states each (S = min(N, 4)); the sums over a channel's states
+// (the output s_t, dDelta_t, dx_t) are warp shuffles within the G lanes:
 //
 //   pass 1  the forward recurrence over the whole sequence, writing only the
 //           state at the start of every 8-token tile to the workspace
 //           (batch x dim x ceil(L/8) x N fp32 checkpoints);
+//   (each 8-token tile's inputs are first staged in shared memory by the
+//   whole CTA with coalesced loads, Delta computed once per element)
 //   pass 2  the tiles in reverse order: the tile's states are recomputed
 //           from its checkpoint into shared memory, then the adjoint
 //           recurrence runs backwards through the tile:
@@ -30,8 +33,8 @@
 namespace ssm {
 namespace bwd {
 
-constexpr int kCH = 64;    // channels (threads) per CTA
-constexpr int kTT = 8;     // tokens per tile
+constexpr int kThreads = 256;   // threads per CTA
+constexpr int kTT = 8;          // tokens per tile
 
 struct BwdParams {
     const void* u;
@@ -58,157 +61,216 @@ struct BwdParams {
 };
 
 template <int N> struct BwdShape {
-    static constexpr int NP = N + 4;   // padded row of one channel's states
-    // rows: the state before the tile, then the tile's kTT states
-    static constexpr int TILE = (kTT + 1) * kCH * NP * 4;
+    static constexpr int S = N < 4 ? N : 4;    // states per thread
+    static constexpr int G = N / S;            // threads per channel
+    static constexpr int CH = kThreads / G;    // channels per CTA
+    // [kTT + 1][kThreads][S]: row 0 the state before the tile, then the
+    // tile's states; the adjoints used for dB in rows 0 .. kTT-1 of a second
+    // such array; then ds_t and Delta_t x_t per channel and token
+    static constexpr int TILE = (kTT + 1) * kThreads * S * 4;
     static constexpr int OFF_G = TILE;
     static constexpr int OFF_DS = 2 * TILE;
-    static constexpr int OFF_DX = OFF_DS + kTT * kCH * 4;
-    static constexpr int SMEM = OFF_DX + kTT * kCH * 4;
+    static constexpr int OFF_DX = OFF_DS + kTT * CH * 4;
+    // the tile's inputs, staged with coalesced loads: per channel a row of
+    // kTT + 1 floats (x = u, Delta, v = delta + bias, z, dy), and B, C rows
+    static constexpr int ROW = kTT + 1;
+    static constexpr int OFF_IN = OFF_DX + kTT * CH * 4;
+    static constexpr int IN_PLANE = CH * ROW * 4;
+    static constexpr int OFF_BC = OFF_IN + 5 * IN_PLANE;
+    static constexpr int SMEM = OFF_BC + 2 * kTT * N * 4;
 };
 
 __device__ __forceinline__ float sigmoid(float v) { return rcp(1.0f + ex2(-v * kLog2e)); }
 
+// sum over the G lanes of a channel (adjacent, G a power of two)
+template <int G>
+__device__ __forceinline__ float chan_sum(float v) {
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
 template <typename T, int N, bool HAS_Z, bool SOFTPLUS>
-__global__ void __launch_bounds__(kCH) scan_bwd_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<N>;
+    constexpr int S = Sh::S, G = Sh::G, CH = Sh::CH;
     extern __shared__ __align__(16) unsigned char smem[];
-    float* Hs = reinterpret_cast<float*>(smem);                  // [kTT + 1][kCH][NP] h_(t0-1), h_t
-    float* Gs = reinterpret_cast<float*>(smem + Sh::OFF_G);      // [kTT + 1][kCH][NP] g used for dB_t (rows 0..kTT-1)
-    float* DS = reinterpret_cast<float*>(smem + Sh::OFF_DS);     // [kTT][kCH] ds_t
-    float* DX = reinterpret_cast<float*>(smem + Sh::OFF_DX);     // [kTT][kCH] Delta_t x_t
+    float* Hs = reinterpret_cast<float*>(smem);
+    float* Gs = reinterpret_cast<float*>(smem + Sh::OFF_G);
+    float* DS = reinterpret_cast<float*>(smem + Sh::OFF_DS);     // [kTT][CH]
+    float* DX = reinterpret_cast<float*>(smem + Sh::OFF_DX);     // [kTT][CH]
+    float* XU = reinterpret_cast<float*>(smem + Sh::OFF_IN);                    // [CH][ROW] x
+    float* DT = reinterpret_cast<float*>(smem + Sh::OFF_IN + Sh::IN_PLANE);     // Delta
+    float* VV = reinterpret_cast<float*>(smem + Sh::OFF_IN + 2 * Sh::IN_PLANE); // delta + bias
+    float* ZZ = reinterpret_cast<float*>(smem + Sh::OFF_IN + 3 * Sh::IN_PLANE); // z
+    float* DY = reinterpret_cast<float*>(smem + Sh::OFF_IN + 4 * Sh::IN_PLANE); // dy
+    float* BB = reinterpret_cast<float*>(smem + Sh::OFF_BC);                    // [kTT][N]
+    float* CC = BB + kTT * N;
+    constexpr int ROW = Sh::ROW;
 
     const int tid = threadIdx.x;
+    const int lc = tid / G, gi = tid % G;          // channel within the CTA, state slice
+    const int n0 = gi * S;
     const int64_t b = blockIdx.y;
-    const int64_t d = (int64_t)blockIdx.x * kCH + tid;
+    const int64_t d = (int64_t)blockIdx.x * CH + lc;
     const bool active = d < p.dim;
     const int64_t dd = active ? d : 0;
     const int64_t c = b * p.dim + dd;     // flat channel
     const int64_t L = p.L;
-    const T* gu = static_cast<const T*>(p.u) + c * L;
-    const T* gdl = static_cast<const T*>(p.delta) + c * L;
-    const T* gz = HAS_Z ? static_cast<const T*>(p.z) + c * L : nullptr;
-    const T* gB = static_cast<const T*>(p.B) + b * L * N;
-    const T* gC = static_cast<const T*>(p.C) + b * L * N;
-    const float* gdy = p.dy + c * L;
-    float* ck = p.ckpt + c * p.ntiles * N;
+    float* ck = p.ckpt + c * p.ntiles * N + n0;
 
-    float A[N], A2[N];
+    float A[S], A2[S];
 #pragma unroll
-    for (int n = 0; n < N; n++) {
-        A[n] = active ? p.A[dd * N + n] : 0.0f;
+    for (int n = 0; n < S; n++) {
+        A[n] = active ? p.A[dd * N + n0 + n] : 0.0f;
         A2[n] = A[n] * kLog2e;
     }
-    const float bias = (active && p.bias) ? p.bias[dd] : 0.0f;
     const float Dv = (active && p.D) ? p.D[dd] : 0.0f;
-    auto delta_of = [&](int64_t t, float& v) {
-        v = io<T>::load(gdl, t) + bias;
-        return SOFTPLUS ? softplus(v) : v;
+    // stage tokens [t0, t0 + nt) of the CTA's channels: consecutive threads
+    // take consecutive tokens of a row; `full` also stages z, dy and C
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const T* bu = static_cast<const T*>(p.u);
+    const T* bdl = static_cast<const T*>(p.delta);
+    const T* bz = static_cast<const T*>(p.z);
+    const T* bB = static_cast<const T*>(p.B) + b * L * N;
+    const T* bC = static_cast<const T*>(p.C) + b * L * N;
+    auto stage = [&](int64_t t0, int nt, bool full) {
+        for (int i = tid; i < CH * kTT; i += kThreads) {
+            const int cl = i / kTT, j = i % kTT;
+            const bool ok = d0 + cl < p.dim && j < nt;
+            const int64_t gi2 = ((b * p.dim + d0 + cl) * L + t0 + j);
+            float x = 0.0f, vv = 0.0f, dt = 0.0f;
+            if (ok) {
+                x = io<T>::load(bu, gi2);
+                vv = io<T>::load(bdl, gi2) + ((p.bias) ? p.bias[d0 + cl] : 0.0f);
+                dt = SOFTPLUS ? softplus(vv) : vv;
+            }
+            XU[cl * ROW + j] = x;
+            DT[cl * ROW + j] = dt;
+            VV[cl * ROW + j] = vv;
+            if (full) {
+                ZZ[cl * ROW + j] = (ok && HAS_Z) ? io<T>::load(bz, gi2) : 0.0f;
+                DY[cl * ROW + j] = ok ? p.dy[gi2] : 0.0f;
+            }
+        }
+        for (int i = tid; i < kTT * N; i += kThreads) {
+            const int j = i / N;
+            const bool ok = j < nt;
+            BB[i] = ok ? io<T>::load(bB, t0 * N + i) : 0.0f;
+            if (full) CC[i] = ok ? io<T>::load(bC, t0 * N + i) : 0.0f;
+        }
     };
 
     // ---- pass 1: forward, checkpoint every tile ----
-    float h[N];
+    float h[S];
 #pragma unroll
-    for (int n = 0; n < N; n++) h[n] = 0.0f;
-    if (active) {
-        for (int64_t t = 0; t < L; t++) {
-            if (t % kTT == 0) {
+    for (int n = 0; n < S; n++) h[n] = 0.0f;
+    for (int64_t k = 0; k < p.ntiles; k++) {
+        const int64_t t0 = k * kTT;
+        const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
+        if (active) {
 #pragma unroll
-                for (int n = 0; n < N; n++) ck[(t / kTT) * N + n] = h[n];
-            }
-            float v;
-            const float dt = delta_of(t, v);
-            const float dtx = dt * io<T>::load(gu, t);
-#pragma unroll
-            for (int n = 0; n < N; n++)
-                h[n] = fmaf(ex2(dt * A2[n]), h[n], dtx * io<T>::load(gB, t * N + n));
+            for (int n = 0; n < S; n++) ck[k * N + n] = h[n];
         }
+        stage(t0, nt, false);
+        __syncthreads();
+        for (int j = 0; j < nt; j++) {
+            const float dt = DT[lc * ROW + j];
+            const float dtx = dt * XU[lc * ROW + j];
+#pragma unroll
+            for (int n = 0; n < S; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], dtx * BB[j * N + n0 + n]);
+        }
+        __syncthreads();
     }
 
     // ---- pass 2: tiles in reverse ----
-    float g[N], dA[N];
+    float g[S], dA[S];
 #pragma unroll
-    for (int n = 0; n < N; n++) {
-        g[n] = (active && p.dlast) ? p.dlast[c * N + n] : 0.0f;
+    for (int n = 0; n < S; n++) {
+        g[n] = (active && p.dlast) ? p.dlast[c * N + n0 + n] : 0.0f;
         dA[n] = 0.0f;
     }
     float dD = 0.0f, dbias = 0.0f;
     for (int64_t k = p.ntiles - 1; k >= 0; k--) {
         const int64_t t0 = k * kTT;
         const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
+        stage(t0, nt, true);
         // recompute the tile's states (row 0: the state before the tile)
-        {
-            float* hs = Hs + tid * Sh::NP;
 #pragma unroll
-            for (int n = 0; n < N; n++) hs[n] = h[n] = active ? ck[k * N + n] : 0.0f;
-        }
+        for (int n = 0; n < S; n++) Hs[tid * S + n] = h[n] = active ? ck[k * N + n] : 0.0f;
+        __syncthreads();
         for (int j = 0; j < nt; j++) {
-            float v;
-            const float dt = active ? delta_of(t0 + j, v) : 0.0f;
-            const float x = active ? io<T>::load(gu, t0 + j) : 0.0f;
-            float* hs = Hs + ((j + 1) * kCH + tid) * Sh::NP;
+            const float dt = DT[lc * ROW + j];
+            const float dtx = dt * XU[lc * ROW + j];
+            float* hs = Hs + ((j + 1) * kThreads + tid) * S;
 #pragma unroll
-            for (int n = 0; n < N; n++) {
-                const float bv = active ? io<T>::load(gB, (t0 + j) * N + n) : 0.0f;
-                h[n] = fmaf(ex2(dt * A2[n]), h[n], dt * x * bv);
+            for (int n = 0; n < S; n++) {
+                h[n] = fmaf(ex2(dt * A2[n]), h[n], dtx * BB[j * N + n0 + n]);
                 hs[n] = h[n];
             }
         }
         // adjoint recurrence, backwards through the tile
         for (int j = nt - 1; j >= 0; j--) {
             const int64_t t = t0 + j;
-            float v = 0.0f;
-            const float dt = active ? delta_of(t, v) : 0.0f;
-            const float x = active ? io<T>::load(gu, t) : 0.0f;
-            const float* ht = Hs + ((j + 1) * kCH + tid) * Sh::NP;
-            const float* hp = Hs + (j * kCH + tid) * Sh::NP;
-            float s = Dv * x;
-            float Cv[N];
+            const float v = VV[lc * ROW + j];
+            const float dt = DT[lc * ROW + j];
+            const float x = XU[lc * ROW + j];
+            const float* ht = Hs + ((j + 1) * kThreads + tid) * S;
+            const float* hp = Hs + (j * kThreads + tid) * S;
+            float Cv[S], Bv[S];
+            float sp = 0.0f;
 #pragma unroll
-            for (int n = 0; n < N; n++) {
-                Cv[n] = active ? io<T>::load(gC, t * N + n) : 0.0f;
-                s = fmaf(Cv[n], ht[n], s);
+            for (int n = 0; n < S; n++) {
+                Cv[n] = CC[j * N + n0 + n];
+                Bv[n] = BB[j * N + n0 + n];
+                sp = fmaf(Cv[n], ht[n], sp);
             }
-            const float dyv = active ? gdy[t] : 0.0f;
+            const float s = fmaf(Dv, x, chan_sum<G>(sp));
+            const float dyv = DY[lc * ROW + j];
             float ds = dyv;
             if constexpr (HAS_Z) {
-                const float zv = active ? io<T>::load(gz, t) : 0.0f;
+                const float zv = ZZ[lc * ROW + j];
                 const float sg = sigmoid(zv);
                 ds = dyv * zv * sg;
-                if (active) p.dz[c * L + t] = dyv * s * sg * fmaf(zv, 1.0f - sg, 1.0f);
+                if (active && gi == 0) p.dz[c * L + t] = dyv * s * sg * fmaf(zv, 1.0f - sg, 1.0f);
             }
-            dD = fmaf(ds, x, dD);
-            float dx = ds * Dv, ddt = 0.0f;
-            float* gs = Gs + (j * kCH + tid) * Sh::NP;
+            float dxp = 0.0f, ddtp = 0.0f;
+            float* gs = Gs + (j * kThreads + tid) * S;
 #pragma unroll
-            for (int n = 0; n < N; n++) {
-                const float bv = active ? io<T>::load(gB, t * N + n) : 0.0f;
+            for (int n = 0; n < S; n++) {
                 const float a = ex2(dt * A2[n]);
                 g[n] = fmaf(ds, Cv[n], g[n]);
                 gs[n] = g[n];
                 const float gah = g[n] * a * hp[n];
-                ddt = fmaf(A[n], gah, fmaf(g[n], bv * x, ddt));
-                dx = fmaf(g[n] * dt, bv, dx);
+                ddtp = fmaf(A[n], gah, fmaf(g[n], Bv[n] * x, ddtp));
+                dxp = fmaf(g[n] * dt, Bv[n], dxp);
                 dA[n] = fmaf(dt, gah, dA[n]);
                 g[n] *= a;
             }
-            DS[j * kCH + tid] = ds;
-            DX[j * kCH + tid] = dt * x;
+            const float ddt = chan_sum<G>(ddtp);
+            const float dx = fmaf(ds, Dv, chan_sum<G>(dxp));
             const float dv = SOFTPLUS ? ddt * sigmoid(v) : ddt;
-            dbias += dv;
-            if (active) {
-                p.du[c * L + t] = dx;
-                p.ddelta[c * L + t] = dv;
+            if (gi == 0) {
+                DS[j * CH + lc] = ds;
+                DX[j * CH + lc] = dt * x;
+                dD = fmaf(ds, x, dD);
+                dbias += dv;
+                if (active) {
+                    p.du[c * L + t] = dx;
+                    p.ddelta[c * L + t] = dv;
+                }
             }
         }
         __syncthreads();
         // dB_tn = sum_c g_n Delta_t x_t, dC_tn = sum_c ds_t h_tn over the CTA's channels
-        for (int o = tid; o < nt * N; o += kCH) {
+        for (int o = tid; o < nt * N; o += kThreads) {
             const int j = o / N, n = o % N;
+            const int gn = n / S, sn = n % S;
             float sb = 0.0f, sc = 0.0f;
-            for (int cc = 0; cc < kCH; cc++) {
-                sb = fmaf(Gs[(j * kCH + cc) * Sh::NP + n], DX[j * kCH + cc], sb);
-                sc = fmaf(DS[j * kCH + cc], Hs[((j + 1) * kCH + cc) * Sh::NP + n], sc);
+            for (int cc = 0; cc < CH; cc++) {
+                const int th = cc * G + gn;
+                sb = fmaf(Gs[(j * kThreads + th) * S + sn], DX[j * CH + cc], sb);
+                sc = fmaf(DS[j * CH + cc], Hs[((j + 1) * kThreads + th) * S + sn], sc);
             }
             atomicAdd(p.dB + (b * L + t0 + j) * N + n, sb);
             atomicAdd(p.dC + (b * L + t0 + j) * N + n, sc);
@@ -217,12 +279,14 @@ __global__ void __launch_bounds__(kCH) scan_bwd_kernel(BwdParams p) {
     }
     if (active) {
 #pragma unroll
-        for (int n = 0; n < N; n++) atomicAdd(p.dA + dd * N + n, dA[n]);
-        if (p.dD) atomicAdd(p.dD + dd, dD);
-        if (p.dbias) atomicAdd(p.dbias + dd, dbias);
+        for (int n = 0; n < S; n++) atomicAdd(p.dA + dd * N + n0 + n, dA[n]);
+        if (gi == 0) {
+            if (p.dD) atomicAdd(p.dD + dd, dD);
+            if (p.dbias) atomicAdd(p.dbias + dd, dbias);
+        }
         if (p.dh0)
 #pragma unroll
-            for (int n = 0; n < N; n++) p.dh0[c * N + n] = g[n];
+            for (int n = 0; n < S; n++) p.dh0[c * N + n0 + n] = g[n];
     }
 }
 

@@ -696,8 +696,8 @@ int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
     auto kern = ssm::bwd::scan_bwd_kernel<T, N, Z, SP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess)
         return SSM_ERR_CUDA;
-    const dim3 grid((unsigned)((p.dim + ssm::bwd::kCH - 1) / ssm::bwd::kCH), (unsigned)p.batch);
-    kern<<<grid, ssm::bwd::kCH, Sh::SMEM, st>>>(p);
+    const dim3 grid((unsigned)((p.dim + Sh::CH - 1) / Sh::CH), (unsigned)p.batch);
+    kern<<<grid, ssm::bwd::kThreads, Sh::SMEM, st>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
