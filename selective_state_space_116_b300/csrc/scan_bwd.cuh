@@ -33,7 +33,7 @@
 namespace ssm {
 namespace bwd {
 
-constexpr int kThreads = 256;   // threads per CTA
+constexpr int kThreads = 64;    // threads per CTA (more, smaller CTAs: more warps per SM)
 constexpr int kTT = 8;          // tokens per tile
 
 struct BwdParams {
