@@ -195,6 +195,17 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
         const int64_t t0 = k * kTT;
         const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
         stage(t0, nt, true);
+        if (k > 0 && tid < 4 * CH) {   // the previous tile's rows into L2 while this one runs
+            const int cl = tid % CH, which = tid / CH;
+            if (d0 + cl < p.dim) {
+                const int64_t row = (b * p.dim + d0 + cl) * L + t0 - kTT;
+                const void* q = which == 0 ? static_cast<const void*>(static_cast<const T*>(p.u) + row)
+                              : which == 1 ? static_cast<const void*>(static_cast<const T*>(p.delta) + row)
+                              : which == 2 ? static_cast<const void*>(p.dy + row)
+                              : (HAS_Z ? static_cast<const void*>(static_cast<const T*>(p.z) + row) : nullptr);
+                if (q) asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+            }
+        }
         // recompute the tile's states (row 0: the state before the tile)
 #pragma unroll
         for (int n = 0; n < S; n++) Hs[tid * S + n] = h[n] = active ? ck[k * N + n] : 0.0f;
