@@ -61,7 +61,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_scan_bwd.restype = i32
         lib.oracle_scan_bwd.argtypes = [i64, i64, i64, i64, i32, i32,
                                         vp, vp, vp, vp, vp, vp, vp, vp, i32,
-                                        dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, i32]
+                                        dp, dp, vp, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, i32]
         _lib_cache[path] = lib
     return _lib_cache[path]
 
@@ -173,7 +173,7 @@ def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
-             dlast=None, nthreads: int = 1, lib: ctypes.CDLL | None = None):
+             dlast=None, channels=None, nthreads: int = 1, lib: ctypes.CDLL | None = None):
     """Oracle backward scan: the gradients of a loss with dLoss/dy = ``dy``
     (batch, dim, L) and dLoss/dlast_state = ``dlast`` (batch, dim, N, or
     None) with respect to every input of ``scan_fwd`` (zero initial state).
@@ -183,6 +183,11 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
     dh0 (batch, dim, N: the gradient with respect to the initial state).
     The per-channel C code leaves the sums over channels (dB, dC) and over
     the batch (dA, dD, ddelta_bias) to this wrapper.
+
+    ``channels``: flat ids b*dim + d to compute instead of all.  Then the
+    result holds the per-channel rows instead of the sums: du, ddelta, dz
+    (nchan, L), dA_chan (nchan, N), dD_chan, ddelta_bias_chan (nchan,),
+    dh0 (nchan, N); dB, dC are not formed (they need every channel).
     """
     lib = lib or load()
     batch, dim, L = (int(s) for s in u.shape)
@@ -200,19 +205,32 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
     dy = np.ascontiguousarray(np.asarray(dy, dtype=np.float64).reshape(batch, dim, L))
     if dlast is not None:
         dlast = np.ascontiguousarray(np.asarray(dlast, dtype=np.float64).reshape(batch, dim, N))
-    du = np.empty((batch, dim, L)); ddelta = np.empty((batch, dim, L))
-    dz = np.empty((batch, dim, L)) if z is not None else None
-    dA = np.empty((batch, dim, N)); dD = np.empty((batch, dim)); dbias = np.empty((batch, dim))
-    dBc = np.empty((batch, dim, L, N)); dCc = np.empty((batch, dim, L, N))
-    dh0 = np.empty((batch, dim, N))
+    if channels is None:
+        chan, nchan = None, batch * dim
+    else:
+        chan = np.ascontiguousarray(np.asarray(channels, dtype=np.int64))
+        nchan = int(chan.size)
+    du = np.empty((nchan, L)); ddelta = np.empty((nchan, L))
+    dz = np.empty((nchan, L)) if z is not None else None
+    dA = np.empty((nchan, N)); dD = np.empty(nchan); dbias = np.empty(nchan)
+    dBc = np.empty((nchan, L, N)); dCc = np.empty((nchan, L, N))
+    dh0 = np.empty((nchan, N))
     rc = lib.oracle_scan_bwd(batch, dim, N, L, io, pio,
                              _ptr(arrs["u"][0]), _ptr(arrs["delta"][0]), _ptr(parr["A"][0]),
                              _ptr(arrs["B"][0]), _ptr(arrs["C"][0]), _ptr(parr["D"][0]),
                              _ptr(arrs["z"][0]), _ptr(parr["bias"][0]), int(bool(delta_softplus)),
-                             _ptr(dy), _ptr(dlast), _ptr(du), _ptr(ddelta), _ptr(dz), _ptr(dA),
-                             _ptr(dD), _ptr(dbias), _ptr(dBc), _ptr(dCc), _ptr(dh0), int(nthreads))
+                             _ptr(dy), _ptr(dlast), _ptr(chan), nchan, _ptr(du), _ptr(ddelta),
+                             _ptr(dz), _ptr(dA), _ptr(dD), _ptr(dbias), _ptr(dBc), _ptr(dCc),
+                             _ptr(dh0), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_scan_bwd rejected its arguments")
-    return {"du": du, "ddelta": ddelta, "dz": dz, "dA": dA.sum(axis=0), "dD": dD.sum(axis=0),
-            "ddelta_bias": dbias.sum(axis=0), "dB": dBc.sum(axis=1), "dC": dCc.sum(axis=1),
-            "dh0": dh0}
+    if channels is not None:
+        return {"du": du, "ddelta": ddelta, "dz": dz, "dA_chan": dA, "dD_chan": dD,
+                "ddelta_bias_chan": dbias, "dh0": dh0}
+    sh = (batch, dim)
+    return {"du": du.reshape(*sh, L), "ddelta": ddelta.reshape(*sh, L),
+            "dz": None if dz is None else dz.reshape(*sh, L),
+            "dA": dA.reshape(*sh, N).sum(axis=0), "dD": dD.reshape(sh).sum(axis=0),
+            "ddelta_bias": dbias.reshape(sh).sum(axis=0),
+            "dB": dBc.reshape(*sh, L, N).sum(axis=1), "dC": dCc.reshape(*sh, L, N).sum(axis=1),
+            "dh0": dh0.reshape(*sh, N)}

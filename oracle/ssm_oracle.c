@@ -242,16 +242,20 @@ typedef struct {
     int io, pio;
     const void *u, *delta, *A, *B, *C, *D, *z, *bias;
     int softplus_on;
-    const double *dy, *dlast;   /* nchan x L, nchan x N (dlast may be NULL) */
+    const double *dy, *dlast;   /* (batch, dim, L), (batch, dim, N) (dlast may be NULL) */
     double *du, *ddelta, *dz, *dA, *dD, *dbias, *dBc, *dCc, *dh0;
+    const int64_t* chan;        /* flat channel ids, or NULL for all */
     int64_t nchan, next;
     pthread_mutex_t mu;
 } bwd_job;
 
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
 
-static void bwd_channel(const bwd_job* j, int64_t c, double* hs, double* g) {
+/* channel c = chan[k] (or k); its outputs go to row k of the compact arrays,
+ * dy and dlast are read at row c of the full arrays */
+static void bwd_channel(const bwd_job* j, int64_t k, double* hs, double* g) {
     const int64_t L = j->seqlen, N = j->dstate;
+    const int64_t c = j->chan ? j->chan[k] : k;
     const int64_t b = c / j->dim, d = c % j->dim;
     const int64_t row = c * L, bc_row = b * L * N;
     const double bias = j->bias ? load(j->pio, j->bias, d) : 0.0;
@@ -270,7 +274,7 @@ static void bwd_channel(const bwd_job* j, int64_t c, double* hs, double* g) {
     /* reverse */
     for (int64_t n = 0; n < N; n++) {
         g[n] = j->dlast ? j->dlast[c * N + n] : 0.0;
-        j->dA[c * N + n] = 0.0;
+        j->dA[k * N + n] = 0.0;
     }
     double dD = 0.0, dbias = 0.0;
     for (int64_t t = L - 1; t >= 0; t--) {
@@ -287,9 +291,9 @@ static void bwd_channel(const bwd_job* j, int64_t c, double* hs, double* g) {
             const double zv = load(j->io, j->z, row + t);
             const double sg = sigmoid(zv);
             ds = dyv * zv * sg;
-            j->dz[c * L + t] = dyv * s * sg * (1.0 + zv * (1.0 - sg));
+            j->dz[k * L + t] = dyv * s * sg * (1.0 + zv * (1.0 - sg));
         } else if (j->dz) {
-            j->dz[c * L + t] = 0.0;
+            j->dz[k * L + t] = 0.0;
         }
         dD += ds * x;
         double dx = ds * Dskip, ddt = 0.0;
@@ -299,22 +303,22 @@ static void bwd_channel(const bwd_job* j, int64_t c, double* hs, double* g) {
             const double An = load(j->pio, j->A, d * N + n);
             const double a = exp(dt * An);
             g[n] += ds * Cv;
-            j->dCc[(c * L + t) * N + n] = ds * h[n];
+            j->dCc[(k * L + t) * N + n] = ds * h[n];
             ddt += g[n] * (An * a * hp[n] + Bv * x);
             dx += g[n] * dt * Bv;
-            j->dBc[(c * L + t) * N + n] = g[n] * dt * x;
-            j->dA[c * N + n] += g[n] * dt * a * hp[n];
+            j->dBc[(k * L + t) * N + n] = g[n] * dt * x;
+            j->dA[k * N + n] += g[n] * dt * a * hp[n];
             g[n] *= a;
         }
         const double dv = j->softplus_on ? ddt * sigmoid(v) : ddt;
-        j->ddelta[c * L + t] = dv;
-        j->du[c * L + t] = dx;
+        j->ddelta[k * L + t] = dv;
+        j->du[k * L + t] = dx;
         dbias += dv;
     }
-    j->dD[c] = dD;
-    j->dbias[c] = dbias;
+    j->dD[k] = dD;
+    j->dbias[k] = dbias;
     if (j->dh0)
-        for (int64_t n = 0; n < N; n++) j->dh0[c * N + n] = g[n];
+        for (int64_t n = 0; n < N; n++) j->dh0[k * N + n] = g[n];
 }
 
 static void* bwd_worker(void* arg) {
@@ -328,10 +332,10 @@ static void* bwd_worker(void* arg) {
     }
     for (;;) {
         pthread_mutex_lock(&j->mu);
-        const int64_t c = j->next++;
+        const int64_t k = j->next++;
         pthread_mutex_unlock(&j->mu);
-        if (c >= j->nchan) break;
-        bwd_channel(j, c, hs, g);
+        if (k >= j->nchan) break;
+        bwd_channel(j, k, hs, g);
     }
     free(hs);
     free(g);
@@ -339,26 +343,33 @@ static void* bwd_worker(void* arg) {
 }
 
 /*
- * Backward selective scan over every channel (see the comment above).
- * Inputs as for oracle_scan_fwd; dy is (batch, dim, L) fp64 and dlast
- * (batch, dim, N) fp64 or NULL.  Outputs (fp64, per channel): du, ddelta,
- * dz (batch, dim, L; dz may be NULL when z is), dA (batch, dim, N: the
- * channel's share, summed over the batch by the caller), dD, dbias
- * (batch, dim), dBc, dCc (batch, dim, L, N: per-channel terms) and dh0
- * (batch, dim, N) or NULL.  Returns 0, or -1 on a bad argument.
+ * Backward selective scan over the channels listed in `chan` (flat ids
+ * b*dim + d; NULL means every channel in order, and then nchan must equal
+ * batch*dim); see the comment above.  Inputs as for oracle_scan_fwd; dy is
+ * (batch, dim, L) fp64 and dlast (batch, dim, N) fp64 or NULL, both full.
+ * Outputs (fp64, compact, one row per listed channel): du, ddelta, dz
+ * (nchan x L; dz may be NULL when z is), dA (nchan x N: the channel's
+ * share, summed over the batch by the caller), dD, dbias (nchan), dBc, dCc
+ * (nchan x L x N: per-channel terms) and dh0 (nchan x N) or NULL.
+ * Returns 0, or -1 on a bad argument.
  */
 int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io, int pio,
                     const void* u, const void* delta, const void* A, const void* B,
                     const void* C, const void* D, const void* z, const void* delta_bias,
-                    int delta_softplus, const double* dy, const double* dlast, double* du,
-                    double* ddelta, double* dz, double* dA, double* dD, double* dbias,
-                    double* dBc, double* dCc, double* dh0, int nthreads) {
+                    int delta_softplus, const double* dy, const double* dlast,
+                    const int64_t* chan, int64_t nchan, double* du, double* ddelta, double* dz,
+                    double* dA, double* dD, double* dbias, double* dBc, double* dCc, double* dh0,
+                    int nthreads) {
     if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
     if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dD || !dbias || !dBc ||
         !dCc)
         return -1;
     if (z && !dz) return -1;
     if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
+    if (!chan && nchan != batch * dim) return -1;
+    if (chan)
+        for (int64_t k = 0; k < nchan; k++)
+            if (chan[k] < 0 || chan[k] >= batch * dim) return -1;
     bwd_job j;
     memset(&j, 0, sizeof j);
     j.batch = batch; j.dim = dim; j.dstate = dstate; j.seqlen = seqlen;
@@ -368,7 +379,8 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
     j.dy = dy; j.dlast = dlast;
     j.du = du; j.ddelta = ddelta; j.dz = dz; j.dA = dA; j.dD = dD; j.dbias = dbias;
     j.dBc = dBc; j.dCc = dCc; j.dh0 = dh0;
-    j.nchan = batch * dim;
+    j.chan = chan;
+    j.nchan = nchan;
     j.next = 0;
     pthread_mutex_init(&j.mu, NULL);
     if (nthreads < 1) nthreads = 1;

@@ -96,3 +96,29 @@ def test_backward_oracle_zero_gradient_and_linearity():
     for k in g1:
         if g1[k] is not None:
             np.testing.assert_allclose(g12[k], g1[k] + 2.0 * g2[k], rtol=1e-10, atol=1e-12)
+
+
+def test_backward_oracle_channel_subset_matches_full():
+    """A channel subset gives exactly the full computation's per-channel rows,
+    and the per-channel shares sum to the full dA, dD, ddelta_bias."""
+    rng = np.random.default_rng(5)
+    b, d, L, N = 3, 5, 11, 4
+    x = make(rng, b, d, L, N, z=True, softplus=True, bias=True, skip=True)
+    dy = rng.standard_normal((b, d, L))
+    dl = rng.standard_normal((b, d, N))
+    full = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x["D"], z=x["z"],
+                           delta_bias=x["delta_bias"], delta_softplus=True, dlast=dl)
+    chans = [0, 7, 14, 3]
+    sub = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x["D"], z=x["z"],
+                          delta_bias=x["delta_bias"], delta_softplus=True, dlast=dl, channels=chans)
+    for k, c in enumerate(chans):
+        bb, dd = divmod(c, d)
+        for name in ("du", "ddelta", "dz", "dh0"):
+            assert np.array_equal(sub[name][k], full[name][bb, dd]), name
+    allc = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x["D"], z=x["z"],
+                           delta_bias=x["delta_bias"], delta_softplus=True, dlast=dl,
+                           channels=list(range(b * d)))
+    np.testing.assert_allclose(allc["dA_chan"].reshape(b, d, N).sum(0), full["dA"], rtol=1e-14)
+    np.testing.assert_allclose(allc["dD_chan"].reshape(b, d).sum(0), full["dD"], rtol=1e-14)
+    np.testing.assert_allclose(allc["ddelta_bias_chan"].reshape(b, d).sum(0), full["ddelta_bias"],
+                               rtol=1e-14)
