@@ -19,7 +19,7 @@ import torch
 from . import _lib
 from ._lib import SSMError, ssm_dims
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
+__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "selective_scan", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
            "library_path", "version"]
 
 _IO = {torch.float32: _lib.SSM_IO_F32, torch.bfloat16: _lib.SSM_IO_BF16}
@@ -261,3 +261,37 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     if rc != 0:
         raise SSMError(rc, "ssm_scan_bwd")
     return g
+
+
+class _SelectiveScan(torch.autograd.Function):
+    """Forward through ssm_scan_fwd, backward through ssm_scan_bwd (which
+    recomputes the forward states; nothing but the inputs is saved)."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus):
+        y, last = ssm_scan_fwd(u, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
+                               delta_softplus=delta_softplus, return_last_state=True)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
+        ctx.delta_softplus = delta_softplus
+        return y, last
+
+    @staticmethod
+    def backward(ctx, dy, dlast):
+        u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
+        dy = torch.zeros_like(u, dtype=torch.float32) if dy is None else dy.float().contiguous()
+        dlast = None if dlast is None else dlast.float().contiguous()
+        g = ssm_scan_bwd(u, delta, A, B, C, dy, D=D, z=z, delta_bias=delta_bias,
+                         delta_softplus=ctx.delta_softplus, dlast_state=dlast)
+        cast = lambda t, like: None if t is None else t.to(like.dtype)
+        return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B),
+                cast(g["dC"], C), g["dD"] if D is not None else None,
+                cast(g["dz"], z) if z is not None else None,
+                g["ddelta_bias"] if delta_bias is not None else None, None)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False):
+    """Differentiable forward scan on CUDA tensors: returns (y, last_state)
+    and, under autograd, gradients for every tensor input from the library's
+    backward kernel.  Gradients are computed in fp32 and returned in each
+    input's dtype."""
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus))

@@ -125,3 +125,34 @@ def test_bwd_layer_shape_m2p8_sampled_channels():
         gt = got[gname][ds].double().cpu().numpy()
         err = np.abs(gt - r).max()
         assert err <= 1e-3 * np.abs(r).max() + 1e-6, (gname, err)
+
+
+def test_autograd_wrapper_returns_the_library_gradients():
+    """selective_scan under torch.autograd: the forward equals ssm_scan_fwd
+    bit for bit and the gradients equal ssm_scan_bwd's for the same upstream
+    gradient (up to the fp32 atomics' summation order for dA, dB, dC, dD,
+    ddelta_bias), and they match the oracle."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=45, io="f32", last_state=True)
+    inp = make_scan_inputs(w, seed=4)
+    g = to_cuda(inp)
+    leaves = {k: g[k].clone().requires_grad_(True) for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")}
+    y, last = ssm.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"],
+                                 D=leaves["D"], z=leaves["z"], delta_bias=leaves["delta_bias"],
+                                 delta_softplus=True)
+    y_ref, last_ref = ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                       delta_bias=g["delta_bias"], delta_softplus=True)
+    assert torch.equal(y.detach(), y_ref) and torch.equal(last.detach(), last_ref)
+    rng = np.random.default_rng(8)
+    wy = torch.from_numpy(rng.standard_normal(tuple(y.shape)).astype(np.float32)).cuda()
+    wl = torch.from_numpy(rng.standard_normal(tuple(last.shape)).astype(np.float32)).cuda()
+    ((y * wy).sum() + (last * wl).sum()).backward()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], wy.double().cpu().numpy(),
+                          D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"], delta_softplus=True,
+                          dlast=wl.double().cpu().numpy())
+    for k, rk in (("u", "du"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("D", "dD"),
+                  ("z", "dz"), ("delta_bias", "ddelta_bias")):
+        gt = leaves[k].grad.double().cpu().numpy()
+        r = ref[rk]
+        assert gt.shape == r.shape, (k, gt.shape, r.shape)
+        err = np.abs(gt - r).max()
+        assert err <= 1e-3 * np.abs(r).max() + 1e-6, (k, err)
