@@ -366,7 +366,8 @@ def time_scan_bwd(w, local, reps=5):
     dev = torch.device("cuda", local)
     inp = make_scan_inputs(w, seed=0)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    dy = torch.randn(w.batch, w.dim, w.seqlen, device=dev)
+    dy = torch.randn(w.batch, w.dim, w.seqlen, device=dev,
+                     generator=torch.Generator(device=dev).manual_seed(0))
 
     def run():
         return ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], z=g["z"],
