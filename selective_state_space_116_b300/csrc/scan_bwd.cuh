@@ -10,8 +10,9 @@
 //   pass 1  the forward recurrence over the whole sequence, writing only the
 //           state at the start of every 8-token tile to the workspace
 //           (batch x dim x ceil(L/8) x N fp32 checkpoints);
-//   (each 8-token tile's inputs are first staged in shared memory by the
-//   whole CTA with coalesced loads, Delta computed once per element)
+//   (each 8-token tile's inputs are staged in shared memory by the whole CTA
+//   with coalesced loads, Delta computed once per element; the loads of the
+//   next tile are issued into registers while the current tile computes)
 //   pass 2  the tiles in reverse order: the tile's states are recomputed
 //           from its checkpoint into shared memory, then the adjoint
 //           recurrence runs backwards through the tile:
@@ -134,30 +135,55 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
     const T* bz = static_cast<const T*>(p.z);
     const T* bB = static_cast<const T*>(p.B) + b * L * N;
     const T* bC = static_cast<const T*>(p.C) + b * L * N;
-    auto stage = [&](int64_t t0, int nt, bool full) {
-        for (int i = tid; i < CH * kTT; i += kThreads) {
+    // A tile's inputs are fetched into registers (`fetch`, global loads in
+    // flight while the previous tile computes) and written to shared memory
+    // later (`put`).
+    constexpr int E = (CH * kTT + kThreads - 1) / kThreads;   // elements per thread
+    constexpr int EB = (kTT * N + kThreads - 1) / kThreads;
+    float rx[E], rv[E], rz[E], rd[E], rb[EB], rc[EB];
+    auto fetch = [&](int64_t t0, int nt, bool full) {
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = tid + e * kThreads;
             const int cl = i / kTT, j = i % kTT;
-            const bool ok = d0 + cl < p.dim && j < nt;
+            const bool ok = i < CH * kTT && d0 + cl < p.dim && j < nt;
             const int64_t gi2 = ((b * p.dim + d0 + cl) * L + t0 + j);
-            float x = 0.0f, vv = 0.0f, dt = 0.0f;
-            if (ok) {
-                x = io<T>::load(bu, gi2);
-                vv = io<T>::load(bdl, gi2) + ((p.bias) ? p.bias[d0 + cl] : 0.0f);
-                dt = SOFTPLUS ? softplus(vv) : vv;
-            }
-            XU[cl * ROW + j] = x;
-            DT[cl * ROW + j] = dt;
-            VV[cl * ROW + j] = vv;
-            if (full) {
-                ZZ[cl * ROW + j] = (ok && HAS_Z) ? io<T>::load(bz, gi2) : 0.0f;
-                DY[cl * ROW + j] = ok ? p.dy[gi2] : 0.0f;
+            rx[e] = ok ? io<T>::load(bu, gi2) : 0.0f;
+            rv[e] = ok ? io<T>::load(bdl, gi2) + ((p.bias) ? p.bias[d0 + cl] : 0.0f) : 0.0f;
+            rz[e] = (full && ok && HAS_Z) ? io<T>::load(bz, gi2) : 0.0f;
+            rd[e] = (full && ok) ? p.dy[gi2] : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < EB; e++) {
+            const int i = tid + e * kThreads;
+            const bool ok = i < kTT * N && i / N < nt;
+            rb[e] = ok ? io<T>::load(bB, t0 * N + i) : 0.0f;
+            rc[e] = (full && ok) ? io<T>::load(bC, t0 * N + i) : 0.0f;
+        }
+    };
+    auto put = [&](int nt, bool full) {
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = tid + e * kThreads;
+            if (i < CH * kTT) {
+                const int cl = i / kTT, j = i % kTT;
+                const bool ok = d0 + cl < p.dim && j < nt;
+                XU[cl * ROW + j] = rx[e];
+                VV[cl * ROW + j] = rv[e];
+                DT[cl * ROW + j] = ok ? (SOFTPLUS ? softplus(rv[e]) : rv[e]) : 0.0f;
+                if (full) {
+                    ZZ[cl * ROW + j] = rz[e];
+                    DY[cl * ROW + j] = rd[e];
+                }
             }
         }
-        for (int i = tid; i < kTT * N; i += kThreads) {
-            const int j = i / N;
-            const bool ok = j < nt;
-            BB[i] = ok ? io<T>::load(bB, t0 * N + i) : 0.0f;
-            if (full) CC[i] = ok ? io<T>::load(bC, t0 * N + i) : 0.0f;
+#pragma unroll
+        for (int e = 0; e < EB; e++) {
+            const int i = tid + e * kThreads;
+            if (i < kTT * N) {
+                BB[i] = rb[e];
+                if (full) CC[i] = rc[e];
+            }
         }
     };
 
@@ -165,6 +191,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
     float h[S];
 #pragma unroll
     for (int n = 0; n < S; n++) h[n] = 0.0f;
+    if (p.ntiles > 0) fetch(0, (int)(L < kTT ? L : kTT), false);
     for (int64_t k = 0; k < p.ntiles; k++) {
         const int64_t t0 = k * kTT;
         const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
@@ -172,8 +199,12 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
             for (int n = 0; n < S; n++) ck[k * N + n] = h[n];
         }
-        stage(t0, nt, false);
+        put(nt, false);
         __syncthreads();
+        if (k + 1 < p.ntiles) {
+            const int64_t t1 = t0 + kTT;
+            fetch(t1, (int)(L - t1 < kTT ? L - t1 : kTT), false);
+        }
         for (int j = 0; j < nt; j++) {
             const float dt = DT[lc * ROW + j];
             const float dtx = dt * XU[lc * ROW + j];
@@ -191,25 +222,19 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
         dA[n] = 0.0f;
     }
     float dD = 0.0f, dbias = 0.0f;
+    if (p.ntiles > 0) {
+        const int64_t tl = (p.ntiles - 1) * kTT;
+        fetch(tl, (int)(L - tl < kTT ? L - tl : kTT), true);
+    }
     for (int64_t k = p.ntiles - 1; k >= 0; k--) {
         const int64_t t0 = k * kTT;
         const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
-        stage(t0, nt, true);
-        if (k > 0 && tid < 4 * CH) {   // the previous tile's rows into L2 while this one runs
-            const int cl = tid % CH, which = tid / CH;
-            if (d0 + cl < p.dim) {
-                const int64_t row = (b * p.dim + d0 + cl) * L + t0 - kTT;
-                const void* q = which == 0 ? static_cast<const void*>(static_cast<const T*>(p.u) + row)
-                              : which == 1 ? static_cast<const void*>(static_cast<const T*>(p.delta) + row)
-                              : which == 2 ? static_cast<const void*>(p.dy + row)
-                              : (HAS_Z ? static_cast<const void*>(static_cast<const T*>(p.z) + row) : nullptr);
-                if (q) asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
-            }
-        }
+        put(nt, true);
         // recompute the tile's states (row 0: the state before the tile)
 #pragma unroll
         for (int n = 0; n < S; n++) Hs[tid * S + n] = h[n] = active ? ck[k * N + n] : 0.0f;
         __syncthreads();
+        if (k > 0) fetch(t0 - kTT, kTT, true);   // the next tile back, in flight during this one
         for (int j = 0; j < nt; j++) {
             const float dt = DT[lc * ROW + j];
             const float dtx = dt * XU[lc * ROW + j];
