@@ -53,7 +53,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         i64, i32, vp, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
         lib.oracle_scan_fwd.restype = i32
         lib.oracle_scan_fwd.argtypes = [i64, i64, i64, i64, i32, i32,
-                                        vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                        vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                         vp, i64, dp, dp, dp, i32]
         lib.oracle_state_step.restype = i32
         lib.oracle_state_step.argtypes = [i64, i64, i64, i32, i32,
@@ -93,7 +93,8 @@ def _ptr(a):
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
-             channels=None, h0=None, nthreads: int = 1, lib: ctypes.CDLL | None = None):
+             channels=None, h0=None, nthreads: int = 1, lib: ctypes.CDLL | None = None,
+             zoh: bool = False):
     """Oracle forward scan.
 
     Shapes: u, delta, z (batch, dim, L); B, C (batch, L, N); A (dim, N);
@@ -101,6 +102,8 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     or fp64); A/D/delta_bias share another (fp32 or fp64).
     ``channels``: optional flat ids b*dim + d to compute (default: all).
     ``h0``: optional fp64 initial state, one row of N per computed channel.
+    ``zoh``: the exact zero-order-hold input term (exp(Delta A) - 1) / A B x
+    instead of the first-order Delta B x.
     Returns (y, last_state) as fp64 arrays of shape (nchan, L) and (nchan, N);
     with channels=None they are reshaped to (batch, dim, L) and (batch, dim, N).
     """
@@ -135,7 +138,8 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                              _ptr(arrs["u"][0]), _ptr(arrs["delta"][0]), _ptr(parr["A"][0]),
                              _ptr(arrs["B"][0]), _ptr(arrs["C"][0]), _ptr(parr["D"][0]),
                              _ptr(arrs["z"][0]), _ptr(parr["bias"][0]), int(bool(delta_softplus)),
-                             _ptr(chan), nchan, _ptr(h0), _ptr(y), _ptr(last), int(nthreads))
+                             int(bool(zoh)), _ptr(chan), nchan, _ptr(h0), _ptr(y), _ptr(last),
+                             int(nthreads))
     if rc != 0:
         raise ValueError("oracle_scan_fwd rejected its arguments")
     if channels is None:

@@ -19,8 +19,12 @@ import numpy as np
 from scipy.special import expit
 
 
-def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False):
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+             zoh=False, h0=None):
     """u, delta, z: (batch, dim, L); B, C: (batch, L, N); A: (dim, N).
+    zoh: the exact zero-order-hold input weight expm1(Delta_s A_n) / A_n in
+    place of Delta_s (Delta_s where A_n = 0).  h0: (batch, dim, N) initial
+    state, carried to token t by exp(A_n * sum_{r<=t} Delta_r).
     Returns (y (batch, dim, L), last_state (batch, dim, N)) in fp64."""
     u = np.asarray(u, np.float64)
     delta = np.asarray(delta, np.float64)
@@ -37,12 +41,22 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     # decay[b,d,t,s,n] = exp(A_n * gap) for s <= t, else 0 (exp(-inf))
     expo = A[None, :, None, None, :] * gap[..., None]
     decay = np.exp(np.where(causal[None, None, :, :, None], expo, -np.inf))
-    drive = (dt * u)[..., None] * B[:, None, :, :]                   # (b, d, s, n)
+    if zoh:   # weight[b,d,s,n] = expm1(dt_s A_n) / A_n, or dt_s where A_n = 0
+        prod = dt[..., None] * A[None, :, None, :]
+        safe = np.where(A == 0.0, 1.0, A)[None, :, None, :]
+        weight = np.where(A[None, :, None, :] == 0.0, dt[..., None], np.expm1(prod) / safe)
+    else:
+        weight = np.broadcast_to(dt[..., None], dt.shape + (N,))
+    drive = (weight * u[..., None]) * B[:, None, :, :]                # (b, d, s, n)
     h = np.einsum("bdtsn,bdsn->bdtn", decay, drive)                   # (b, d, t, n)
+    if h0 is not None:   # the initial state decays by exp(A_n S_t)
+        h = h + np.exp(A[None, :, None, :] * S[..., None]) * np.asarray(h0, np.float64)[:, :, None, :]
     y = np.einsum("btn,bdtn->bdt", C, h)
     if D is not None:
         y = y + np.asarray(D, np.float64)[None, :, None] * u
     if z is not None:
         z = np.asarray(z, np.float64)
         y = y * (z * expit(z))
-    return y, h[:, :, -1, :].copy() if L > 0 else np.zeros((batch, dim, N))
+    if L == 0:
+        return y, (np.zeros((batch, dim, N)) if h0 is None else np.array(h0, np.float64))
+    return y, h[:, :, -1, :].copy()

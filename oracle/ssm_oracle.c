@@ -15,10 +15,14 @@
  *     interactive paper explainer, Chapter 02 "The Discretized View").
  *   - Zero-order-hold discretisation with step size Delta: Abar = exp(Delta A)
  *     ("Mamba remembers by forgetting, read closely", interactiveml.org,
- *     the scalar recurrence h_t = exp(-Delta_t) h_{t-1} + ...), and the
- *     first-order input term Bbar x = Delta B x (the plain reading adopted by
- *     this library; the pages say only that Abar and Bbar are derived from
- *     (Delta, A, B)).
+ *     the scalar recurrence h_t = exp(-Delta_t) h_{t-1} + ...), and one of
+ *     two input terms, chosen by the caller:
+ *       Bbar x = Delta B x (the first-order form, the library's default; the
+ *       pages say only that Abar and Bbar are derived from (Delta, A, B)), or
+ *       Bbar x = (exp(Delta A) - 1) / A * B x, the exact zero-order hold of
+ *       a diagonal A (with the limit Delta B x at A = 0).  For A = -1, B = 1
+ *       this is the interactiveml.org scalar update
+ *       h_t = exp(-Delta_t) h_{t-1} + (1 - exp(-Delta_t)) x_t.
  *   - Selection: Delta, B and C are given per token ("How it works",
  *     elemedex; "The Discretized View", papermap).  A is diagonal: one real
  *     decay per (channel, state) pair.
@@ -67,11 +71,21 @@ static double softplus(double v) {
 /* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* The factor that multiplies B x in the state update: Delta for the
+ * first-order input term, (exp(Delta A) - 1) / A for the exact zero-order
+ * hold, whose limit at A = 0 is Delta (expm1 keeps it accurate when
+ * Delta A is small). */
+static double input_weight(int zoh, double dt, double a) {
+    if (!zoh) return dt;
+    return a != 0.0 ? expm1(dt * a) / a : dt;
+}
+
 typedef struct {
     int64_t batch, dim, dstate, seqlen;
     int io, pio; /* element types: io for u/delta/B/C/z, pio for A/D/bias */
     const void *u, *delta, *A, *B, *C, *D, *z, *bias;
     int softplus_on;
+    int zoh;             /* 0: Bbar = Delta B; 1: Bbar = (exp(Delta A) - 1) / A B */
     const int64_t* chan; /* flat channel ids b*dim + d, or NULL for all */
     int64_t nchan;
     double* y;          /* nchan x seqlen */
@@ -99,7 +113,7 @@ static void scan_channel(const scan_job* j, int64_t k, double* h) {
         for (int64_t n = 0; n < N; n++) {
             const double a = load(j->pio, j->A, d * N + n);
             const double Bv = load(j->io, j->B, bc_row + t * N + n);
-            h[n] = exp(dt * a) * h[n] + dt * Bv * x;
+            h[n] = exp(dt * a) * h[n] + input_weight(j->zoh, dt, a) * Bv * x;
         }
         for (int64_t n = 0; n < N; n++)
             yv += load(j->io, j->C, bc_row + t * N + n) * h[n];
@@ -131,15 +145,16 @@ static void* scan_worker(void* arg) {
  * b*dim + d; NULL means every channel in order, and then nchan must equal
  * batch*dim).  Outputs are compact: y is nchan x seqlen, last_state is
  * nchan x dstate.  h0 (nchan x dstate, fp64) is an optional initial state;
- * NULL means zero.  Channels are independent, so they are spread over
- * `nthreads` POSIX threads; each channel's loop is sequential.
- * Returns 0, or -1 on a bad argument.
+ * NULL means zero.  zoh selects the input term (0: Delta B x, 1: the exact
+ * zero-order hold (exp(Delta A) - 1) / A B x).  Channels are independent, so
+ * they are spread over `nthreads` POSIX threads; each channel's loop is
+ * sequential.  Returns 0, or -1 on a bad argument.
  */
 int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io, int pio,
                     const void* u, const void* delta, const void* A, const void* B,
                     const void* C, const void* D, const void* z, const void* delta_bias,
-                    int delta_softplus, const int64_t* chan, int64_t nchan, const double* h0,
-                    double* y, double* last_state, int nthreads) {
+                    int delta_softplus, int zoh, const int64_t* chan, int64_t nchan,
+                    const double* h0, double* y, double* last_state, int nthreads) {
     if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || nchan < 0) return -1;
     if (!u || !delta || !A || !B || !C || !y) return -1;
     if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
@@ -152,7 +167,7 @@ int oracle_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
     j.batch = batch; j.dim = dim; j.dstate = dstate; j.seqlen = seqlen;
     j.io = io; j.pio = pio;
     j.u = u; j.delta = delta; j.A = A; j.B = B; j.C = C; j.D = D; j.z = z;
-    j.bias = delta_bias; j.softplus_on = delta_softplus;
+    j.bias = delta_bias; j.softplus_on = delta_softplus; j.zoh = zoh != 0;
     j.chan = chan; j.nchan = nchan; j.y = y; j.last_state = last_state; j.h0 = h0;
     j.next = 0;
     pthread_mutex_init(&j.mu, NULL);

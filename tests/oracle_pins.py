@@ -43,7 +43,7 @@ def close(got, want, rtol, atol=0.0, what=""):
         f"at {np.unravel_index(np.argmax(err - bound), err.shape)}")
 
 
-def _scalar_scan(lib, delta, u, A=-1.0, h0=None, N=1, extra_A=None):
+def _scalar_scan(lib, delta, u, A=-1.0, h0=None, N=1, extra_A=None, zoh=False):
     """Run the oracle scan with one channel whose state 0 carries the
     scalar recurrence (B=C=1); states 1..N-1, if any, get B=C=0."""
     L = len(delta)
@@ -61,7 +61,7 @@ def _scalar_scan(lib, delta, u, A=-1.0, h0=None, N=1, extra_A=None):
     y, last = oracle.scan_fwd(np.asarray(u, np.float64)[None, None],
                               np.asarray(delta, np.float64)[None, None],
                               Am, Bm, Cm, channels=[0] if hh is not None else None,
-                              h0=hh, lib=lib)
+                              h0=hh, lib=lib, zoh=zoh)
     return np.asarray(y).reshape(-1), np.asarray(last).reshape(-1)
 
 
@@ -302,6 +302,88 @@ def pin_decode_and_subset(lib):
     assert np.array_equal(yt, y) and np.array_equal(lt, last)
 
 
+# -- pin 10: the exact zero-order-hold input term -------------------------------
+def pin_zoh_page_loop(lib):
+    """With the exact input term the scan IS the interactiveml.org scalar
+    loop (A = -1, B = C = 1, N = 1), with no input substitution."""
+    rng = np.random.default_rng(10)
+    L = 500
+    x = rng.standard_normal(L)
+    d = rng.uniform(0.001, 4.0, L)
+    want = page_scalar_loop(x, d)
+    y, last = _scalar_scan(lib, d, x, zoh=True)
+    close(y, want, 1e-12, 1e-14, what="page scalar loop, exact ZOH")
+    close(last[0], want[-1], 1e-12, what="page scalar loop, exact ZOH, last state")
+    # and it continues from a given state exactly as the loop does
+    y, _ = _scalar_scan(lib, d, x, zoh=True, h0=0.75)
+    close(y, page_scalar_loop(x, d, state=0.75), 1e-12, 1e-14, what="page loop from state 0.75")
+
+
+def pin_zoh_closed_form(lib):
+    """Constant step, constant input 1: h_t = B (1 - e^{(t+1) Delta A}) / (-A);
+    for A = -1, B = 1 that is the page's 1 - e^{-Delta (t+1)}."""
+    for A, d, L in ((-1.0, 0.25, 1000), (-3.0, 0.02, 3000), (-1.0, 1e-3, 1 << 20)):
+        y, last = _scalar_scan(lib, np.full(L, d), np.ones(L), A=A, zoh=True)
+        t = np.arange(L)
+        want = -np.expm1((t + 1) * A * d) / (-A)
+        close(y, want, 1e-11, what=f"ZOH closed form A={A} d={d} L={L}")
+        close(last[0], want[-1], 1e-11, what="ZOH closed form last state")
+
+
+def pin_zoh_limits(lib):
+    rng = np.random.default_rng(11)
+    L = 64
+    d = rng.uniform(0.01, 0.5, L)
+    u = rng.standard_normal(L)
+    # A = 0: (e^{Delta A} - 1) / A -> Delta and e^{Delta A} = 1: a running sum
+    y, _ = _scalar_scan(lib, d, u, A=0.0, zoh=True)
+    close(y, np.cumsum(d * u), 1e-13, 1e-14, what="ZOH at A = 0: running sum of Delta u")
+    # tiny |A|: the exact term agrees with the first-order one to O(Delta A)
+    y1, _ = _scalar_scan(lib, d, u, A=-1e-9, zoh=True)
+    y0, _ = _scalar_scan(lib, d, u, A=-1e-9, zoh=False)
+    close(y1, y0, 1e-8, 1e-12, what="ZOH vs first order as A -> 0")
+    # Delta |A| huge: memoryless, h_t = B u_t / (-A)
+    y, _ = _scalar_scan(lib, np.full(L, 900.0), u, A=-2.0, zoh=True)
+    close(y, u / 2.0, 1e-13, 1e-14, what="ZOH memoryless limit")
+
+
+def pin_zoh_brute_force(lib):
+    rng = np.random.default_rng(12)
+    for gate, bias, softplus in ((False, False, False), (True, True, True), (True, False, True)):
+        L = int(rng.integers(1, 40))
+        kw = random_tiny(rng, 2, 3, L, 4, gate, bias, True, softplus)
+        kw["A"][0, 1] = 0.0                  # one state with A = 0 (the limit Delta)
+        y, last = oracle.scan_fwd(**kw, zoh=True, lib=lib)
+        yb, lb = brute.scan_fwd(**kw, zoh=True)
+        close(y, yb, 1e-12, 1e-12, what=f"ZOH brute y {gate, bias, softplus}")
+        close(last, lb, 1e-12, 1e-12, what="ZOH brute last_state")
+
+
+# -- pin 11: the initial state ----------------------------------------------------
+def pin_initial_state(lib):
+    rng = np.random.default_rng(13)
+    for zoh in (False, True):
+        kw = random_tiny(rng, 2, 3, 30, 4, True, True, True, True)
+        h0 = rng.standard_normal((2, 3, 4))
+        # against the unrolled sum, where h0 decays by exp(A_n sum_{r<=t} Delta_r)
+        y, last = oracle.scan_fwd(**kw, h0=h0.reshape(6, 4), zoh=zoh, lib=lib)
+        yb, lb = brute.scan_fwd(**kw, zoh=zoh, h0=h0)
+        close(y, yb, 1e-12, 1e-12, what=f"h0 brute y (zoh={zoh})")
+        close(last, lb, 1e-12, 1e-12, what=f"h0 brute last_state (zoh={zoh})")
+        # a scan split at k and resumed from its last_state is the whole scan
+        k = 11
+        head = {n: (v[..., :k] if n in ("u", "delta", "z") else v) for n, v in kw.items()}
+        head["B"], head["C"] = kw["B"][:, :k], kw["C"][:, :k]
+        tail = {n: (v[..., k:] if n in ("u", "delta", "z") else v) for n, v in kw.items()}
+        tail["B"], tail["C"] = kw["B"][:, k:], kw["C"][:, k:]
+        yf, lf = oracle.scan_fwd(**kw, zoh=zoh, lib=lib)
+        _, lh = oracle.scan_fwd(**head, zoh=zoh, lib=lib)
+        yt, lt = oracle.scan_fwd(**tail, h0=lh.reshape(6, 4), zoh=zoh, lib=lib)
+        close(yt, yf[..., k:], 1e-12, 1e-13, what=f"split at {k} and resumed, y (zoh={zoh})")
+        close(lt, lf, 1e-12, 1e-13, what=f"split at {k} and resumed, last_state (zoh={zoh})")
+
+
 ALL_PINS = [pin_gate_fixed, pin_gate_selective, pin_affine_compose, pin_page_scalar_zoh,
             pin_closed_form, pin_convolution, pin_brute_force, pin_special_cases,
-            pin_step_equals_scan, pin_decode_and_subset]
+            pin_step_equals_scan, pin_decode_and_subset, pin_zoh_page_loop,
+            pin_zoh_closed_form, pin_zoh_limits, pin_zoh_brute_force, pin_initial_state]

@@ -11,7 +11,12 @@ import oracle_pins
 
 # (name, text in ssm_oracle.c, replacement) -- every mutant stays in bounds.
 MUTANTS = [
-    ("drop_delta_in_input_term", "dt * Bv * x;", "Bv * x;"),
+    ("drop_delta_in_input_term", "if (!zoh) return dt;", "if (!zoh) return 1.0;"),
+    ("zoh_sign", "expm1(dt * a) / a", "expm1(-dt * a) / a"),
+    ("zoh_no_divide", "expm1(dt * a) / a", "expm1(dt * a)"),
+    ("zoh_limit_at_zero", "expm1(dt * a) / a : dt;", "expm1(dt * a) / a : 0.0;"),
+    ("zoh_ignored", "return a != 0.0 ? expm1(dt * a) / a : dt;", "return dt;"),
+    ("h0_ignored", "h[n] = j->h0 ? j->h0[k * N + n] : 0.0;", "h[n] = 0.0;"),
     ("wrong_sign_in_decay", "exp(dt * a) * h[n]", "exp(-dt * a) * h[n]"),
     ("drop_skip_term", "yv += Dskip * x;", "(void)Dskip;"),
     ("gate_sigmoid_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
@@ -33,7 +38,7 @@ def _output_before_update(src):
     upd = ("        for (int64_t n = 0; n < N; n++) {\n"
            "            const double a = load(j->pio, j->A, d * N + n);\n"
            "            const double Bv = load(j->io, j->B, bc_row + t * N + n);\n"
-           "            h[n] = exp(dt * a) * h[n] + dt * Bv * x;\n"
+           "            h[n] = exp(dt * a) * h[n] + input_weight(j->zoh, dt, a) * Bv * x;\n"
            "        }\n")
     out = ("        for (int64_t n = 0; n < N; n++)\n"
            "            yv += load(j->io, j->C, bc_row + t * N + n) * h[n];\n")
