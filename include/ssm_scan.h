@@ -294,6 +294,11 @@ SSM_API const char* ssm_status_string(int status);
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 SSM_API int ssm_version(void);
 
+/* Identifier of the sources and compiler flags the library was built from
+ * (a hash written in at build time; static text, never NULL).  The build
+ * script compares it with the sources on disk to decide whether to rebuild. */
+SSM_API const char* ssm_build_id(void);
+
 #ifdef __cplusplus
 }
 #endif

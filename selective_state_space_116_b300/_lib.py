@@ -28,7 +28,7 @@ SSM_IO_F32 = 0
 SSM_IO_BF16 = 1
 
 # every symbol include/ssm_scan.h declares
-EXPORTS = ("ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
+EXPORTS = ("ssm_build_id", "ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_host", "ssm_scan_fwd_noalloc",
            "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_workspace_size", "ssm_state_step",
            "ssm_status_string", "ssm_version")
@@ -84,6 +84,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     lib.ssm_status_string.argtypes = [i32]
     lib.ssm_version.restype = i32
     lib.ssm_version.argtypes = []
+    lib.ssm_build_id.restype = ctypes.c_char_p
+    lib.ssm_build_id.argtypes = []
     _lib = lib
     return lib
 

@@ -174,6 +174,21 @@ template <> __device__ __forceinline__ float gate<__nv_bfloat16>(float z) {
     return fmaf(hz, t, hz);
 }
 
+// gate on a pair of values, packed: the same operations as gate<T>.
+template <typename T> __device__ __forceinline__ float2 gate2(float2 z);
+template <> __device__ __forceinline__ float2 gate2<float>(float2 z) {
+    const float2 e = __fmul2_rn(make_float2(-z.x, -z.y), make_float2(kLog2e, kLog2e));
+    const float2 p = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(ex2(e.x), ex2(e.y)));
+    return __fmul2_rn(z, make_float2(rcp(p.x), rcp(p.y)));
+}
+template <> __device__ __forceinline__ float2 gate2<__nv_bfloat16>(float2 z) {
+    const float2 hz = __fmul2_rn(make_float2(0.5f, 0.5f), z);
+    float tx, ty;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(tx) : "f"(hz.x));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(ty) : "f"(hz.y));
+    return __ffma2_rn(hz, make_float2(tx, ty), hz);
+}
+
 // Copy tile [t0, t0 + kTL) of CH rows of a (rows, L) tensor into a raw plane.
 // VEC: rows are 16-byte aligned and L is a multiple of EPC, so a 16-byte chunk
 // is either wholly inside or wholly outside the tensor.
@@ -226,10 +241,14 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// NT consecutive tokens for one thread, software-pipelined: the B, C loads
-// and the 2^x of token t + 1 are issued before the state update of token t,
-// so the exponentials overlap the FMA chain instead of following it.  Same
-// operations as token_step, in the same order per token: bit-identical.
+// NT consecutive tokens for one thread, software-pipelined: while the state
+// update of token t runs, the 2^x of token t + 1 are issued two at a time
+// between its FMAs, so that the special-function unit and the FMA pipe work
+// side by side instead of in alternating bursts (the two pipes bound this
+// loop together: per element-state one 2^x and four fp32 operations).  The
+// B, C rows and (Delta, Delta u) of token t + 1 are loaded before token t's
+// update.  Same operations per token as token_step, in the same order:
+// bit-identical.
 // wrow: (Delta, Delta u) pairs, two tokens per float4; bcf: B (S floats) then
 // C (S floats) of this thread's states, BCT floats per token; yrow: NT
 // partial outputs (16-byte aligned).
@@ -241,10 +260,10 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
                                             float (&h)[S], const float (&A2)[S], float* __restrict__ yrow) {
     static_assert(S % 4 == 0 && NT % 4 == 0, "scan_tokens takes S and NT multiples of 4");
     static_assert(!RAW || S == 4 || S == 8, "raw B/C rows take 4 or 8 states");
-    float a_n[S], B_n[S], C_n[S];
+    float a[S], B_n[S], C_n[S];
     float dt_n, dtx_n;
     float4 wq = wrow[0];
-    auto fetch = [&](int t) {   // inputs and exponentials of token t
+    auto load = [&](int t) {   // inputs of token t
         if (t % 2 == 0) {
             wq = wrow[t / 2];
             dt_n = wq.x;
@@ -283,24 +302,27 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
                 C_n[n] = c4.x; C_n[n + 1] = c4.y; C_n[n + 2] = c4.z; C_n[n + 3] = c4.w;
             }
         }
+    };
+    load(0);
+    {
         const float2 dt2 = make_float2(dt_n, dt_n);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
             const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
-            a_n[n] = ex2(e.x);
-            a_n[n + 1] = ex2(e.y);
+            a[n] = ex2(e.x);
+            a[n + 1] = ex2(e.y);
         }
-    };
-    fetch(0);
+    }
     float4 out;
 #pragma unroll
     for (int t = 0; t < NT; t++) {
-        float a[S], Bv[S], Cv[S];
+        float Bv[S], Cv[S];
 #pragma unroll
-        for (int n = 0; n < S; n++) { a[n] = a_n[n]; Bv[n] = B_n[n]; Cv[n] = C_n[n]; }
+        for (int n = 0; n < S; n++) { Bv[n] = B_n[n]; Cv[n] = C_n[n]; }
         const float dtx = dtx_n;
-        if (t + 1 < NT) fetch(t + 1);
+        if (t + 1 < NT) load(t + 1);
         const float2 dtx2 = make_float2(dtx, dtx);
+        const float2 dtn2 = make_float2(dt_n, dt_n);
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
@@ -309,6 +331,11 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
             h[n] = hn.x;
             h[n + 1] = hn.y;
             acc = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc);
+            if (t + 1 < NT) {   // token t + 1's decays for these two states
+                const float2 e = __fmul2_rn(dtn2, make_float2(A2[n], A2[n + 1]));
+                a[n] = ex2(e.x);
+                a[n + 1] = ex2(e.y);
+            }
         }
         const float yv = acc.x + acc.y;
         if (t % 4 == 0) out.x = yv;
@@ -329,19 +356,18 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
                                                    const float* __restrict__ bcf, float (&h)[S],
                                                    const float (&A2)[S]) {
     static_assert(S % 4 == 0 && NT % 2 == 0, "scan_tokens_state takes S % 4 == 0, even NT");
-    float a_n[S], B_n[S];
-    float dtx_n;
+    float a[S], B_n[S];
+    float dt_n, dtx_n;
     float4 wq = wrow[0];
     float tsum = 0.0f;
-    auto fetch = [&](int t) {
-        float dt;
+    auto load = [&](int t) {
         if (t % 2 == 0) {
             wq = wrow[t / 2];
-            dt = wq.x;
+            dt_n = wq.x;
             dtx_n = wq.y;
             tsum += wq.x + wq.z;
         } else {
-            dt = wq.z;
+            dt_n = wq.z;
             dtx_n = wq.w;
         }
         const float* bc = bcf + t * BCT;
@@ -350,29 +376,37 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
             const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
             B_n[n] = b4.x; B_n[n + 1] = b4.y; B_n[n + 2] = b4.z; B_n[n + 3] = b4.w;
         }
-        const float2 dt2 = make_float2(dt, dt);
+    };
+    load(0);
+    {
+        const float2 dt2 = make_float2(dt_n, dt_n);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
             const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
-            a_n[n] = ex2(e.x);
-            a_n[n + 1] = ex2(e.y);
+            a[n] = ex2(e.x);
+            a[n + 1] = ex2(e.y);
         }
-    };
-    fetch(0);
+    }
 #pragma unroll
     for (int t = 0; t < NT; t++) {
-        float a[S], Bv[S];
+        float Bv[S];
 #pragma unroll
-        for (int n = 0; n < S; n++) { a[n] = a_n[n]; Bv[n] = B_n[n]; }
+        for (int n = 0; n < S; n++) Bv[n] = B_n[n];
         const float dtx = dtx_n;
-        if (t + 1 < NT) fetch(t + 1);
+        if (t + 1 < NT) load(t + 1);
         const float2 dtx2 = make_float2(dtx, dtx);
+        const float2 dtn2 = make_float2(dt_n, dt_n);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
             const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
             const float2 hn = __ffma2_rn(make_float2(a[n], a[n + 1]), make_float2(h[n], h[n + 1]), bb);
             h[n] = hn.x;
             h[n + 1] = hn.y;
+            if (t + 1 < NT) {
+                const float2 e = __fmul2_rn(dtn2, make_float2(A2[n], A2[n + 1]));
+                a[n] = ex2(e.x);
+                a[n + 1] = ex2(e.y);
+            }
         }
     }
     return tsum;
@@ -416,12 +450,27 @@ __device__ __forceinline__ float token_step(float dt, float dtx, const float* __
     }
 }
 
-// softplus(v) from x = v log2(e): ln2 * log2(1 + 2^x), or v itself once
-// v > 20 (the correction e^-v is then below half an fp32 ulp of v).
-__device__ __forceinline__ float softplus_log2(float x) {
+// softplus_log2 on a pair, for the whole warp (every lane must call it).
+// log2(1 + 2^x) comes from the special-function unit's log2 of 1 + 2^x,
+// except below x = XS, where the series of log2_1p_small2 replaces it: with
+// 2^x small, forming 1 + 2^x in fp32 and the log2 unit's absolute error
+// (~2^-22) would leave a relative error of about 2^-22 / 2^x in Delta.
+// XS = -5 keeps that below 1e-5 (fp32 I/O); XS = -10 below 3e-4, far inside
+// the bf16 tolerance, and the series is then rarely needed.  It is evaluated
+// only when some lane of the warp needs it (a warp vote), so typical step
+// sizes never pay for it.
+template <int XS>
+__device__ __forceinline__ float2 softplus2_log2(float2 x) {
     constexpr float kX20 = 20.0f * kLog2e;
-    const float s = lg2(1.0f + ex2(x));
-    return kLn2 * (x > kX20 ? x : s);
+    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+    const float2 p = __fadd2_rn(make_float2(1.0f, 1.0f), e);
+    float2 s = make_float2(x.x > kX20 ? x.x : lg2(p.x), x.y > kX20 ? x.y : lg2(p.y));
+    if (__any_sync(0xffffffffu, fminf(x.x, x.y) < (float)XS)) {
+        const float2 q = log2_1p_small2(e);
+        if (x.x < (float)XS) s.x = q.x;
+        if (x.y < (float)XS) s.y = q.y;
+    }
+    return __fmul2_rn(make_float2(kLn2, kLn2), s);
 }
 
 // Bounded wait for the carry of `group` (set by the CTA that scanned the
@@ -574,21 +623,33 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             float uv[8], dv[8];
             unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
             unpack8<T>(buf + Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, dv);
-            float dt[8];
+            // pairs of tokens in packed fp32 arithmetic (same roundings as
+            // the scalar form: fused multiply-add, add, multiply)
+            float2 dt[4];
+            const float2 bias2 = make_float2(bias_r[it], bias_r[it]);
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                if constexpr (SOFTPLUS) dt[e] = softplus_log2(fmaf(dv[e], kLog2e, bias_r[it]));
-                else dt[e] = dv[e] + bias_r[it];
+            for (int e = 0; e < 8; e += 2) {
+                const float2 d2 = make_float2(dv[e], dv[e + 1]);
+                if constexpr (SOFTPLUS) {
+                    constexpr int XS = std::is_same<T, float>::value ? -5 : -10;
+                    dt[e / 2] = softplus2_log2<XS>(__ffma2_rn(d2, make_float2(kLog2e, kLog2e), bias2));
+                } else {
+                    dt[e / 2] = __fadd2_rn(d2, bias2);
+                }
             }
             if (tvalid < kTL) {   // tokens past the end leave the state untouched
 #pragma unroll
-                for (int e = 0; e < 8; e++)
-                    if (q * 8 + e >= tvalid) dt[e] = 0.0f;
+                for (int e = 0; e < 8; e += 2) {
+                    if (q * 8 + e >= tvalid) dt[e / 2].x = 0.0f;
+                    if (q * 8 + e + 1 >= tvalid) dt[e / 2].y = 0.0f;
+                }
             }
             float4* w = reinterpret_cast<float4*>(smem + Sh::OFF_W + r * Sh::W_ROW + q * 64);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2)
-                w[e / 2] = make_float4(dt[e], dt[e] * uv[e], dt[e + 1], dt[e + 1] * uv[e + 1]);
+            for (int e = 0; e < 8; e += 2) {
+                const float2 du = __fmul2_rn(dt[e / 2], make_float2(uv[e], uv[e + 1]));
+                w[e / 2] = make_float4(dt[e / 2].x, du.x, dt[e / 2].y, du.y);
+            }
         }
         if constexpr (!RAW_BC) {
             const unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
@@ -673,26 +734,35 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         for (int it = 0; it < (AGG ? 0 : Sh::CHUNK_ITERS); it++) {
             int r, q;
             chunk_of<CH>(it, r, q);
-            float ys[8];
+            // pairs of tokens in packed fp32 arithmetic, the partial sums
+            // added in group order
+            float2 y2[4];
 #pragma unroll
             for (int gg = 0; gg < G; gg++) {
                 const float4* yp = reinterpret_cast<const float4*>(
                     smem + Sh::OFF_Y + (gg * CH + r) * Sh::Y_ROW + q * 32);
                 const float4 a = yp[0], c = yp[1];
-                const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+                const float2 v[4] = {make_float2(a.x, a.y), make_float2(a.z, a.w),
+                                     make_float2(c.x, c.y), make_float2(c.z, c.w)};
 #pragma unroll
-                for (int e = 0; e < 8; e++) ys[e] = gg == 0 ? v[e] : ys[e] + v[e];
+                for (int e = 0; e < 4; e++) y2[e] = gg == 0 ? v[e] : __fadd2_rn(y2[e], v[e]);
             }
             float uv[8];
             unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            const float2 D2 = make_float2(D_r[it], D_r[it]);
 #pragma unroll
-            for (int e = 0; e < 8; e++) ys[e] = fmaf(D_r[it], uv[e], ys[e]);
+            for (int e = 0; e < 4; e++)
+                y2[e] = __ffma2_rn(D2, make_float2(uv[2 * e], uv[2 * e + 1]), y2[e]);
             if constexpr (HAS_Z) {
                 float zv[8];
                 unpack8<T>(buf + 2 * Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, zv);
 #pragma unroll
-                for (int e = 0; e < 8; e++) ys[e] *= gate<T>(zv[e]);
+                for (int e = 0; e < 4; e++)
+                    y2[e] = __fmul2_rn(y2[e], gate2<T>(make_float2(zv[2 * e], zv[2 * e + 1])));
             }
+            float ys[8];
+#pragma unroll
+            for (int e = 0; e < 4; e++) { ys[2 * e] = y2[e].x; ys[2 * e + 1] = y2[e].y; }
             if (r < rows && q * 8 < tvalid) {
                 T* dst = gy + (row0 + r) * L + t0 + q * 8;
                 if (VEC && q * 8 + 8 <= tvalid) {

@@ -2,7 +2,10 @@
 oracle (itself pinned by finite differences) on the same seeded inputs.
 
 Tolerance: every gradient is compared in fp64 against the oracle with
-|got - ref| <= 1e-3 * max|ref| + 1e-6.  The kernel works in fp32 with the
+|got - ref| <= 1e-3 * max|ref| + 1e-6 over the tensor, and element by
+element with |got - ref| <= 2e-3 * |ref| + 1e-4 * max|ref| + 1e-6, so that
+the small entries of a tensor (a quiet channel, a token with a small
+adjoint) are held to their own size and not only to the largest entry.  The kernel works in fp32 with the
 hardware 2^x (relative error ~2^-22); a gradient entry is a sum of up to
 L (or batch * L, for dA, dD, ddelta_bias, or dim, for dB, dC) terms, so
 its rounding error grows like sqrt(terms) * 2^-23 of the largest term:
@@ -48,9 +51,16 @@ def check(got, ref, what):
         gt = gt.double().cpu().numpy()
         assert gt.shape == r.shape, (what, name, gt.shape, r.shape)
         assert np.all(np.isfinite(gt)), (what, name, "non-finite")
-        err = np.abs(gt - r).max()
-        bound = 1e-3 * np.abs(r).max() + 1e-6
-        assert err <= bound, f"{what} {name}: max err {err:.3e} > {bound:.3e}"
+        err = np.abs(gt - r)
+        scale = np.abs(r).max()
+        bound = 1e-3 * scale + 1e-6
+        assert err.max() <= bound, f"{what} {name}: max err {err.max():.3e} > {bound:.3e}"
+        elem = 2e-3 * np.abs(r) + 1e-4 * scale + 1e-6
+        ratio = err / elem
+        worst = np.unravel_index(np.argmax(ratio), ratio.shape)
+        assert ratio.max() <= 1.0, (f"{what} {name}: {(ratio > 1).sum()} entries outside the "
+                                    f"elementwise bound; worst at {worst}: got {gt[worst]:.6g} "
+                                    f"ref {r[worst]:.6g}")
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])

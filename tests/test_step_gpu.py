@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import selective_state_space_116_b300 as ssm
-from parity import as64, assert_close, gpu_scan, oracle_scan, to_cuda
+from parity import TOL, as64, assert_close, gpu_scan, oracle_scan, to_cuda
 from selective_state_space_116_b300.workloads import (WORKLOADS, make_step_inputs,
                                                       steps_as_scan)
 
@@ -107,3 +107,79 @@ def test_generation_workload_full_size():
     y_ref, state_ref = oracle_steps(inp, 8)
     assert_close(as64(y), y_ref, torch.bfloat16, "gen y")
     assert_close(as64(state), state_ref, torch.bfloat16, "gen state")
+
+
+def _close_on_gpu(got, ref, io_dtype, what):
+    """assert_close's bound, evaluated on the GPU (the full generation run has
+    671 M outputs per comparison)."""
+    got, ref = got.double(), ref.double()
+    ratio = (got - ref).abs() / (TOL[io_dtype] * (1.0 + ref.abs()))
+    assert torch.isfinite(got).all(), f"{what}: non-finite output"
+    worst = ratio.max().item()
+    assert worst <= 1.0, f"{what}: worst scaled error {worst:.3f} of the bound"
+
+
+def _prefix(s, k):
+    pre = dict(s)
+    for key in ("u", "delta", "z"):
+        pre[key] = None if s[key] is None else s[key][..., :k].contiguous()
+    for key in ("B", "C"):
+        pre[key] = s[key][:, :k].contiguous()
+    return pre
+
+
+def test_generation_1024_steps_full_size():
+    """The generation workload as configured: 128 x 5120 channels, N = 16,
+    bf16 inputs, fp32 state, 1024 consecutive ssm_state_step tokens from a
+    zero state.  Every step's y against the GPU scan of the same token stream;
+    the state after k = 1, 2, 17, 1024 steps against the last_state of the
+    GPU scan of the first k tokens; and both against the fp64 oracle on 64
+    sampled channels (d = 0 and d = D - 1 of every batch row among them).
+    The oracle side runs the oracle's scan over the stream, which its own
+    pins tie to its single-token step."""
+    w = WORKLOADS["gen"]
+    steps = 1024
+    K = (1, 2, 17, steps)
+    inp = make_step_inputs(w, seed=0, steps=steps)
+    g = to_cuda(inp)
+    batch, dim, N = w.batch, w.dim, w.dstate
+    state = torch.zeros(batch, dim, N, device="cuda")
+    ys = torch.empty(steps, batch, dim, dtype=g["x"].dtype, device="cuda")
+    states = {}
+    for t in range(steps):
+        ssm.ssm_state_step(state, g["x"][t], g["delta"][t], g["A"], g["B"][t], g["C"][t],
+                           D=g["D"], z=g["z"][t], delta_bias=g["delta_bias"],
+                           delta_softplus=g["delta_softplus"], y=ys[t])
+        if t + 1 in K:
+            states[t + 1] = state.clone()
+    torch.cuda.synchronize()
+    s = steps_as_scan(inp)
+    sg = to_cuda(s)
+    y_scan, h_scan = ssm.ssm_scan_fwd(sg["u"], sg["delta"], sg["A"], sg["B"], sg["C"], D=sg["D"],
+                                      z=sg["z"], delta_bias=sg["delta_bias"],
+                                      delta_softplus=sg["delta_softplus"])
+    _close_on_gpu(ys.permute(1, 2, 0), y_scan, torch.bfloat16, "every step's y vs scan y")
+    for k in K:
+        if k == steps:
+            hk = h_scan
+        else:
+            p = _prefix(sg, k)
+            _, hk = ssm.ssm_scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], D=p["D"],
+                                     z=p["z"], delta_bias=p["delta_bias"],
+                                     delta_softplus=p["delta_softplus"])
+        _close_on_gpu(states[k], hk, torch.bfloat16, f"state after {k} steps vs scan")
+    # 64 channels: d = 0 and d = D - 1 of the first and last batch rows, the
+    # rest drawn at random
+    rng = np.random.default_rng(5)
+    must = {0, dim - 1, (batch - 1) * dim, batch * dim - 1}
+    rest = [int(c) for c in rng.choice(batch * dim, 80, replace=False) if int(c) not in must]
+    chans = np.array(sorted(must | set(rest[:64 - len(must)])), dtype=np.int64)
+    assert len(chans) == 64
+    idx = torch.from_numpy(chans).cuda()
+    y_ref, h_ref = oracle_scan(s, channels=chans)
+    y_got = ys.permute(1, 2, 0).reshape(batch * dim, steps)[idx]
+    assert_close(as64(y_got), y_ref, torch.bfloat16, "step y vs oracle (64 channels)")
+    for k in K:
+        _, hk_ref = (y_ref, h_ref) if k == steps else oracle_scan(_prefix(s, k), channels=chans)
+        hk = states[k].reshape(batch * dim, N)[idx]
+        assert_close(as64(hk), hk_ref, torch.bfloat16, f"state after {k} steps vs oracle")

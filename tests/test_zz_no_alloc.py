@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 
 # 3 x 130 channels, N = 16, 1000 tokens; with chunk = 1.3 L the tokens of some
 # channel groups are split between two CTAs, so the state is handed over
-# through the scratch buffer.
+# through the scratch buffer; with chunk = 0.3 L the chunked schedule keeps
+# its chunk aggregates and carries there instead.
 W = Workload("noalloc", 3, 130, 16, 1000, "bf16", bias_range=(-4.0, -2.0),
              a_kind="neg_exp_uniform", gate=True)
 
@@ -44,7 +45,7 @@ def _noalloc(g, w, chunk, y, last):
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-@pytest.mark.parametrize("frac", [0.0, 1.3])
+@pytest.mark.parametrize("frac", [0.0, 1.3, 0.3])
 def test_noalloc_matches_workspace_entry(io, frac):
     w = W.scaled(io=io)
     g = to_cuda(make_scan_inputs(w, seed=5))
