@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_state_step.restype = i32
         lib.oracle_state_step.argtypes = [i64, i64, i64, i32, i32,
                                           dp, vp, vp, vp, vp, vp, vp, vp, vp, i32, dp]
+        lib.oracle_conv_silu.restype = i32
+        lib.oracle_conv_silu.argtypes = [i64, i64, i64, i64, i32, i32, vp, vp, vp, vp, dp]
         lib.oracle_scan_bwd.restype = i32
         lib.oracle_scan_bwd.argtypes = [i64, i64, i64, i64, i32, i32,
                                         vp, vp, vp, vp, vp, vp, vp, vp, i32,
@@ -145,6 +147,32 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     if channels is None:
         return y.reshape(batch, dim, L), last.reshape(batch, dim, N)
     return y, last
+
+
+def conv_silu(x, w, conv_bias=None, conv_state=None, lib: ctypes.CDLL | None = None):
+    """Oracle short convolution: u = silu(causal depthwise conv(x) + bias).
+
+    x (batch, dim, L) and conv_state (batch, dim, K-1; the inputs before
+    token 0, oldest first, or None for zeros) share one element type; w
+    (dim, K) and conv_bias (dim,) are fp32 or fp64.  Returns u (batch, dim,
+    L) fp64."""
+    lib = lib or load()
+    batch, dim, L = (int(s) for s in x.shape)
+    K = int(w.shape[1])
+    xa, xt = _host(x)
+    sa, st = _host(conv_state)
+    if st is not None and st != xt:
+        raise TypeError("x and conv_state must share one element type")
+    wa, wt = _host(w)
+    ba, bt = _host(conv_bias)
+    if wt not in (F32, F64) or (bt is not None and bt != wt):
+        raise TypeError("w and conv_bias must share one element type, fp32 or fp64")
+    u = np.empty((batch, dim, L), dtype=np.float64)
+    rc = lib.oracle_conv_silu(batch, dim, L, K, xt, wt, _ptr(xa), _ptr(wa), _ptr(ba), _ptr(sa),
+                              _ptr(u))
+    if rc != 0:
+        raise ValueError("oracle_conv_silu rejected its arguments")
+    return u
 
 
 def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,

@@ -409,3 +409,46 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
     pthread_mutex_destroy(&j.mu);
     return 0;
 }
+
+/*
+ * The block's short convolution, which produces the scan's input u from the
+ * block input x ("Mamba", elemedex entry, section "How it works": the block
+ * is a linear projection, a short convolution, the selective SSM and a
+ * multiplicative gate; "Simplifications and limits" of the sghael.github.io
+ * Mamba page: a short convolution).  The pages give no more detail; the
+ * reading taken (the usual Mamba layer) is a causal depthwise convolution of
+ * width K (each channel filtered by its own K taps, output t seeing inputs
+ * t-K+1 .. t), a per-channel bias, and the SiLU activation:
+ *
+ *   u[b,d,t] = silu( sum_{k=0}^{K-1} w[d,k] * x[b,d,t-(K-1)+k] + cbias[d] )
+ *
+ * Inputs before token 0 are the K-1 values of `state` (batch, dim, K-1),
+ * oldest first, or zero when state is NULL.  x and state have the element
+ * type io (fp32, bf16 bits or fp64); w (dim, K) and cbias (dim) have type
+ * pio.  u is fp64 (batch, dim, L).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_conv_silu(int64_t batch, int64_t dim, int64_t seqlen, int64_t K, int io, int pio,
+                     const void* x, const void* w, const void* cbias, const void* state,
+                     double* u) {
+    if (batch <= 0 || dim <= 0 || seqlen < 0 || K < 1 || !x || !w || !u) return -1;
+    if (io < OR_F32 || io > OR_F64 || (pio != OR_F32 && pio != OR_F64)) return -1;
+    for (int64_t b = 0; b < batch; b++) {
+        for (int64_t d = 0; d < dim; d++) {
+            const int64_t c = b * dim + d;
+            for (int64_t t = 0; t < seqlen; t++) {
+                double acc = cbias ? load(pio, cbias, d) : 0.0;
+                for (int64_t k = 0; k < K; k++) {
+                    const int64_t src = t - (K - 1) + k;   /* the input this tap sees */
+                    double xv = 0.0;
+                    if (src >= 0)
+                        xv = load(io, x, c * seqlen + src);
+                    else if (state)
+                        xv = load(io, state, c * (K - 1) + (K - 1) + src);
+                    acc += load(pio, w, d * K + k) * xv;
+                }
+                u[c * seqlen + t] = silu(acc);
+            }
+        }
+    }
+    return 0;
+}

@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from oracle import brute
+from scipy.special import expit
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -383,7 +384,39 @@ def pin_initial_state(lib):
         close(lt, lf, 1e-12, 1e-13, what=f"split at {k} and resumed, last_state (zoh={zoh})")
 
 
+# -- pin 12: the block's short convolution (causal, depthwise, SiLU) ----------------
+def pin_conv_silu(lib):
+    rng = np.random.default_rng(14)
+    batch, dim, L = 2, 5, 70
+    x = rng.standard_normal((batch, dim, L))
+    for K in (1, 2, 3, 4):
+        w = rng.standard_normal((dim, K))
+        cb = rng.standard_normal(dim)
+        u = oracle.conv_silu(x, w, conv_bias=cb, lib=lib)
+        # against numpy.convolve: output t sees inputs t-K+1 .. t, zeros before 0
+        for b in range(batch):
+            for d in range(dim):
+                pre = np.convolve(x[b, d], w[d, ::-1])[:L] + cb[d]
+                close(u[b, d], pre * expit(pre), 1e-13, 1e-14, what=f"conv K={K} ({b},{d})")
+        # the impulse response of channel d is its taps, newest tap first, then zeros
+        imp = np.zeros((1, dim, L))
+        imp[0, :, 10] = 1.0
+        ui = oracle.conv_silu(imp, w, lib=lib)
+        for d in range(dim):
+            pre = np.zeros(L)
+            pre[10:10 + K] = w[d, ::-1]
+            close(ui[0, d], pre * expit(pre), 1e-14, 1e-15, what=f"impulse response K={K}")
+        # a given history continues the sequence: state = the last K-1 inputs
+        if K > 1:
+            k = 23
+            head_state = x[..., k - (K - 1):k].copy()
+            ut = oracle.conv_silu(x[..., k:].copy(), w, conv_bias=cb, conv_state=head_state,
+                                  lib=lib)
+            close(ut, u[..., k:], 1e-14, 1e-15, what=f"conv state continues K={K}")
+
+
 ALL_PINS = [pin_gate_fixed, pin_gate_selective, pin_affine_compose, pin_page_scalar_zoh,
             pin_closed_form, pin_convolution, pin_brute_force, pin_special_cases,
             pin_step_equals_scan, pin_decode_and_subset, pin_zoh_page_loop,
-            pin_zoh_closed_form, pin_zoh_limits, pin_zoh_brute_force, pin_initial_state]
+            pin_zoh_closed_form, pin_zoh_limits, pin_zoh_brute_force, pin_initial_state,
+            pin_conv_silu]

@@ -17,6 +17,11 @@ MUTANTS = [
     ("zoh_limit_at_zero", "expm1(dt * a) / a : dt;", "expm1(dt * a) / a : 0.0;"),
     ("zoh_ignored", "return a != 0.0 ? expm1(dt * a) / a : dt;", "return dt;"),
     ("h0_ignored", "h[n] = j->h0 ? j->h0[k * N + n] : 0.0;", "h[n] = 0.0;"),
+    ("conv_taps_reversed", "acc += load(pio, w, d * K + k) * xv;", "acc += load(pio, w, d * K + (K - 1 - k)) * xv;"),
+    ("conv_off_by_one", "const int64_t src = t - (K - 1) + k;", "const int64_t src = t - K + k;"),
+    ("conv_bias_ignored", "double acc = cbias ? load(pio, cbias, d) : 0.0;", "double acc = 0.0;"),
+    ("conv_no_silu", "u[c * seqlen + t] = silu(acc);", "u[c * seqlen + t] = acc;"),
+    ("conv_state_ignored", "else if (state)", "else if (0)"),
     ("wrong_sign_in_decay", "exp(dt * a) * h[n]", "exp(-dt * a) * h[n]"),
     ("drop_skip_term", "yv += Dskip * x;", "(void)Dskip;"),
     ("gate_sigmoid_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
