@@ -34,12 +34,23 @@
  * nearest even once, at the store.
  *
  * Ownership and execution: the caller owns every buffer.  Every pointer is
- * a device pointer (or a host-mapped pointer the device can read).  The
- * library never allocates, frees or synchronises: each call validates its
- * arguments on the host, enqueues work on the caller's stream and returns.
- * Outputs must not alias inputs (state, the only in/out buffer, excepted).
- * The library keeps no global state and prints nothing; calls on different
- * streams with disjoint outputs may run concurrently.
+ * a device pointer (or a host-mapped pointer the device can read), except
+ * for ssm_scan_fwd_host, which takes host buffers.  Each call validates its
+ * arguments on the host, enqueues work on the caller's stream and returns;
+ * none synchronises the device.  Outputs must not alias inputs (state, the
+ * only in/out buffer, excepted).  The library prints nothing.
+ * Allocation and state kept by the library:
+ *   - ssm_scan_fwd, ssm_scan_fwd_ex, ssm_scan_bwd, ssm_state_step and
+ *     ssm_scan_fwd_noalloc allocate nothing; their scratch is the caller's
+ *     workspace (ssm_scan_fwd_noalloc: a fixed buffer inside the library).
+ *   - ssm_scan_fwd_host allocates its device staging buffers on the caller's
+ *     stream (cudaMallocAsync, returned with cudaFreeAsync) and keeps two
+ *     CUDA streams per device, created at its first call and held until exit.
+ *   - Per device, the library caches the SM count and the occupancy of each
+ *     kernel instance it has launched (read-only facts of the device), and
+ *     ssm_scan_fwd_noalloc keeps its buffer's device address.
+ * Calls on different streams with disjoint outputs and workspaces may run
+ * concurrently.
  *
  * Errors: 0 on success, else a negative ssm_status.  Argument errors are
  * detected on the host before anything is enqueued.  A launch error is
@@ -74,7 +85,8 @@ typedef enum ssm_status {
     SSM_ERR_WORKSPACE = -7,     /* workspace missing, too small or misaligned */
     SSM_ERR_ALIAS = -8,         /* an output overlaps an input */
     SSM_ERR_TIMEOUT = -9,       /* a bounded on-device wait gave up */
-    SSM_ERR_TOO_LARGE = -10     /* needs more scratch than ssm_scan_fwd_noalloc holds */
+    SSM_ERR_TOO_LARGE = -10,    /* needs more scratch than ssm_scan_fwd_noalloc holds */
+    SSM_ERR_BAD_OPTION = -11    /* a field of ssm_scan_opts is out of range */
 } ssm_status;
 
 typedef enum ssm_io_dtype { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
@@ -136,6 +148,61 @@ typedef struct ssm_dims {
  * Returns SSM_OK or a negative ssm_status.
  */
 SSM_API int ssm_scan_fwd(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 void* y, float* last_state,
+                 void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* The input term Bbar u of the state update. */
+typedef enum ssm_input_term {
+    /* Bbar u = Delta B u: the first-order form (the default). */
+    SSM_INPUT_DELTA_B = 0,
+    /* Bbar u = (exp(Delta A) - 1) / A * B u: the exact zero-order hold of a
+     * diagonal A, Delta B u in the limit A = 0.  With A = -1 and B = 1 this is
+     * the scalar update h_t = exp(-Delta_t) h_{t-1} + (1 - exp(-Delta_t)) x_t
+     * of "Mamba remembers by forgetting, read closely" (interactiveml.org,
+     * its recurrence and its selective_scan listing). */
+    SSM_INPUT_ZOH = 1
+} ssm_input_term;
+
+/* Options of ssm_scan_fwd_ex.  A zero-initialised struct (or a NULL pointer)
+ * gives exactly ssm_scan_fwd. */
+typedef struct ssm_scan_opts {
+    int32_t input_term;        /* ssm_input_term */
+    /* The block's short convolution fused into the scan ("Mamba", elemedex
+     * entry, "How it works": the block is a linear projection, a short
+     * convolution, the selective SSM and a multiplicative gate; sghael.github.io
+     * Mamba page, "Simplifications and limits").  0: off, u is the scan input.
+     * 1..4: u is the convolution's input x and the scan runs on
+     *   u'[b,d,t] = silu(sum_{k<K} conv_weight[d,k] x[b,d,t-K+1+k] + conv_bias[d])
+     * (causal, depthwise, width K = conv_width), computed in the scan's
+     * prologue in fp32; u' takes u's place everywhere, the D u skip term
+     * included, and never goes through memory unless u_out asks for it. */
+    int32_t conv_width;
+    /* (batch, dim, dstate) fp32 state before token 0, or NULL for zero.  It
+     * may be the same buffer as last_state (the state is then continued in
+     * place), but may overlap no other output. */
+    const float* h0;
+    const float* conv_weight;  /* (dim, conv_width) fp32 taps, oldest input first; required with conv */
+    const float* conv_bias;    /* (dim) fp32, or NULL for none */
+    /* (batch, dim, conv_width - 1) I/O type: the inputs x before token 0,
+     * oldest first, or NULL for zeros. */
+    const void* conv_state;
+    /* (batch, dim, seqlen) I/O type output: the convolution's output u'
+     * (rounded to the I/O type), or NULL to skip writing it. */
+    void* u_out;
+} ssm_scan_opts;
+
+/*
+ * ssm_scan_fwd with options: the exact zero-order-hold input term, an initial
+ * state, and the fused short convolution (see ssm_scan_opts).  Every other
+ * argument, the workspace (ssm_scan_fwd_workspace_size gives its size for
+ * these dims whatever the options) and the errors are those of ssm_scan_fwd;
+ * an option out of range returns SSM_ERR_BAD_OPTION.
+ */
+SSM_API int ssm_scan_fwd_ex(const ssm_dims* dims, const ssm_scan_opts* opts,
                  const void* u, const void* delta, const float* A,
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus,

@@ -118,15 +118,28 @@ def _scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_l
 
 
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
-                 return_last_state=True, y=None, last_state=None, workspace=None, chunk=0):
+                 return_last_state=True, y=None, last_state=None, workspace=None, chunk=0,
+                 input_term="delta_b", h0=None, conv_weight=None, conv_bias=None,
+                 conv_state=None, u_out=None):
     """Forward selective scan.
 
     u, delta, z: (batch, dim, L); B, C: (batch, L, N), all fp32 or all bf16.
     A: (dim, N) fp32; D, delta_bias: (dim,) fp32 or None.
     Returns (y, last_state); last_state is None unless return_last_state.
     ``y``/``last_state``/``workspace`` may be passed preallocated.
+
+    Options (CUDA tensors; they route the call to ssm_scan_fwd_ex):
+    ``input_term``: "delta_b" (Delta B u) or "zoh" ((exp(Delta A) - 1)/A B u);
+    ``h0``: (batch, dim, N) fp32 initial state (may be ``last_state`` itself);
+    ``conv_weight``: (dim, K) fp32, K <= 4 -- then ``u`` is the input x of the
+    fused short convolution u' = silu(conv(x) + conv_bias) and the scan runs
+    on u'; ``conv_bias``: (dim,) fp32; ``conv_state``: (batch, dim, K - 1)
+    inputs before token 0; ``u_out``: (batch, dim, L) tensor to receive u'.
     """
+    opts = input_term != "delta_b" or h0 is not None or conv_weight is not None
     if u.device.type == "cpu":
+        if opts:
+            raise ValueError("scan options take CUDA tensors")
         return _scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus,
                               return_last_state, y, last_state, chunk)
 
@@ -164,12 +177,36 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     if need.value and workspace is None:
         workspace = torch.empty(int(need.value), dtype=torch.uint8, device=device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.ssm_scan_fwd(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                          _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
-                          _ptr(y), _ptr(last_state), _ptr(workspace), ws_bytes,
-                          _stream(device))
+    args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(delta_softplus)), _ptr(y), _ptr(last_state), _ptr(workspace), ws_bytes,
+            _stream(device))
+    if not opts:
+        rc = lib.ssm_scan_fwd(ctypes.byref(d), *args)
+        if rc != 0:
+            raise SSMError(rc, "ssm_scan_fwd")
+        return y, (last_state if return_last_state else None)
+    if input_term not in ("delta_b", "zoh"):
+        raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
+    o = _lib.ssm_scan_opts()
+    o.input_term = _lib.SSM_INPUT_ZOH if input_term == "zoh" else _lib.SSM_INPUT_DELTA_B
+    _check(h0, "h0", (batch, dim, N), torch.float32, device, optional=True)
+    o.h0 = _ptr(h0)
+    if conv_weight is not None:
+        if conv_weight.dim() != 2:
+            raise ValueError("conv_weight must be (dim, K)")
+        K = conv_weight.shape[1]
+        _check(conv_weight, "conv_weight", (dim, K), torch.float32, device)
+        _check(conv_bias, "conv_bias", (dim,), torch.float32, device, optional=True)
+        _check(conv_state, "conv_state", (batch, dim, K - 1), io, device, optional=True)
+        _check(u_out, "u_out", (batch, dim, L), io, device, optional=True)
+        o.conv_width = K
+        o.conv_weight, o.conv_bias = _ptr(conv_weight), _ptr(conv_bias)
+        o.conv_state, o.u_out = _ptr(conv_state), _ptr(u_out)
+    elif conv_bias is not None or conv_state is not None or u_out is not None:
+        raise ValueError("conv_bias, conv_state and u_out need conv_weight")
+    rc = lib.ssm_scan_fwd_ex(ctypes.byref(d), ctypes.byref(o), *args)
     if rc != 0:
-        raise SSMError(rc, "ssm_scan_fwd")
+        raise SSMError(rc, "ssm_scan_fwd_ex")
     return y, (last_state if return_last_state else None)
 
 

@@ -23,13 +23,17 @@ SSM_ERR_WORKSPACE = -7
 SSM_ERR_ALIAS = -8
 SSM_ERR_TIMEOUT = -9
 SSM_ERR_TOO_LARGE = -10
+SSM_ERR_BAD_OPTION = -11
+
+SSM_INPUT_DELTA_B = 0
+SSM_INPUT_ZOH = 1
 
 SSM_IO_F32 = 0
 SSM_IO_BF16 = 1
 
 # every symbol include/ssm_scan.h declares
 EXPORTS = ("ssm_build_id", "ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
-           "ssm_scan_fwd_host", "ssm_scan_fwd_noalloc",
+           "ssm_scan_fwd_ex", "ssm_scan_fwd_host", "ssm_scan_fwd_noalloc",
            "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_workspace_size", "ssm_state_step",
            "ssm_status_string", "ssm_version")
 
@@ -38,6 +42,13 @@ class ssm_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64),
                 ("dstate", ctypes.c_int64), ("seqlen", ctypes.c_int64),
                 ("io", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+class ssm_scan_opts(ctypes.Structure):
+    _fields_ = [("input_term", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+                ("h0", ctypes.c_void_p), ("conv_weight", ctypes.c_void_p),
+                ("conv_bias", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+                ("u_out", ctypes.c_void_p)]
 
 
 class SSMError(RuntimeError):
@@ -63,6 +74,9 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     dims_p = ctypes.POINTER(ssm_dims)
     lib.ssm_scan_fwd.restype = i32
     lib.ssm_scan_fwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.ssm_scan_fwd_ex.restype = i32
+    lib.ssm_scan_fwd_ex.argtypes = [dims_p, ctypes.POINTER(ssm_scan_opts), vp, vp, vp, vp, vp, vp,
+                                    vp, vp, i32, vp, vp, vp, sz, vp]
     lib.ssm_scan_bwd.restype = i32
     lib.ssm_scan_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]

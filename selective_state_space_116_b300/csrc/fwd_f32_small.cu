@@ -3,14 +3,14 @@
 
 namespace ssm_host {
 
-int fwd_scan_f32_small(int n, const ssm::ScanParams& p, int64_t chunk, bool z, bool sp,
-                 bool vec, unsigned char* ws, int sms, cudaStream_t st) {
+int fwd_scan_f32_small(int n, const ssm::ScanParams& p, int64_t chunk, bool zoh,
+                 bool conv, bool vec, unsigned char* ws, int sms, cudaStream_t st) {
     using T = float;
     switch (n) {
-        case 1: return dispatch_scan_n<T, 1, 1>(p, chunk, z, sp, vec, ws, sms, st);
-        case 2: return dispatch_scan_n<T, 2, 2>(p, chunk, z, sp, vec, ws, sms, st);
-        case 4: return dispatch_scan_n<T, 4, 4>(p, chunk, z, sp, vec, ws, sms, st);
-        case 8: return dispatch_scan_n<T, 8, 8>(p, chunk, z, sp, vec, ws, sms, st);
+        case 1: return dispatch_scan_n<T, 1, 1>(p, chunk, zoh, conv, vec, ws, sms, st);
+        case 2: return dispatch_scan_n<T, 2, 2>(p, chunk, zoh, conv, vec, ws, sms, st);
+        case 4: return dispatch_scan_n<T, 4, 4>(p, chunk, zoh, conv, vec, ws, sms, st);
+        case 8: return dispatch_scan_n<T, 8, 8>(p, chunk, zoh, conv, vec, ws, sms, st);
     }
     return SSM_ERR_UNSUPPORTED_N;
 }

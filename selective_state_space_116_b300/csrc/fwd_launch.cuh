@@ -1,7 +1,10 @@
 // Launch templates of the forward scan: the state-split kernel under the
 // persistent balanced schedule and the three passes of the chunked schedule.
 // Included by the forward translation units, each of which instantiates one
-// group of (I/O type, N, states per thread) instances.
+// group of (I/O type, N, states per thread) instances, each in eight variants:
+// first-order or exact zero-order-hold input term, with or without the fused
+// convolution prologue, 16-byte or element-wise copies.  The gate and
+// softplus are per-call flags in the parameters.
 #pragma once
 
 #include "host_plan.h"
@@ -9,17 +12,15 @@
 namespace ssm_host {
 
 // Chunked schedule: the three passes on `stream`.
-template <typename T, int N, int S, bool Z, bool SP, bool VEC>
+template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC>
 int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int sms,
                    cudaStream_t stream) {
     using namespace ssm::seq;
-    using Sh = Shape<T, N, S, Z>;
-    using ShA = Shape<T, N, S, false>;
-    static_assert(Sh::CH == ShA::CH, "same channel groups in both passes");
-    auto agg = scan_chunk_agg_kernel<T, N, S, SP, VEC>;
-    auto full = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
+    using Sh = Shape<T, N, S, CONV>;
+    auto agg = scan_chunk_agg_kernel<T, N, S, ZOH, CONV, VEC>;
+    auto full = scan_fwd_kernel<T, N, S, ZOH, CONV, VEC>;
     static std::atomic<int> occ_agg[64], occ_full[64];
-    const int oa = occupancy(agg, ShA::SMEM, occ_agg), of = occupancy(full, Sh::SMEM, occ_full);
+    const int oa = occupancy(agg, Sh::SMEM, occ_agg), of = occupancy(full, Sh::SMEM, occ_full);
     if (oa < 1 || of < 1) return SSM_ERR_CUDA;
     p.groups_per_row = (p.dim + Sh::CH - 1) / Sh::CH;
     p.ngroups = p.batch * p.groups_per_row;
@@ -33,7 +34,7 @@ int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int
     const int64_t units = p.ngroups * p.nchunks;
     if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     const int64_t ga = units < (int64_t)oa * sms ? units : (int64_t)oa * sms;
-    agg<<<(unsigned)ga, kThreads, ShA::SMEM, stream>>>(p);
+    agg<<<(unsigned)ga, kThreads, Sh::SMEM, stream>>>(p);
     const int64_t nthr = p.ngroups * Sh::CH * N;
     scan_chunk_carry_kernel<N, Sh::CH><<<(unsigned)((nthr + 255) / 256), 256, 0, stream>>>(p);
     const int64_t gf = units < (int64_t)of * sms ? units : (int64_t)of * sms;
@@ -41,12 +42,12 @@ int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename T, int N, int S, bool Z, bool SP, bool VEC>
+template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false>
 int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
                 cudaStream_t stream) {
     using namespace ssm::seq;
-    using Sh = Shape<T, N, S, Z>;
-    auto kern = scan_fwd_kernel<T, N, S, Z, SP, VEC>;
+    using Sh = Shape<T, N, S, CONV>;
+    auto kern = scan_fwd_kernel<T, N, S, ZOH, CONV, VEC, GS>;
     // per kernel instance: raise its shared-memory limit and ask how many
     // CTAs fit on an SM, once
     static std::atomic<int> occ_cache[64];   // per device: the attribute is per context
@@ -90,35 +91,39 @@ int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
 }
 
 template <typename T, int N, int S>
-int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+int dispatch_scan_n(const ssm::ScanParams& p, int64_t chunk, bool zoh, bool conv, bool vec,
                     unsigned char* ws, int sms, cudaStream_t s) {
-#define SSM_SCAN_CASE(Z, SP, V) \
-    if (z == Z && sp == SP && vec == V) return launch_scan<T, N, S, Z, SP, V>(p, chunk, ws, sms, s);
-    SSM_SCAN_CASE(false, false, false)
+    // the common layer configuration (gate and softplus, 16-byte rows) has
+    // an instance of its own with both options fixed
+    if (!zoh && !conv && vec && p.gate && p.softplus)
+        return launch_scan<T, N, S, false, false, true, true>(p, chunk, ws, sms, s);
+#define SSM_SCAN_CASE(Z, C, V) \
+    if (zoh == Z && conv == C && vec == V) return launch_scan<T, N, S, Z, C, V>(p, chunk, ws, sms, s);
     SSM_SCAN_CASE(false, false, true)
-    SSM_SCAN_CASE(false, true, false)
-    SSM_SCAN_CASE(false, true, true)
-    SSM_SCAN_CASE(true, false, false)
+    SSM_SCAN_CASE(false, false, false)
     SSM_SCAN_CASE(true, false, true)
-    SSM_SCAN_CASE(true, true, false)
+    SSM_SCAN_CASE(true, false, false)
+    SSM_SCAN_CASE(false, true, true)
+    SSM_SCAN_CASE(false, true, false)
     SSM_SCAN_CASE(true, true, true)
+    SSM_SCAN_CASE(true, true, false)
 #undef SSM_SCAN_CASE
     return SSM_ERR_BAD_DIMS;
 }
 
 template <typename T, int N, int S>
-int dispatch_chunked_n(const ssm::ScanParams& p, const ChunkPlan& c, bool z, bool sp, bool vec,
+int dispatch_chunked_n(const ssm::ScanParams& p, const ChunkPlan& c, bool zoh, bool conv, bool vec,
                        unsigned char* ws, int sms, cudaStream_t s) {
-#define SSM_CHUNK_CASE(Z, SP, V) \
-    if (z == Z && sp == SP && vec == V) return launch_chunked<T, N, S, Z, SP, V>(p, c, ws, sms, s);
-    SSM_CHUNK_CASE(false, false, false)
+#define SSM_CHUNK_CASE(Z, C, V) \
+    if (zoh == Z && conv == C && vec == V) return launch_chunked<T, N, S, Z, C, V>(p, c, ws, sms, s);
     SSM_CHUNK_CASE(false, false, true)
-    SSM_CHUNK_CASE(false, true, false)
-    SSM_CHUNK_CASE(false, true, true)
-    SSM_CHUNK_CASE(true, false, false)
+    SSM_CHUNK_CASE(false, false, false)
     SSM_CHUNK_CASE(true, false, true)
-    SSM_CHUNK_CASE(true, true, false)
+    SSM_CHUNK_CASE(true, false, false)
+    SSM_CHUNK_CASE(false, true, true)
+    SSM_CHUNK_CASE(false, true, false)
     SSM_CHUNK_CASE(true, true, true)
+    SSM_CHUNK_CASE(true, true, false)
 #undef SSM_CHUNK_CASE
     return SSM_ERR_BAD_DIMS;
 }

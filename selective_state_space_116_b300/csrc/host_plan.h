@@ -206,19 +206,22 @@ inline int occupancy(K kern, int smem, std::atomic<int>* cache) {
 // Kernel launches, one translation unit per group of instances (they compile
 // in parallel).  Each returns SSM_OK or a negative ssm_status.
 
-// State-split scan, N in {1, 2, 4, 8} (S = N) or N = 16 with S in {4, 8}.
-int fwd_scan_f32_small(int n, const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+// State-split scan, N in {1, 2, 4, 8} (S = N) or N = 16 with S in {4, 8};
+// zoh: the exact zero-order-hold input term; conv: the fused convolution
+// prologue; vec: the 16-byte copy paths (gate and softplus travel in the
+// parameters).
+int fwd_scan_f32_small(int n, const ssm::ScanParams& p, int64_t chunk, bool zoh, bool conv, bool vec,
                        unsigned char* ws, int sms, cudaStream_t st);
-int fwd_scan_f32_n16(int s, const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+int fwd_scan_f32_n16(int s, const ssm::ScanParams& p, int64_t chunk, bool zoh, bool conv, bool vec,
                      unsigned char* ws, int sms, cudaStream_t st);
-int fwd_scan_bf16_small(int n, const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+int fwd_scan_bf16_small(int n, const ssm::ScanParams& p, int64_t chunk, bool zoh, bool conv, bool vec,
                         unsigned char* ws, int sms, cudaStream_t st);
-int fwd_scan_bf16_n16(int s, const ssm::ScanParams& p, int64_t chunk, bool z, bool sp, bool vec,
+int fwd_scan_bf16_n16(int s, const ssm::ScanParams& p, int64_t chunk, bool zoh, bool conv, bool vec,
                       unsigned char* ws, int sms, cudaStream_t st);
 // Chunked (L-parallel) schedule, any supported N.
-int fwd_chunked_f32(int n, const ssm::ScanParams& p, const ChunkPlan& c, bool z, bool sp, bool vec,
+int fwd_chunked_f32(int n, const ssm::ScanParams& p, const ChunkPlan& c, bool zoh, bool conv, bool vec,
                     unsigned char* ws, int sms, cudaStream_t st);
-int fwd_chunked_bf16(int n, const ssm::ScanParams& p, const ChunkPlan& c, bool z, bool sp, bool vec,
+int fwd_chunked_bf16(int n, const ssm::ScanParams& p, const ChunkPlan& c, bool zoh, bool conv, bool vec,
                      unsigned char* ws, int sms, cudaStream_t st);
 // Single-token state step.
 int step_f32(int n, const ssm::StepParams& p, bool z, bool sp, bool vec, cudaStream_t st);

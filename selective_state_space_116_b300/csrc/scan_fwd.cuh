@@ -1,15 +1,15 @@
 // Forward selective scan: state-split sequential kernel.
 //
-// The recurrence h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t u_t is diagonal,
-// so the N state entries of a channel are N independent scalar recurrences
-// that only meet in the output sum y_t = sum_n C_{t,n} h_{t,n}.  This kernel
+// The recurrence h_t = exp(Delta_t A) h_{t-1} + Bbar_t u_t is diagonal, so the
+// N state entries of a channel are N independent scalar recurrences that
+// only meet in the output sum y_t = sum_n C_{t,n} h_{t,n}.  This kernel
 // therefore walks each channel's sequence in order, exactly once, with its
 // state held in registers: S state entries per thread and G = N / S threads
 // per channel.  Per element-state that is the minimum work of the method (one
 // 2^x on the special-function unit, a multiply for Delta*A, a multiply for
-// Delta*u*B, one FMA for the state and one for the output); no second pass and
-// no scan of affine pairs is needed, and the B x D x L x N expanded state
-// never leaves the register file.
+// the input term, one FMA for the state and one for the output); no second
+// pass and no scan of affine pairs is needed, and the B x D x L x N expanded
+// state never leaves the register file.
 //
 // The G threads of a channel sit in different warps (the group index is
 // warp-uniform), so every warp reads the same B/C row of shared memory
@@ -18,13 +18,20 @@
 //
 // A CTA owns CH = 128 / G channels of one batch row and a contiguous range of
 // that row's tokens, walked in tiles of kTL tokens.  Per tile:
-//   load      u, delta, z rows and the B, C tile -> shared memory (16-byte
-//             cp.async, double-buffered, zero-filled past the edges)
-//   prologue  Delta = softplus(delta + bias), Delta*u  -> fp32 (Delta, Delta u)
-//             pairs; B, C -> fp32, grouped by thread group
+//   load      u (or x), delta, z rows and the B, C tile -> shared memory
+//             (16-byte cp.async, double-buffered, zero-filled past the edges)
+//   prologue  [CONV: u = silu(causal depthwise conv(x) + bias)]
+//             Delta = softplus(delta + bias), Delta*u  -> fp32 pairs; B, C ->
+//             fp32, grouped by thread group
 //   recur     every thread advances its S states over the tile's tokens and
 //             writes its partial output sums
 //   epilogue  y = (sum of partials + D u) * silu(z) -> global, 16-byte stores
+//
+// Compile-time variants: ZOH, the exact zero-order-hold input term
+// Bbar u = (exp(Delta A) - 1) / A * B u in place of Delta B u; CONV, the
+// block's short convolution fused into the prologue, so that u never goes
+// through memory; VEC, the 16-byte copy and store paths, for calls whose rows
+// all start on 16-byte boundaries.  The gate and softplus are per-call flags.
 #pragma once
 
 #include <type_traits>
@@ -34,7 +41,7 @@
 namespace ssm {
 
 struct ScanParams {
-    const void* u;
+    const void* u;        // the scan input u; CONV: the convolution's input x
     const void* delta;
     const float* A;
     const void* B;
@@ -45,6 +52,16 @@ struct ScanParams {
     void* y;
     float* last_state;    // may be null
     int64_t batch, dim, L;
+    // per-call options
+    int gate;             // z is given: y *= silu(z)
+    int softplus;         // Delta = softplus(delta + bias)
+    const float* h0;      // (batch, dim, N) initial state, or null for zero
+    // convolution prologue (CONV instances)
+    const float* conv_w;      // (dim, conv_k) taps, oldest input first
+    const float* conv_b;      // (dim), or null
+    const void* conv_state;   // (batch, dim, conv_k - 1) inputs before token 0, or null
+    void* u_out;              // (batch, dim, L): the convolution's output, or null
+    int conv_k;               // 1 .. 4
     // schedule (see scan_fwd_kernel)
     int64_t groups_per_row;   // ceil(dim / channels per CTA)
     int64_t ngroups;          // batch * groups_per_row
@@ -63,7 +80,8 @@ struct ScanParams {
 
 // How one part of a channel group starts and ends.
 struct PartIO {
-    int init;            // 0: zero state, 1: handed over (flag + carry), 2: from h0
+    int init;            // 0: zero state, 1: handed over (flag + carry),
+                         // 2: from h0 below, 3: from the caller's initial state
     const float* h0;     // [CH][N] initial state when init == 2
     float* hout;         // [CH][N] final state (chunk aggregate), or null
     float* dsum;         // [CH] sum of Delta over the part, or null
@@ -82,7 +100,7 @@ constexpr int kTL = 32;         // tokens per tile
 // Shared-memory layout.  Row paddings of 16 bytes make every access pattern
 // below free of bank conflicts (each quarter-warp touches 8 distinct 16-byte
 // bank groups).
-template <typename T, int N, int S, bool HAS_Z>
+template <typename T, int N, int S, bool CONV>
 struct Shape {
     static constexpr int G = N / S;                    // thread groups per channel
     static constexpr int CH = kThreads / G;            // channels per CTA
@@ -91,20 +109,27 @@ struct Shape {
     static constexpr int RAW_ROW = kTL * ES + 16;      // one channel's tokens, raw
     static constexpr int RAW_PLANE = CH * RAW_ROW;
     static constexpr int BC_RAW = kTL * N * ES;        // one raw B (or C) tile
-    static constexpr int NPLANES = HAS_Z ? 3 : 2;
+    static constexpr int NPLANES = 3;                  // u (or x), delta, z
     static constexpr int RAW_BUF = NPLANES * RAW_PLANE + 2 * BC_RAW;
     static constexpr int W_ROW = kTL * 8 + 16;         // (Delta, Delta u) per token
     static constexpr int Y_ROW = kTL * 4 + 16;         // partial output per token
     static constexpr int OFF_W = 2 * RAW_BUF;
     static constexpr int OFF_BC = OFF_W + CH * W_ROW;
     static constexpr int OFF_Y = OFF_BC + kTL * N * 2 * 4;
-    static constexpr int SMEM = OFF_Y + G * CH * Y_ROW;
+    static constexpr int END_Y = OFF_Y + G * CH * Y_ROW;
+    // CONV: the convolution's output u per token (fp32, for D u) and the last
+    // three inputs of the previous tile per channel (two slots)
+    static constexpr int U_ROW = kTL * 4 + 16;
+    static constexpr int OFF_U = END_Y;
+    static constexpr int OFF_HALO = OFF_U + CH * U_ROW;
+    static constexpr int SMEM = CONV ? OFF_HALO + 2 * CH * 16 : END_Y;
     // (row, 8-token chunk) work items of the prologue / epilogue per thread
     static constexpr int CHUNKS = CH * kTL / 8;
     static constexpr int CHUNK_ITERS = CHUNKS / kThreads;
     static_assert(N % S == 0 && CH % 32 == 0, "bad state split");
     static_assert(CHUNKS % kThreads == 0 && kTL % 32 == 0, "bad tile");
-    static_assert(RAW_BUF % 16 == 0 && OFF_BC % 16 == 0 && OFF_Y % 16 == 0, "alignment");
+    static_assert(RAW_BUF % 16 == 0 && OFF_BC % 16 == 0 && OFF_Y % 16 == 0 && OFF_U % 16 == 0,
+                  "alignment");
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
@@ -162,26 +187,24 @@ template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16*
     *reinterpret_cast<uint4*>(dst) = q;
 }
 
-// Gate: silu(z).  bf16 outputs take the one-instruction tanh form
-// silu(z) = z/2 (1 + tanh(z/2)) (relative error ~2^-11, far below bf16's
-// 2^-9 rounding); fp32 outputs take z / (1 + 2^(-z log2 e)).
-template <typename T> __device__ __forceinline__ float gate(float z);
-template <> __device__ __forceinline__ float gate<float>(float z) { return silu(z); }
-template <> __device__ __forceinline__ float gate<__nv_bfloat16>(float z) {
-    const float hz = 0.5f * z;
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hz));
-    return fmaf(hz, t, hz);
+// The first n of 8 values -> global, one element at a time (n >= 8: all).
+template <typename T>
+__device__ __forceinline__ void store_first(T* dst, const float (&v)[8], int n) {
+#pragma unroll
+    for (int e = 0; e < 8; e++)
+        if (e < n) dst[e] = io<T>::from_f32(v[e]);
 }
 
-// gate on a pair of values, packed: the same operations as gate<T>.
-template <typename T> __device__ __forceinline__ float2 gate2(float2 z);
-template <> __device__ __forceinline__ float2 gate2<float>(float2 z) {
+// silu on a pair.  bf16 I/O takes the one-instruction tanh form
+// silu(z) = z/2 (1 + tanh(z/2)) (relative error ~2^-11, far below bf16's
+// 2^-9 rounding); fp32 takes z / (1 + 2^(-z log2 e)).
+template <typename T> __device__ __forceinline__ float2 silu2(float2 z);
+template <> __device__ __forceinline__ float2 silu2<float>(float2 z) {
     const float2 e = __fmul2_rn(make_float2(-z.x, -z.y), make_float2(kLog2e, kLog2e));
     const float2 p = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(ex2(e.x), ex2(e.y)));
     return __fmul2_rn(z, make_float2(rcp(p.x), rcp(p.y)));
 }
-template <> __device__ __forceinline__ float2 gate2<__nv_bfloat16>(float2 z) {
+template <> __device__ __forceinline__ float2 silu2<__nv_bfloat16>(float2 z) {
     const float2 hz = __fmul2_rn(make_float2(0.5f, 0.5f), z);
     float tx, ty;
     asm("tanh.approx.f32 %0, %1;" : "=f"(tx) : "f"(hz.x));
@@ -241,6 +264,53 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// ---------------------------------------------------------------------------
+// The input term of the state update, for a pair of states.
+//
+// First order (ZOH = false): Bbar u = Delta B u; xs is Delta u.
+// Exact zero-order hold (ZOH = true): Bbar u = w B u with the weight
+// w = (exp(Delta A) - 1) / A; xs is u, dt is Delta, ia = 1 / A (0 where
+// A = 0), a = exp(Delta A) = 2^e with e = Delta A log2(e).
+// w = (a - 1) ia, except for |e| < 1/8, where a - 1 would keep only the
+// absolute accuracy of the 2^x unit (~2^-22, a relative error up to
+// 2^-22 / |Delta A|) and w = Delta (1 + Delta A / 2 + (Delta A)^2 / 6 +
+// (Delta A)^3 / 24) is used instead (truncation below 5e-7 relative; at
+// A = 0 it is Delta, the limit of w).
+constexpr float kZohSeries = 0.125f;
+constexpr float kZ2 = 0.34657359027997264f;    // ln 2 / 2
+constexpr float kZ3 = 0.08007374029168081f;    // (ln 2)^2 / 6
+constexpr float kZ4 = 0.013874441803734374f;   // (ln 2)^3 / 24
+
+template <bool ZOH>
+__device__ __forceinline__ float2 input_term2(float2 a, float2 e, float dt, float xs, float2 Bv,
+                                              float2 ia) {
+    const float2 xb = __fmul2_rn(make_float2(xs, xs), Bv);
+    if constexpr (!ZOH) {
+        return xb;
+    } else {
+        float2 w = __fmul2_rn(__fadd2_rn(a, make_float2(-1.0f, -1.0f)), ia);
+        float2 t = __ffma2_rn(e, make_float2(kZ4, kZ4), make_float2(kZ3, kZ3));
+        t = __ffma2_rn(e, t, make_float2(kZ2, kZ2));
+        t = __ffma2_rn(e, t, make_float2(1.0f, 1.0f));
+        const float2 ws = __fmul2_rn(make_float2(dt, dt), t);
+        if (fabsf(e.x) < kZohSeries) w.x = ws.x;
+        if (fabsf(e.y) < kZohSeries) w.y = ws.y;
+        return __fmul2_rn(w, xb);
+    }
+}
+template <bool ZOH>
+__device__ __forceinline__ float input_term1(float a, float e, float dt, float xs, float Bv,
+                                             float ia) {
+    const float xb = xs * Bv;
+    if constexpr (!ZOH) {
+        return xb;
+    } else {
+        float w = (a - 1.0f) * ia;
+        if (fabsf(e) < kZohSeries) w = dt * fmaf(e, fmaf(e, fmaf(e, kZ4, kZ3), kZ2), 1.0f);
+        return w * xb;
+    }
+}
+
 // NT consecutive tokens for one thread, software-pipelined: while the state
 // update of token t runs, the 2^x of token t + 1 are issued two at a time
 // between its FMAs, so that the special-function unit and the FMA pipe work
@@ -249,28 +319,30 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
 // B, C rows and (Delta, Delta u) of token t + 1 are loaded before token t's
 // update.  Same operations per token as token_step, in the same order:
 // bit-identical.
-// wrow: (Delta, Delta u) pairs, two tokens per float4; bcf: B (S floats) then
-// C (S floats) of this thread's states, BCT floats per token; yrow: NT
-// partial outputs (16-byte aligned).
-// RAW: B and C are bf16 rows of the raw tile instead (bcf then points at this
+// wrow: (Delta, xs) pairs, two tokens per float4 (xs = Delta u, or u for
+// ZOH); bcp: B (S floats) then C (S floats) of this thread's states, BCT
+// floats per token; yrow: NT partial outputs (16-byte aligned).  ia: 1 / A
+// per state (ZOH only).
+// RAW: B and C are bf16 rows of the raw tile instead (bcp then points at this
 // thread's B states, C follows RAW_C bytes on, BCT bytes per token; S = 4 or
 // 8), unpacked exactly in registers.
-template <int S, int BCT, int NT, bool RAW = false, int RAW_C = 0>
+template <int S, int BCT, int NT, bool ZOH, bool RAW = false, int RAW_C = 0>
 __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, const void* __restrict__ bcp,
-                                            float (&h)[S], const float (&A2)[S], float* __restrict__ yrow) {
+                                            float (&h)[S], const float (&A2)[S], const float (&ia)[S],
+                                            float* __restrict__ yrow) {
     static_assert(S % 4 == 0 && NT % 4 == 0, "scan_tokens takes S and NT multiples of 4");
     static_assert(!RAW || S == 4 || S == 8, "raw B/C rows take 4 or 8 states");
-    float a[S], B_n[S], C_n[S];
-    float dt_n, dtx_n;
+    float a[S], ec[S], B_n[S], C_n[S];
+    float dt_n, xs_n;
     float4 wq = wrow[0];
     auto load = [&](int t) {   // inputs of token t
         if (t % 2 == 0) {
             wq = wrow[t / 2];
             dt_n = wq.x;
-            dtx_n = wq.y;
+            xs_n = wq.y;
         } else {
             dt_n = wq.z;
-            dtx_n = wq.w;
+            xs_n = wq.w;
         }
         if constexpr (RAW) {
             const unsigned char* bc = static_cast<const unsigned char*>(bcp) + t * BCT;
@@ -311,6 +383,8 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
             const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
             a[n] = ex2(e.x);
             a[n + 1] = ex2(e.y);
+            ec[n] = e.x;
+            ec[n + 1] = e.y;
         }
     }
     float4 out;
@@ -319,14 +393,15 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
         float Bv[S], Cv[S];
 #pragma unroll
         for (int n = 0; n < S; n++) { Bv[n] = B_n[n]; Cv[n] = C_n[n]; }
-        const float dtx = dtx_n;
+        const float dt = dt_n, xs = xs_n;
         if (t + 1 < NT) load(t + 1);
-        const float2 dtx2 = make_float2(dtx, dtx);
         const float2 dtn2 = make_float2(dt_n, dt_n);
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
-            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 bb = input_term2<ZOH>(make_float2(a[n], a[n + 1]), make_float2(ec[n], ec[n + 1]),
+                                               dt, xs, make_float2(Bv[n], Bv[n + 1]),
+                                               make_float2(ia[n], ia[n + 1]));
             const float2 hn = __ffma2_rn(make_float2(a[n], a[n + 1]), make_float2(h[n], h[n + 1]), bb);
             h[n] = hn.x;
             h[n + 1] = hn.y;
@@ -335,6 +410,8 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
                 const float2 e = __fmul2_rn(dtn2, make_float2(A2[n], A2[n + 1]));
                 a[n] = ex2(e.x);
                 a[n + 1] = ex2(e.y);
+                ec[n] = e.x;
+                ec[n + 1] = e.y;
             }
         }
         const float yv = acc.x + acc.y;
@@ -351,24 +428,24 @@ __device__ __forceinline__ void scan_tokens(const float4* __restrict__ wrow, con
 // The aggregate pass's token loop (state only: no C, no output), pipelined
 // like scan_tokens; returns the tile's sum of Delta, added pairwise in token
 // order exactly as the unpipelined loop does.
-template <int S, int BCT, int NT>
+template <int S, int BCT, int NT, bool ZOH>
 __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wrow,
                                                    const float* __restrict__ bcf, float (&h)[S],
-                                                   const float (&A2)[S]) {
+                                                   const float (&A2)[S], const float (&ia)[S]) {
     static_assert(S % 4 == 0 && NT % 2 == 0, "scan_tokens_state takes S % 4 == 0, even NT");
-    float a[S], B_n[S];
-    float dt_n, dtx_n;
+    float a[S], ec[S], B_n[S];
+    float dt_n, xs_n;
     float4 wq = wrow[0];
     float tsum = 0.0f;
     auto load = [&](int t) {
         if (t % 2 == 0) {
             wq = wrow[t / 2];
             dt_n = wq.x;
-            dtx_n = wq.y;
+            xs_n = wq.y;
             tsum += wq.x + wq.z;
         } else {
             dt_n = wq.z;
-            dtx_n = wq.w;
+            xs_n = wq.w;
         }
         const float* bc = bcf + t * BCT;
 #pragma unroll
@@ -385,6 +462,8 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
             const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
             a[n] = ex2(e.x);
             a[n + 1] = ex2(e.y);
+            ec[n] = e.x;
+            ec[n + 1] = e.y;
         }
     }
 #pragma unroll
@@ -392,13 +471,14 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
         float Bv[S];
 #pragma unroll
         for (int n = 0; n < S; n++) Bv[n] = B_n[n];
-        const float dtx = dtx_n;
+        const float dt = dt_n, xs = xs_n;
         if (t + 1 < NT) load(t + 1);
-        const float2 dtx2 = make_float2(dtx, dtx);
         const float2 dtn2 = make_float2(dt_n, dt_n);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
-            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 bb = input_term2<ZOH>(make_float2(a[n], a[n + 1]), make_float2(ec[n], ec[n + 1]),
+                                               dt, xs, make_float2(Bv[n], Bv[n + 1]),
+                                               make_float2(ia[n], ia[n + 1]));
             const float2 hn = __ffma2_rn(make_float2(a[n], a[n + 1]), make_float2(h[n], h[n + 1]), bb);
             h[n] = hn.x;
             h[n + 1] = hn.y;
@@ -406,45 +486,44 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
                 const float2 e = __fmul2_rn(dtn2, make_float2(A2[n], A2[n + 1]));
                 a[n] = ex2(e.x);
                 a[n + 1] = ex2(e.y);
+                ec[n] = e.x;
+                ec[n + 1] = e.y;
             }
         }
     }
     return tsum;
 }
 
-// One token for one thread: advance S states, return the partial C.h.
-template <int S>
-__device__ __forceinline__ float token_step(float dt, float dtx, const float* __restrict__ bc,
-                                            float (&h)[S], const float (&A2)[S]) {
+// One token for one thread (S = 1 or 2): advance S states; with WITH_Y,
+// return the partial C.h.
+template <int S, bool ZOH, bool WITH_Y>
+__device__ __forceinline__ float token_step(float dt, float xs, const float* __restrict__ bc,
+                                            float (&h)[S], const float (&A2)[S],
+                                            const float (&ia)[S]) {
     float Bv[S], Cv[S];
-    if constexpr (S % 4 == 0) {
 #pragma unroll
-        for (int n = 0; n < S; n += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
-            const float4 c4 = *reinterpret_cast<const float4*>(bc + S + n);
-            Bv[n] = b4.x; Bv[n + 1] = b4.y; Bv[n + 2] = b4.z; Bv[n + 3] = b4.w;
-            Cv[n] = c4.x; Cv[n + 1] = c4.y; Cv[n + 2] = c4.z; Cv[n + 3] = c4.w;
-        }
-    } else {
-#pragma unroll
-        for (int n = 0; n < S; n++) { Bv[n] = bc[n]; Cv[n] = bc[S + n]; }
+    for (int n = 0; n < S; n++) {
+        Bv[n] = bc[n];
+        Cv[n] = WITH_Y ? bc[S + n] : 0.0f;
     }
     if constexpr (S == 1) {
-        h[0] = fmaf(ex2(dt * A2[0]), h[0], dtx * Bv[0]);
-        return Cv[0] * h[0];
+        const float e = dt * A2[0];
+        const float a = ex2(e);
+        h[0] = fmaf(a, h[0], input_term1<ZOH>(a, e, dt, xs, Bv[0], ia[0]));
+        return WITH_Y ? Cv[0] * h[0] : 0.0f;
     } else {
         const float2 dt2 = make_float2(dt, dt);
-        const float2 dtx2 = make_float2(dtx, dtx);
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int n = 0; n < S; n += 2) {
             const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
             const float2 a = make_float2(ex2(e.x), ex2(e.y));
-            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
+            const float2 bb = input_term2<ZOH>(a, e, dt, xs, make_float2(Bv[n], Bv[n + 1]),
+                                               make_float2(ia[n], ia[n + 1]));
             const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
             h[n] = hn.x;
             h[n + 1] = hn.y;
-            acc = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc);
+            if constexpr (WITH_Y) acc = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc);
         }
         return acc.x + acc.y;
     }
@@ -457,15 +536,16 @@ __device__ __forceinline__ float token_step(float dt, float dtx, const float* __
 // (~2^-22) would leave a relative error of about 2^-22 / 2^x in Delta.
 // XS = -5 keeps that below 1e-5 (fp32 I/O); XS = -10 below 3e-4, far inside
 // the bf16 tolerance, and the series is then rarely needed.  It is evaluated
-// only when some lane of the warp needs it (a warp vote), so typical step
-// sizes never pay for it.
+// only when some lane of the warp needs it (`series`, a warp vote taken by
+// the caller), so typical step sizes never pay for it.  Returns Delta in
+// natural units; for v > 20 it is v.
 template <int XS>
-__device__ __forceinline__ float2 softplus2_log2(float2 x) {
+__device__ __forceinline__ float2 softplus2_log2(float2 x, bool series) {
     constexpr float kX20 = 20.0f * kLog2e;
     const float2 e = make_float2(ex2(x.x), ex2(x.y));
     const float2 p = __fadd2_rn(make_float2(1.0f, 1.0f), e);
     float2 s = make_float2(x.x > kX20 ? x.x : lg2(p.x), x.y > kX20 ? x.y : lg2(p.y));
-    if (__any_sync(0xffffffffu, fminf(x.x, x.y) < (float)XS)) {
+    if (series) {
         const float2 q = log2_1p_small2(e);
         if (x.x < (float)XS) s.x = q.x;
         if (x.y < (float)XS) s.y = q.y;
@@ -486,58 +566,30 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag) {
     return false;
 }
 
-// One token for one thread without the output sum (the aggregate pass of the
-// chunked schedule needs only the final state).
-template <int S>
-__device__ __forceinline__ void token_state(float dt, float dtx, const float* __restrict__ bc,
-                                            float (&h)[S], const float (&A2)[S]) {
-    float Bv[S];
-    if constexpr (S % 4 == 0) {
-#pragma unroll
-        for (int n = 0; n < S; n += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(bc + n);
-            Bv[n] = b4.x; Bv[n + 1] = b4.y; Bv[n + 2] = b4.z; Bv[n + 3] = b4.w;
-        }
-    } else {
-#pragma unroll
-        for (int n = 0; n < S; n++) Bv[n] = bc[n];
-    }
-    if constexpr (S == 1) {
-        h[0] = fmaf(ex2(dt * A2[0]), h[0], dtx * Bv[0]);
-    } else {
-        const float2 dt2 = make_float2(dt, dt);
-        const float2 dtx2 = make_float2(dtx, dtx);
-#pragma unroll
-        for (int n = 0; n < S; n += 2) {
-            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
-            const float2 a = make_float2(ex2(e.x), ex2(e.y));
-            const float2 bb = __fmul2_rn(dtx2, make_float2(Bv[n], Bv[n + 1]));
-            const float2 hn = __ffma2_rn(a, make_float2(h[n], h[n + 1]), bb);
-            h[n] = hn.x;
-            h[n + 1] = hn.y;
-        }
-    }
-}
-
 // Tiles [tb, te) of channel group `grp`.  AGG: the aggregate pass of the
 // chunked schedule (no output; the final state and the sum of Delta go to
 // part.hout / part.dsum).
-template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC, bool AGG = false>
+template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false, bool AGG = false>
 __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* smem, int64_t grp,
                                           int64_t tb, int64_t te, int* s_ok, const PartIO& part) {
-    using Sh = Shape<T, N, S, HAS_Z>;
+    using Sh = Shape<T, N, S, CONV>;
     constexpr int G = Sh::G, CH = Sh::CH;
+    constexpr int QLAST = kTL / 8 - 1;   // the last 8-token chunk of a tile
+    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
     // bf16 B and C read by the recurrence straight from the raw tile (S = 4:
     // one 8-byte load each, no fp32 staging pass; the Mamba-130M layer shape
     // runs 168 -> 156 us.  At S = 8 the extra unpacking made the Mamba-2.8B
     // shape 5% slower, 428 -> 450 us, so S = 8 keeps the fp32 staging.)
-    constexpr bool RAW_BC = std::is_same<T, __nv_bfloat16>::value && VEC && S == 4 && !AGG;
+    constexpr bool RAW_BC = BF && S == 4 && !AGG && VEC;
 
     const int64_t b = grp / p.groups_per_row;
     const int64_t d0 = (grp % p.groups_per_row) * CH;
     const int rows = (int)(p.dim - d0 < CH ? p.dim - d0 : CH);
     const int64_t row0 = b * p.dim + d0;   // first flat (b, d) row of the group
     const int64_t L = p.L;
+    // GS: an instance for calls with both the gate and softplus, where both
+    // are known at compile time (the common layer configuration)
+    const bool gate = GS || p.gate != 0, softplus = GS || p.softplus != 0;
 
     const T* gu = static_cast<const T*>(p.u);
     const T* gdl = static_cast<const T*>(p.delta);
@@ -549,20 +601,31 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     // recurrence role: group g, channel ch; g is warp-uniform
     const int g = threadIdx.x / CH, ch = threadIdx.x % CH;
     const bool active = ch < rows;
-    float A2[S], h[S];
+    float A2[S], h[S], ia[S];
 #pragma unroll
-    for (int j = 0; j < S; j++)   // exp(Delta A) = 2^(Delta A log2 e)
-        A2[j] = active ? p.A[(d0 + ch) * N + g * S + j] * kLog2e : 0.0f;
+    for (int j = 0; j < S; j++) {   // exp(Delta A) = 2^(Delta A log2 e)
+        const float av = active ? p.A[(d0 + ch) * N + g * S + j] : 0.0f;
+        A2[j] = av * kLog2e;
+        ia[j] = (ZOH && av != 0.0f) ? 1.0f / av : 0.0f;   // the ZOH weight's 1/A
+    }
 
     // prologue / epilogue role: constants of the rows this thread touches
     float bias_r[Sh::CHUNK_ITERS], D_r[Sh::CHUNK_ITERS];
+    float cw_r[CONV ? Sh::CHUNK_ITERS : 1][4], cb_r[CONV ? Sh::CHUNK_ITERS : 1];
 #pragma unroll
     for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
         int r, q;
         chunk_of<CH>(it, r, q);
         const float bv = (p.bias && r < rows) ? p.bias[d0 + r] : 0.0f;
-        bias_r[it] = SOFTPLUS ? bv * kLog2e : bv;
+        bias_r[it] = softplus ? bv * kLog2e : bv;
         D_r[it] = (p.D && r < rows) ? p.D[d0 + r] : 0.0f;
+        if constexpr (CONV) {   // taps aligned to the newest input (4 - K leading zeros)
+            const int K = p.conv_k;
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                cw_r[it][j] = (r < rows && j >= 4 - K) ? p.conv_w[(d0 + r) * K + j - (4 - K)] : 0.0f;
+            cb_r[it] = (p.conv_b && r < rows) ? p.conv_b[d0 + r] : 0.0f;
+        }
     }
 
     auto load_tile = [&](int64_t tile, int slot) {
@@ -570,7 +633,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         const int64_t t0 = tile * kTL;
         load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0);
         load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0);
-        if constexpr (HAS_Z && !AGG)
+        if (gate && !AGG)
             load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0);
         unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
         load_bc<T, N, VEC>(bcraw, gB, L, t0);
@@ -581,14 +644,34 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     load_tile(tb, 0);
     cp_async_commit();
 
+    if constexpr (CONV) {   // the three inputs before the part's first token
+        const int64_t t0 = tb * kTL;
+        const int K = p.conv_k;
+        const T* gs = static_cast<const T*>(p.conv_state);
+        for (int r = threadIdx.x; r < CH; r += kThreads) {
+            float hv[3] = {0.0f, 0.0f, 0.0f};
+            if (r < rows) {
+#pragma unroll
+                for (int j = 0; j < 3; j++) {
+                    const int64_t src = t0 - 3 + j;   // token index of halo entry j
+                    if (src >= 0)
+                        hv[j] = io<T>::to_f32(gu[(row0 + r) * L + src]);
+                    else if (gs && src >= -(K - 1))
+                        hv[j] = io<T>::to_f32(gs[(row0 + r) * (K - 1) + (K - 1) + src]);
+                }
+            }
+            *reinterpret_cast<float4*>(smem + Sh::OFF_HALO + r * 16) = make_float4(hv[0], hv[1], hv[2], 0.0f);
+        }
+    }
+
     // initial state: zero, given, or the carry handed over by another CTA
     if (part.init == 0) {
 #pragma unroll
         for (int j = 0; j < S; j++) h[j] = 0.0f;
-    } else if (part.init == 2) {
-        const float* src = part.h0 + ch * N + g * S;
+    } else if (part.init == 2 || part.init == 3) {
+        const float* src = (part.init == 2 ? part.h0 + ch * N : p.h0 + (row0 + ch) * N) + g * S;
 #pragma unroll
-        for (int j = 0; j < S; j++) h[j] = __ldcg(src + j);
+        for (int j = 0; j < S; j++) h[j] = active ? __ldcg(src + j) : 0.0f;
     } else {
         if (threadIdx.x == 0) {
             const bool ok = wait_flag(p.flags + grp);
@@ -615,27 +698,73 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         const int64_t t0 = tile * kTL;
         const int tvalid = (int)(L - t0 < kTL ? L - t0 : kTL);
 
-        // ---- prologue: (Delta, Delta u) pairs, B/C to fp32 ----
+        // ---- prologue: [u from the convolution], (Delta, Delta u) pairs, B/C to fp32 ----
 #pragma unroll
         for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
             int r, q;
             chunk_of<CH>(it, r, q);
             float uv[8], dv[8];
-            unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            if constexpr (CONV) {
+                // inputs t-3 .. t+7 for the chunk's tokens t = 8q .. 8q+7: the
+                // previous chunk's last three, or the previous tile's (halo)
+                float xx[11], xc[8];
+                unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, xc);
+                if (q == 0) {
+                    const float4 hv = *reinterpret_cast<const float4*>(smem + Sh::OFF_HALO +
+                                                                       slot * CH * 16 + r * 16);
+                    xx[0] = hv.x; xx[1] = hv.y; xx[2] = hv.z;
+                } else {
+                    float xp[8];
+                    unpack8<T>(buf + r * Sh::RAW_ROW + (q - 1) * 8 * Sh::ES, xp);
+                    xx[0] = xp[5]; xx[1] = xp[6]; xx[2] = xp[7];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; e++) xx[3 + e] = xc[e];
+                if (q == QLAST)   // the next tile's first chunk reads these
+                    *reinterpret_cast<float4*>(smem + Sh::OFF_HALO + (slot ^ 1) * CH * 16 + r * 16) =
+                        make_float4(xc[5], xc[6], xc[7], 0.0f);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    float2 s2 = make_float2(cb_r[it], cb_r[it]);
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        s2 = __ffma2_rn(make_float2(cw_r[it][j], cw_r[it][j]),
+                                        make_float2(xx[e + j], xx[e + 1 + j]), s2);
+                    const float2 sv = silu2<T>(s2);
+                    uv[e] = sv.x;
+                    uv[e + 1] = sv.y;
+                }
+                float4* us = reinterpret_cast<float4*>(smem + Sh::OFF_U + r * Sh::U_ROW + q * 32);
+                us[0] = make_float4(uv[0], uv[1], uv[2], uv[3]);
+                us[1] = make_float4(uv[4], uv[5], uv[6], uv[7]);
+                if (!AGG && p.u_out && r < rows && q * 8 < tvalid) {
+                    T* dst = static_cast<T*>(p.u_out) + (row0 + r) * L + t0 + q * 8;
+                    if (VEC && q * 8 + 8 <= tvalid) store8<T>(dst, uv);
+                    else store_first<T>(dst, uv, tvalid - q * 8);
+                }
+            } else {
+                unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            }
             unpack8<T>(buf + Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, dv);
             // pairs of tokens in packed fp32 arithmetic (same roundings as
             // the scalar form: fused multiply-add, add, multiply)
             float2 dt[4];
             const float2 bias2 = make_float2(bias_r[it], bias_r[it]);
+            if (softplus) {
+                constexpr int XS = BF ? -10 : -5;
+                float2 xv[4];
+                float xmin = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float2 d2 = make_float2(dv[e], dv[e + 1]);
-                if constexpr (SOFTPLUS) {
-                    constexpr int XS = std::is_same<T, float>::value ? -5 : -10;
-                    dt[e / 2] = softplus2_log2<XS>(__ffma2_rn(d2, make_float2(kLog2e, kLog2e), bias2));
-                } else {
-                    dt[e / 2] = __fadd2_rn(d2, bias2);
+                for (int e = 0; e < 8; e += 2) {
+                    xv[e / 2] = __ffma2_rn(make_float2(dv[e], dv[e + 1]), make_float2(kLog2e, kLog2e), bias2);
+                    xmin = fminf(xmin, fminf(xv[e / 2].x, xv[e / 2].y));
                 }
+                const bool series = __any_sync(0xffffffffu, xmin < (float)XS);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) dt[e / 2] = softplus2_log2<XS>(xv[e / 2], series);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) dt[e / 2] = __fadd2_rn(make_float2(dv[e], dv[e + 1]), bias2);
             }
             if (tvalid < kTL) {   // tokens past the end leave the state untouched
 #pragma unroll
@@ -647,8 +776,11 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             float4* w = reinterpret_cast<float4*>(smem + Sh::OFF_W + r * Sh::W_ROW + q * 64);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const float2 du = __fmul2_rn(dt[e / 2], make_float2(uv[e], uv[e + 1]));
-                w[e / 2] = make_float4(dt[e / 2].x, du.x, dt[e / 2].y, du.y);
+                // the second entry of each token: Delta u, or u itself for the
+                // exact zero-order hold (which weighs it by (2^e - 1) / A)
+                const float2 xs = ZOH ? make_float2(uv[e], uv[e + 1])
+                                      : __fmul2_rn(dt[e / 2], make_float2(uv[e], uv[e + 1]));
+                w[e / 2] = make_float4(dt[e / 2].x, xs.x, dt[e / 2].y, xs.y);
             }
         }
         if constexpr (!RAW_BC) {
@@ -680,51 +812,44 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         __syncthreads();
 
         // ---- recurrence over the tile ----
-        if constexpr (RAW_BC && !AGG) {
+        {
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
-            const unsigned char* braw = buf + Sh::NPLANES * Sh::RAW_PLANE + g * S * 2;
+            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
             float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
-            scan_tokens<S, N * 2, kTL, true, Sh::BC_RAW>(wrow, braw, h, A2, yrow);
-        } else if constexpr (AGG && S % 4 == 0) {
-            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
-            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
-            const float tsum = scan_tokens_state<S, G * 2 * S, kTL>(wrow, bcf, h, A2);
-            const float yk = tsum - dcomp, tk = dsum + yk;
-            dcomp = (tk - dsum) - yk;
-            dsum = tk;
-        } else if constexpr (AGG) {
-            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
-            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
-            float tsum = 0.0f;
+            if constexpr (AGG && S % 4 == 0) {
+                const float tsum = scan_tokens_state<S, G * 2 * S, kTL, ZOH>(wrow, bcf, h, A2, ia);
+                const float yk = tsum - dcomp, tk = dsum + yk;
+                dcomp = (tk - dsum) - yk;
+                dsum = tk;
+            } else if constexpr (AGG) {
+                float tsum = 0.0f;
 #pragma unroll 2
-            for (int t = 0; t < kTL; t += 2) {
-                const float4 w = wrow[t / 2];
-                token_state<S>(w.x, w.y, bcf + (t + 0) * G * 2 * S, h, A2);
-                token_state<S>(w.z, w.w, bcf + (t + 1) * G * 2 * S, h, A2);
-                tsum += w.x + w.z;
-            }
-            const float yk = tsum - dcomp, tk = dsum + yk;
-            dcomp = (tk - dsum) - yk;
-            dsum = tk;
-        } else if constexpr (S % 4 == 0) {
-            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
-            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
-            float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
-            scan_tokens<S, G * 2 * S, kTL>(wrow, bcf, h, A2, yrow);
-        } else {
-            const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
-            const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
-            float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
+                for (int t = 0; t < kTL; t += 2) {
+                    const float4 w = wrow[t / 2];
+                    token_step<S, ZOH, false>(w.x, w.y, bcf + (t + 0) * G * 2 * S, h, A2, ia);
+                    token_step<S, ZOH, false>(w.z, w.w, bcf + (t + 1) * G * 2 * S, h, A2, ia);
+                    tsum += w.x + w.z;
+                }
+                const float yk = tsum - dcomp, tk = dsum + yk;
+                dcomp = (tk - dsum) - yk;
+                dsum = tk;
+            } else if constexpr (RAW_BC) {
+                const unsigned char* braw = buf + Sh::NPLANES * Sh::RAW_PLANE + g * S * 2;
+                scan_tokens<S, N * 2, kTL, ZOH, true, Sh::BC_RAW>(wrow, braw, h, A2, ia, yrow);
+            } else if constexpr (S % 4 == 0) {
+                scan_tokens<S, G * 2 * S, kTL, ZOH>(wrow, bcf, h, A2, ia, yrow);
+            } else {
 #pragma unroll 2
-            for (int t = 0; t < kTL; t += 4) {
-                const float4 w01 = wrow[t / 2];
-                const float4 w23 = wrow[t / 2 + 1];
-                float4 out;
-                out.x = token_step<S>(w01.x, w01.y, bcf + (t + 0) * G * 2 * S, h, A2);
-                out.y = token_step<S>(w01.z, w01.w, bcf + (t + 1) * G * 2 * S, h, A2);
-                out.z = token_step<S>(w23.x, w23.y, bcf + (t + 2) * G * 2 * S, h, A2);
-                out.w = token_step<S>(w23.z, w23.w, bcf + (t + 3) * G * 2 * S, h, A2);
-                *reinterpret_cast<float4*>(yrow + t) = out;
+                for (int t = 0; t < kTL; t += 4) {
+                    const float4 w01 = wrow[t / 2];
+                    const float4 w23 = wrow[t / 2 + 1];
+                    float4 out;
+                    out.x = token_step<S, ZOH, true>(w01.x, w01.y, bcf + (t + 0) * G * 2 * S, h, A2, ia);
+                    out.y = token_step<S, ZOH, true>(w01.z, w01.w, bcf + (t + 1) * G * 2 * S, h, A2, ia);
+                    out.z = token_step<S, ZOH, true>(w23.x, w23.y, bcf + (t + 2) * G * 2 * S, h, A2, ia);
+                    out.w = token_step<S, ZOH, true>(w23.z, w23.w, bcf + (t + 3) * G * 2 * S, h, A2, ia);
+                    *reinterpret_cast<float4*>(yrow + t) = out;
+                }
             }
         }
         __syncthreads();
@@ -748,30 +873,32 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
                 for (int e = 0; e < 4; e++) y2[e] = gg == 0 ? v[e] : __fadd2_rn(y2[e], v[e]);
             }
             float uv[8];
-            unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            if constexpr (CONV) {
+                const float4* us = reinterpret_cast<const float4*>(smem + Sh::OFF_U + r * Sh::U_ROW + q * 32);
+                const float4 u0 = us[0], u1 = us[1];
+                uv[0] = u0.x; uv[1] = u0.y; uv[2] = u0.z; uv[3] = u0.w;
+                uv[4] = u1.x; uv[5] = u1.y; uv[6] = u1.z; uv[7] = u1.w;
+            } else {
+                unpack8<T>(buf + r * Sh::RAW_ROW + q * 8 * Sh::ES, uv);
+            }
             const float2 D2 = make_float2(D_r[it], D_r[it]);
 #pragma unroll
             for (int e = 0; e < 4; e++)
                 y2[e] = __ffma2_rn(D2, make_float2(uv[2 * e], uv[2 * e + 1]), y2[e]);
-            if constexpr (HAS_Z) {
+            if (gate) {
                 float zv[8];
                 unpack8<T>(buf + 2 * Sh::RAW_PLANE + r * Sh::RAW_ROW + q * 8 * Sh::ES, zv);
 #pragma unroll
                 for (int e = 0; e < 4; e++)
-                    y2[e] = __fmul2_rn(y2[e], gate2<T>(make_float2(zv[2 * e], zv[2 * e + 1])));
+                    y2[e] = __fmul2_rn(y2[e], silu2<T>(make_float2(zv[2 * e], zv[2 * e + 1])));
             }
             float ys[8];
 #pragma unroll
             for (int e = 0; e < 4; e++) { ys[2 * e] = y2[e].x; ys[2 * e + 1] = y2[e].y; }
             if (r < rows && q * 8 < tvalid) {
                 T* dst = gy + (row0 + r) * L + t0 + q * 8;
-                if (VEC && q * 8 + 8 <= tvalid) {
-                    store8<T>(dst, ys);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; e++)
-                        if (q * 8 + e < tvalid) dst[e] = io<T>::from_f32(ys[e]);
-                }
+                if (VEC && q * 8 + 8 <= tvalid) store8<T>(dst, ys);
+                else store_first<T>(dst, ys, tvalid - q * 8);
             }
         }
         __syncthreads();
@@ -808,19 +935,20 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 // head first (publishing that state), then its whole groups, and the
 // continuation of its first group last, so the state it needs has long been
 // published when it gets there.  With P <= ngroups no group is split twice.
-template <typename T, int N, int S, bool HAS_Z, bool SOFTPLUS, bool VEC>
+template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false>
 __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
+    using Sh = Shape<T, N, S, CONV>;
     if (p.nchunks > 0) {   // pass 3 of the chunked schedule (see scan_chunk_agg_kernel)
-        using Sh = Shape<T, N, S, HAS_Z>;
         const int64_t units = p.ngroups * p.nchunks;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
             const int64_t grp = u / p.nchunks, ck = u % p.nchunks;
             const int64_t tb = ck * p.tiles_per_chunk;
             const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
-            const PartIO io{ck == 0 ? 0 : 2, p.agg + u * Sh::CH * N, nullptr, nullptr, false};
-            scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok, io);
+            // every chunk starts from its carry-in (the first: the initial state)
+            const PartIO io{2, p.agg + u * Sh::CH * N, nullptr, nullptr, false};
+            scan_part<T, N, S, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
             __syncthreads();
         }
         return;
@@ -830,13 +958,13 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
     const int64_t e = W * (blockIdx.x + 1) / gridDim.x;
     if (s >= e) {   // empty sequence (or more CTAs than tiles): only last_state remains
         if (p.ntiles == 0 && p.last_state) {
-            using Sh = Shape<T, N, S, HAS_Z>;
             for (int64_t grp = blockIdx.x; grp < p.ngroups; grp += gridDim.x) {
                 const int64_t b = grp / p.groups_per_row;
                 const int64_t d0 = (grp % p.groups_per_row) * Sh::CH;
                 const int rows = (int)(p.dim - d0 < Sh::CH ? p.dim - d0 : Sh::CH);
+                const int64_t base = (b * p.dim + d0) * N;
                 for (int i = threadIdx.x; i < rows * N; i += kThreads)
-                    p.last_state[(b * p.dim + d0) * N + i] = 0.0f;
+                    p.last_state[base + i] = p.h0 ? p.h0[base + i] : 0.0f;
             }
         }
         return;
@@ -846,8 +974,9 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
         const int64_t lo = grp * p.ntiles;
         const int64_t tb = (s > lo ? s : lo) - lo;
         const int64_t te = (e < lo + p.ntiles ? e : lo + p.ntiles) - lo;
-        const PartIO io{tb == 0 ? 0 : 1, nullptr, nullptr, nullptr, true};
-        scan_part<T, N, S, HAS_Z, SOFTPLUS, VEC>(p, smem, grp, tb, te, &s_ok, io);
+        const int init = tb > 0 ? 1 : (p.h0 ? 3 : 0);
+        const PartIO io{init, nullptr, nullptr, nullptr, true};
+        scan_part<T, N, S, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
     }
 }
 
@@ -859,15 +988,16 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
 //           final state is the chunk's b; its a is exp(A sum Delta)
 //           (scan_chunk_agg_kernel)
 //   pass 2  per (channel, state) a sequential scan over the chunks composes
-//           them into each chunk's carry-in (scan_chunk_carry_kernel)
+//           them into each chunk's carry-in, starting from the initial state
+//           (scan_chunk_carry_kernel)
 //   pass 3  every unit scans its chunk again from its carry-in and writes y
 //           and, for the last chunk, last_state (scan_fwd_kernel with
 //           p.nchunks > 0).
 // Passes 1 and 3 are independent over units: grid-stride loops of
 // persistent CTAs.  The price is a second pass over the inputs (no z, no y).
-template <typename T, int N, int S, bool SOFTPLUS, bool VEC>
+template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC>
 __global__ void __launch_bounds__(kThreads, 2) scan_chunk_agg_kernel(ScanParams p) {
-    using Sh = Shape<T, N, S, false>;
+    using Sh = Shape<T, N, S, CONV>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
     const int64_t units = p.ngroups * p.nchunks;
@@ -876,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_chunk_agg_kernel(ScanParams 
         const int64_t tb = ck * p.tiles_per_chunk;
         const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
         const PartIO io{0, nullptr, p.agg + u * Sh::CH * N, p.dsum + u * Sh::CH, false};
-        scan_part<T, N, S, false, SOFTPLUS, VEC, true>(p, smem, grp, tb, te, &s_ok, io);
+        scan_part<T, N, S, ZOH, CONV, VEC, false, true>(p, smem, grp, tb, te, &s_ok, io);
         __syncthreads();
     }
 }
@@ -889,16 +1019,18 @@ __global__ void scan_chunk_carry_kernel(ScanParams p) {
     if (idx >= p.ngroups * CH * N) return;
     const int64_t grp = idx / (CH * N);
     const int rem = (int)(idx % (CH * N)), ch = rem / N, n = rem % N;
+    const int64_t b = grp / p.groups_per_row;
     const int64_t d = (grp % p.groups_per_row) * CH + ch;
-    const float A2 = d < p.dim ? p.A[d * N + n] * kLog2e : 0.0f;
-    float carry = 0.0f;
+    const bool in = d < p.dim;
+    const float A2 = in ? p.A[d * N + n] * kLog2e : 0.0f;
+    float carry = (in && p.h0) ? p.h0[(b * p.dim + d) * N + n] : 0.0f;
     for (int64_t ck = 0; ck < p.nchunks; ck++) {
         const int64_t u = grp * p.nchunks + ck;
         float* st = p.agg + (u * CH + ch) * N + n;
-        const float b = *st;                          // the chunk's state from zero
+        const float bk = *st;                          // the chunk's state from zero
         const float a = ex2(A2 * p.dsum[u * CH + ch]);   // prod of exp(Delta A) over the chunk
-        *st = carry;                                  // the state entering the chunk
-        carry = fmaf(a, carry, b);
+        *st = carry;                                   // the state entering the chunk
+        carry = fmaf(a, carry, bk);
     }
 }
 

@@ -22,21 +22,21 @@ constexpr int kVersion = 100;  // 0.1.0
 
 // The kernel instance for these sizes and options.  split (N = 16 only): 0
 // picks the state split from the sizes, 4 or 8 forces it.
-int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool z, bool sp, bool vec,
+int dispatch_scan(const ssm_dims* d, const ssm::ScanParams& p, bool zoh, bool conv, bool vec,
                   unsigned char* ws, int sms, cudaStream_t s, int split) {
     const bool bf = d->io == SSM_IO_BF16;
     const int n = (int)d->dstate;
     const ChunkPlan cp = chunk_plan(d);
     if (cp.on)
-        return bf ? fwd_chunked_bf16(n, p, cp, z, sp, vec, ws, sms, s)
-                  : fwd_chunked_f32(n, p, cp, z, sp, vec, ws, sms, s);
+        return bf ? fwd_chunked_bf16(n, p, cp, zoh, conv, vec, ws, sms, s)
+                  : fwd_chunked_f32(n, p, cp, zoh, conv, vec, ws, sms, s);
     if (n == 16) {
         const int sp16 = split ? split : n16_split(d, sms);
-        return bf ? fwd_scan_bf16_n16(sp16, p, d->chunk, z, sp, vec, ws, sms, s)
-                  : fwd_scan_f32_n16(sp16, p, d->chunk, z, sp, vec, ws, sms, s);
+        return bf ? fwd_scan_bf16_n16(sp16, p, d->chunk, zoh, conv, vec, ws, sms, s)
+                  : fwd_scan_f32_n16(sp16, p, d->chunk, zoh, conv, vec, ws, sms, s);
     }
-    return bf ? fwd_scan_bf16_small(n, p, d->chunk, z, sp, vec, ws, sms, s)
-              : fwd_scan_f32_small(n, p, d->chunk, z, sp, vec, ws, sms, s);
+    return bf ? fwd_scan_bf16_small(n, p, d->chunk, zoh, conv, vec, ws, sms, s)
+              : fwd_scan_f32_small(n, p, d->chunk, zoh, conv, vec, ws, sms, s);
 }
 
 }  // namespace
@@ -47,32 +47,53 @@ namespace {
 // The scan; split (N = 16 only): 0 picks the state split from the sizes, 4 or
 // 8 forces it (the host entry point keeps its slices on the full problem's
 // choice).
-int scan_fwd_impl(const ssm_dims* dims, const void* u, const void* delta, const float* A,
-                  const void* B, const void* C, const float* D, const void* z,
-                  const float* delta_bias, int delta_softplus, void* y, float* last_state,
-                  void* workspace, size_t workspace_bytes, void* stream, int split) {
+int scan_fwd_impl(const ssm_dims* dims, const ssm_scan_opts* opts, const void* u,
+                  const void* delta, const float* A, const void* B, const void* C,
+                  const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                  void* y, float* last_state, void* workspace, size_t workspace_bytes,
+                  void* stream, int split) {
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
+    const ssm_scan_opts none{};
+    const ssm_scan_opts& o = opts ? *opts : none;
+    if (o.input_term != SSM_INPUT_DELTA_B && o.input_term != SSM_INPUT_ZOH) return SSM_ERR_BAD_OPTION;
+    if (o.conv_width < 0 || o.conv_width > 4) return SSM_ERR_BAD_OPTION;
+    const bool conv = o.conv_width > 0;
+    if (conv && !o.conv_weight) return SSM_ERR_NULL_ARG;
     // With L = 0 the (batch, dim, L) and (batch, L, N) tensors are empty and
-    // may be NULL; only last_state is written (zeros).
+    // may be NULL; only last_state is written (the initial state).
     const bool empty = dims->seqlen == 0;
     if (!A || (!empty && (!u || !delta || !B || !C || !y))) return SSM_ERR_NULL_ARG;
     const size_t es = io_size(dims->io);
-    for (const void* q : {u, delta, B, C, z, static_cast<const void*>(y)})
+    const void* u_out = conv ? o.u_out : nullptr;
+    const void* cstate = conv ? o.conv_state : nullptr;
+    for (const void* q : {u, delta, B, C, z, static_cast<const void*>(y), u_out, cstate})
         if (q && !aligned(q, es)) return SSM_ERR_MISALIGNED;
     for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
                           static_cast<const void*>(delta_bias),
-                          static_cast<const void*>(last_state)})
+                          static_cast<const void*>(last_state), static_cast<const void*>(o.h0),
+                          static_cast<const void*>(conv ? o.conv_weight : nullptr),
+                          static_cast<const void*>(conv ? o.conv_bias : nullptr)})
         if (q && !aligned(q, 4)) return SSM_ERR_MISALIGNED;
+    const int64_t K = o.conv_width;
     const Range in[] = {{u, s.seq * (int64_t)es}, {delta, s.seq * (int64_t)es},
                         {z, s.seq * (int64_t)es}, {B, s.bc * (int64_t)es},
                         {C, s.bc * (int64_t)es},  {A, s.par * 4},
-                        {D, dims->dim * 4},       {delta_bias, dims->dim * 4}};
-    const Range out_y{y, s.seq * (int64_t)es}, out_h{last_state, s.state * 4};
+                        {D, dims->dim * 4},       {delta_bias, dims->dim * 4},
+                        {conv ? o.conv_weight : nullptr, dims->dim * K * 4},
+                        {conv ? o.conv_bias : nullptr, dims->dim * 4},
+                        {cstate, s.chan * (K > 0 ? K - 1 : 0) * (int64_t)es}};
+    const Range out_y{y, s.seq * (int64_t)es}, out_h{last_state, s.state * 4},
+        out_u{u_out, s.seq * (int64_t)es}, in_h0{o.h0, s.state * 4};
     for (const Range& r : in)
-        if (overlap(r, out_y) || overlap(r, out_h)) return SSM_ERR_ALIAS;
-    if (overlap(out_y, out_h)) return SSM_ERR_ALIAS;
+        if (overlap(r, out_y) || overlap(r, out_h) || overlap(r, out_u)) return SSM_ERR_ALIAS;
+    if (overlap(out_y, out_h) || overlap(out_y, out_u) || overlap(out_h, out_u))
+        return SSM_ERR_ALIAS;
+    // the initial state may be last_state itself (a state continued in place),
+    // but no other output
+    if (overlap(in_h0, out_y) || overlap(in_h0, out_u)) return SSM_ERR_ALIAS;
+    if (overlap(in_h0, out_h) && o.h0 != last_state) return SSM_ERR_ALIAS;
 
     const ScanWorkspace wl = scan_workspace(dims);
     if (wl.total > 0) {
@@ -81,22 +102,33 @@ int scan_fwd_impl(const ssm_dims* dims, const void* u, const void* delta, const 
         const Range ws{workspace, (int64_t)wl.total};
         for (const Range& r : in)
             if (overlap(r, ws)) return SSM_ERR_ALIAS;
-        if (overlap(out_y, ws) || overlap(out_h, ws)) return SSM_ERR_ALIAS;
+        if (overlap(out_y, ws) || overlap(out_h, ws) || overlap(out_u, ws) || overlap(in_h0, ws))
+            return SSM_ERR_ALIAS;
     }
     ssm::ScanParams p{};
     p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
     p.bias = delta_bias; p.y = y; p.last_state = last_state;
     p.batch = dims->batch; p.dim = dims->dim; p.L = dims->seqlen;
-    // 16-byte vector path: every row of u/delta/z/y starts on a 16-byte boundary
+    // 16-byte vector path: every row of u/delta/z/y (and u_out) starts on a
+    // 16-byte boundary
     const bool vec = (dims->seqlen * (int64_t)es) % 16 == 0 && aligned(u, 16) &&
                      aligned(delta, 16) && aligned(y, 16) && (!z || aligned(z, 16)) &&
-                     aligned(B, 16) && aligned(C, 16);
-    const bool sp = delta_softplus != 0;
+                     aligned(B, 16) && aligned(C, 16) && (!u_out || aligned(u_out, 16));
+    p.gate = z != nullptr;
+    p.softplus = delta_softplus != 0;
+    p.h0 = o.h0;
+    if (conv) {
+        p.conv_w = o.conv_weight;
+        p.conv_b = o.conv_bias;
+        p.conv_state = cstate;
+        p.u_out = const_cast<void*>(u_out);
+        p.conv_k = (int)K;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int sms = 0;
     if (device_sms(&sms) != SSM_OK) return SSM_ERR_CUDA;
-    return dispatch_scan(dims, p, z != nullptr, sp, vec, ws, sms, st, split);
+    return dispatch_scan(dims, p, o.input_term == SSM_INPUT_ZOH, conv, vec, ws, sms, st, split);
 }
 
 }  // namespace
@@ -122,6 +154,7 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
         case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
+        case SSM_ERR_BAD_OPTION: return "an option of ssm_scan_opts is out of range";
         case SSM_ERR_TOO_LARGE:
             return "the problem needs more scratch than the library's built-in buffer holds";
     }
@@ -149,8 +182,17 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus, void* y, float* last_state,
                  void* workspace, size_t workspace_bytes, void* stream) {
-    return scan_fwd_impl(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
-                         workspace, workspace_bytes, stream, 0);
+    return scan_fwd_impl(dims, nullptr, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y,
+                         last_state, workspace, workspace_bytes, stream, 0);
+}
+
+int ssm_scan_fwd_ex(const ssm_dims* dims, const ssm_scan_opts* opts, const void* u,
+                    const void* delta, const float* A, const void* B, const void* C,
+                    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                    void* y, float* last_state, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    return scan_fwd_impl(dims, opts, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y,
+                         last_state, workspace, workspace_bytes, stream, 0);
 }
 
 int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void* delta,
@@ -411,7 +453,7 @@ int ssm_scan_fwd_host(const ssm_dims* dims, const void* u, const void* delta, co
         ok = ok && cudaStreamWaitEvent(st, ev_in[set], 0) == cudaSuccess;
         if (ok) {
             ssm_dims d1{1, w, N, L, dims->io, slice_chunk};
-            rc = scan_fwd_impl(&d1, sb + o_u, sb + o_dl, dA + d0 * N, sb + o_B, sb + o_C,
+            rc = scan_fwd_impl(&d1, nullptr, sb + o_u, sb + o_dl, dA + d0 * N, sb + o_B, sb + o_C,
                               dD ? dD + d0 : nullptr, z ? sb + o_z : nullptr, dbias ? dbias + d0 : nullptr,
                               delta_softplus, sb + o_y, last_state ? reinterpret_cast<float*>(sb + o_h) : nullptr,
                               ws_bytes ? dev + off_ws : nullptr, ws_bytes, st, split);

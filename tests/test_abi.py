@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.ssm_version() >= 100
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         s = _lib.status_string(code)
         assert s and s != "unknown status", code
     assert _lib.status_string(-99) == "unknown status"
@@ -180,3 +180,34 @@ def test_noalloc_refuses_problems_beyond_its_buffer(lib):
     assert noalloc(None) == _lib.SSM_ERR_NULL_ARG
     assert noalloc(dims(dstate=3)) == _lib.SSM_ERR_UNSUPPORTED_N
     assert noalloc(dims(batch=0)) == _lib.SSM_ERR_BAD_DIMS
+
+
+def scan_ex(lib, d, opts, **kw):
+    a = dict(u=P[0], delta=P[1], A=P[2], B=P[3], C=P[4], D=P[5], z=P[6], bias=P[7], y=P[8],
+             last=P[9])
+    a.update(kw)
+    return lib.ssm_scan_fwd_ex(ctypes.byref(d), None if opts is None else ctypes.byref(opts),
+                               a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                               a["bias"], 1, a["y"], a["last"], None, 0, None)
+
+
+def test_scan_ex_option_checks(lib):
+    """ssm_scan_fwd_ex refuses options out of range, a convolution without
+    taps, and an initial state or convolution output that overlaps an output,
+    before anything is enqueued."""
+    d = dims(batch=2, dim=8, dstate=16, seqlen=64)
+    O = _lib.ssm_scan_opts
+    assert scan_ex(lib, d, O(input_term=2)) == _lib.SSM_ERR_BAD_OPTION
+    assert scan_ex(lib, d, O(input_term=-1)) == _lib.SSM_ERR_BAD_OPTION
+    assert scan_ex(lib, d, O(conv_width=5)) == _lib.SSM_ERR_BAD_OPTION
+    assert scan_ex(lib, d, O(conv_width=-1)) == _lib.SSM_ERR_BAD_OPTION
+    assert scan_ex(lib, d, O(conv_width=4)) == _lib.SSM_ERR_NULL_ARG          # no taps
+    assert scan_ex(lib, d, O(h0=P[10] + 2)) == _lib.SSM_ERR_MISALIGNED
+    assert scan_ex(lib, d, O(h0=P[8])) == _lib.SSM_ERR_ALIAS                  # h0 == y
+    assert scan_ex(lib, d, O(h0=P[9] + 64)) == _lib.SSM_ERR_ALIAS             # h0 straddles last_state
+    assert scan_ex(lib, d, O(conv_width=4, conv_weight=P[11], u_out=P[8])) == _lib.SSM_ERR_ALIAS
+    assert scan_ex(lib, d, O(conv_width=4, conv_weight=P[11], u_out=P[1])) == _lib.SSM_ERR_ALIAS
+    assert scan_ex(lib, d, O(conv_width=4, conv_weight=P[11] + 1)) == _lib.SSM_ERR_MISALIGNED
+    # the workspace is still checked (these options are all valid)
+    ok = O(input_term=_lib.SSM_INPUT_ZOH, conv_width=4, conv_weight=P[11], h0=P[9])
+    assert scan_ex(lib, d, ok) == _lib.SSM_ERR_WORKSPACE
