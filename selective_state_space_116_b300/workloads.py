@@ -27,6 +27,11 @@ Workloads, named after the Mamba layer sizes they imitate:
   delta~N(-3,1) with softplus, no bias; A=-exp(U(0,1.5)); B,C,D~N(0,1).
 * ``gen``   generation: 128 x 5120, N=16, one token per step, bf16 x/delta/
   z/B/C, fp32 state, bias~U(-4,-2) with softplus, A_n=-(n+1), D~N(0,1).
+
+The selective-copying experiment of "Mamba remembers by forgetting, read
+closely" (interactiveml.org) has its own generator, ``selective_copy_inputs``:
+a target scalar followed by Gaussian distractors, with a fixed or a
+selective step size.
 """
 from __future__ import annotations
 
@@ -164,4 +169,41 @@ def steps_as_scan(inp: dict) -> dict:
         "A": inp["A"], "B": tr(inp["B"], (1, 0, 2)), "C": tr(inp["C"], (1, 0, 2)),
         "D": inp["D"], "z": tr(inp["z"], (1, 2, 0)), "delta_bias": inp["delta_bias"],
         "delta_softplus": inp["delta_softplus"],
+    }
+
+
+# The step sizes of the selective-copying experiment: one fixed step for every
+# item, or a large step on the target and a tiny one on the distractors
+# ("Mamba remembers by forgetting, read closely", interactiveml.org, the
+# selective-copying paragraphs).
+COPY_FIXED_DELTA = 0.25
+COPY_TARGET_DELTA = 6.0
+COPY_NOISE_DELTA = 0.002
+
+
+def selective_copy_inputs(gap: int, n_seq: int = 400, seed: int = 0, selective: bool = True) -> dict:
+    """Host tensors for the selective-copying experiment at one gap.
+
+    Each of the ``n_seq`` independently drawn sequences is one channel: token 0
+    is the target x_0 ~ N(0, 1), tokens 1..gap are distractors ~ N(0, 1).  The
+    scan is the page's scalar recurrence (N = 1, A = -1, B = C = 1, no skip
+    term, no gate, Delta given directly), to be run with the exact zero-order
+    hold input term, so that y[0, d, t] is the state after token t and
+    y[0, d, gap] is what the memory holds when the target is recalled.
+    Delta is 0.25 everywhere (fixed), or 6 on the target and 0.002 on the
+    distractors (selective).  The same seed gives the same sequences in both
+    settings.  Returns the scan inputs plus ``target`` (n_seq,).
+    """
+    rng = np.random.default_rng(seed)
+    L = gap + 1
+    x = _normal(rng, (1, n_seq, L))
+    delta = np.full((1, n_seq, L), COPY_NOISE_DELTA if selective else COPY_FIXED_DELTA,
+                    dtype=np.float32)
+    if selective:
+        delta[..., 0] = COPY_TARGET_DELTA
+    return {
+        "u": torch.from_numpy(x), "delta": torch.from_numpy(delta),
+        "A": torch.full((n_seq, 1), -1.0), "B": torch.ones(1, L, 1), "C": torch.ones(1, L, 1),
+        "D": None, "z": None, "delta_bias": None, "delta_softplus": False,
+        "target": torch.from_numpy(x[0, :, 0].copy()),
     }

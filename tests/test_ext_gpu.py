@@ -316,3 +316,53 @@ def test_conv_with_unit_tap_is_silu_of_input():
     y2, h2 = gpu_ex(plain)
     assert_close(as64(y), as64(y2), torch.float32, "fused vs unfused")
     assert_close(as64(h), as64(h2), torch.float32, "fused vs unfused state")
+
+
+# -- the configured workload shapes -------------------------------------------------
+def _subset(inp, chans):
+    """The sub-problem of the listed channels of batch row 0 (batch = 1)."""
+    sub = dict(inp)
+    idx = torch.from_numpy(np.asarray(chans))
+    for key in ("u", "delta", "z"):
+        if inp[key] is not None:
+            sub[key] = inp[key][:, idx].contiguous()
+    sub["A"] = inp["A"][idx].contiguous()
+    for key in ("D", "delta_bias"):
+        if inp[key] is not None:
+            sub[key] = inp[key][idx].contiguous()
+    return sub
+
+
+@pytest.mark.parametrize("name", ["tiny", "m130", "m2p8", "dna"])
+@pytest.mark.parametrize("variant", ["zoh_h0", "conv"])
+def test_options_on_workload_shapes(name, variant):
+    """The exact zero-order hold (with an initial state) and the fused
+    convolution at every scan workload's full size; the long DNA-like
+    sequence (the chunked schedule) on 64 sampled channels."""
+    from selective_state_space_116_b300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    inp = make_scan_inputs(w, seed=60)
+    if variant == "zoh_h0":
+        h0 = random_h0(w, 5)
+        opts = dict(input_term="zoh", h0=h0)
+    else:
+        cw, cb, _ = conv_params(w, 4, 10)
+        opts = dict(conv_weight=cw, conv_bias=cb)
+    y, h = gpu_ex(inp, **opts)
+    if name == "dna":
+        chans = np.array(sorted({0, w.dim - 1} | set(np.random.default_rng(3).choice(
+            w.dim, 70, replace=False).tolist())))[:64]
+        sub = _subset(inp, chans)
+        idx = torch.from_numpy(chans).cuda()
+        y, h = y[:, idx], h[:, idx]
+    else:
+        sub = inp
+    if variant == "zoh_h0":
+        h0s = h0 if name != "dna" else h0[:, torch.from_numpy(chans)].contiguous()
+        y_ref, h_ref = oracle_ex(sub, zoh=True, h0=h0s)
+    else:
+        cws = cw if name != "dna" else cw[torch.from_numpy(chans)].contiguous()
+        cbs = cb if name != "dna" else cb[torch.from_numpy(chans)].contiguous()
+        y_ref, h_ref = oracle_ex(sub, u=oracle_conv(sub, cws, cbs, None))
+    assert_close(as64(y), y_ref, w.torch_io, f"{name} {variant} y")
+    assert_close(as64(h), h_ref, w.torch_io, f"{name} {variant} last_state")
