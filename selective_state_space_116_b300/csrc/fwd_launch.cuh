@@ -35,8 +35,9 @@ int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int
     if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     const int64_t ga = units < (int64_t)oa * sms ? units : (int64_t)oa * sms;
     agg<<<(unsigned)ga, kThreads, Sh::SMEM, stream>>>(p);
-    const int64_t nthr = p.ngroups * Sh::CH * N;
-    scan_chunk_carry_kernel<N, Sh::CH><<<(unsigned)((nthr + 255) / 256), 256, 0, stream>>>(p);
+    const int64_t nseq = p.ngroups * Sh::CH * N;   // one CTA per (group, channel, state)
+    if (nseq > INT32_MAX) return SSM_ERR_BAD_DIMS;
+    scan_chunk_carry_kernel<N, Sh::CH><<<(unsigned)nseq, kCarryThreads, 0, stream>>>(p);
     const int64_t gf = units < (int64_t)of * sms ? units : (int64_t)of * sms;
     full<<<(unsigned)gf, kThreads, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -987,9 +987,9 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
 //   pass 1  every (group, chunk) unit scans its chunk from a zero state: the
 //           final state is the chunk's b; its a is exp(A sum Delta)
 //           (scan_chunk_agg_kernel)
-//   pass 2  per (channel, state) a sequential scan over the chunks composes
-//           them into each chunk's carry-in, starting from the initial state
-//           (scan_chunk_carry_kernel)
+//   pass 2  per (channel, state) an exclusive scan of the chunks' maps under
+//           composition (lanes, warps, tiles of chunks) gives each chunk's
+//           carry-in from the initial state (scan_chunk_carry_kernel)
 //   pass 3  every unit scans its chunk again from its carry-in and writes y
 //           and, for the last chunk, last_state (scan_fwd_kernel with
 //           p.nchunks > 0).
@@ -1011,26 +1011,72 @@ __global__ void __launch_bounds__(kThreads, 2) scan_chunk_agg_kernel(ScanParams 
     }
 }
 
-// Pass 2: one thread per (group, channel, state) walks the chunks in order,
-// replacing each chunk's aggregate state by its carry-in.
+// Pass 2: the carry-in of every chunk, as an exclusive scan of the chunks'
+// affine maps under composition.  Chunk k maps the state entering it to the
+// state leaving it: h -> a_k h + b_k, with a_k = exp(A sum of Delta over the
+// chunk) and b_k its state from zero (pass 1).  Composition
+// (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) is associative ("Mamba remembers
+// by forgetting, read closely", interactiveml.org: the compose operator and
+// its associativity; "Mamba", sghael.github.io, "Training without stepping
+// token by token": updates combined in pairs, then pairs of pairs), so one
+// CTA per (group, channel, state) sequence scans it in tiles of kCarryThreads
+// chunks: lanes combine with __shfl_up_sync (log2 32 rounds), warps through
+// shared memory, and each tile starts from the previous tiles' total.  The
+// carry-in of chunk k is the composition of chunks 0 .. k-1 applied to the
+// initial state; it overwrites the chunk's aggregate.
+constexpr int kCarryThreads = 256;
+
+struct Affine {
+    float a, b;
+};
+// (later) o (earlier)
+__device__ __forceinline__ Affine compose(Affine later, Affine earlier) {
+    return Affine{later.a * earlier.a, fmaf(later.a, earlier.b, later.b)};
+}
+
 template <int N, int CH>
-__global__ void scan_chunk_carry_kernel(ScanParams p) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= p.ngroups * CH * N) return;
-    const int64_t grp = idx / (CH * N);
-    const int rem = (int)(idx % (CH * N)), ch = rem / N, n = rem % N;
+__global__ void __launch_bounds__(kCarryThreads) scan_chunk_carry_kernel(ScanParams p) {
+    constexpr int kWarps = kCarryThreads / 32;
+    __shared__ Affine s_warp[kWarps];
+    const int64_t seq = blockIdx.x;                   // (group, channel, state)
+    const int64_t grp = seq / (CH * N);
+    const int rem = (int)(seq % (CH * N)), ch = rem / N, n = rem % N;
     const int64_t b = grp / p.groups_per_row;
     const int64_t d = (grp % p.groups_per_row) * CH + ch;
     const bool in = d < p.dim;
     const float A2 = in ? p.A[d * N + n] * kLog2e : 0.0f;
-    float carry = (in && p.h0) ? p.h0[(b * p.dim + d) * N + n] : 0.0f;
-    for (int64_t ck = 0; ck < p.nchunks; ck++) {
+    const float h0 = (in && p.h0) ? p.h0[(b * p.dim + d) * N + n] : 0.0f;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    Affine carry{1.0f, 0.0f};                         // the chunks of earlier tiles
+    for (int64_t base = 0; base < p.nchunks; base += kCarryThreads) {
+        const int64_t ck = base + threadIdx.x;
+        const bool live = ck < p.nchunks;
         const int64_t u = grp * p.nchunks + ck;
         float* st = p.agg + (u * CH + ch) * N + n;
-        const float bk = *st;                          // the chunk's state from zero
-        const float a = ex2(A2 * p.dsum[u * CH + ch]);   // prod of exp(Delta A) over the chunk
-        *st = carry;                                   // the state entering the chunk
-        carry = fmaf(a, carry, bk);
+        // this chunk's map (the identity past the last chunk)
+        Affine x{1.0f, 0.0f};
+        if (live) x = Affine{ex2(A2 * p.dsum[u * CH + ch]), *st};
+        // inclusive scan over the warp's lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float pa = __shfl_up_sync(0xffffffffu, x.a, off);
+            const float pb = __shfl_up_sync(0xffffffffu, x.b, off);
+            if (lane >= off) x = compose(x, Affine{pa, pb});
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        // the warps before this one, then the earlier tiles
+        Affine before = carry;
+        for (int w = 0; w < warp; w++) before = compose(s_warp[w], before);
+        // exclusive: the lane before's inclusive map, or the warp's prefix
+        const float ea = __shfl_up_sync(0xffffffffu, x.a, 1);
+        const float eb = __shfl_up_sync(0xffffffffu, x.b, 1);
+        const Affine excl = lane == 0 ? before : compose(Affine{ea, eb}, before);
+        if (live) *st = fmaf(excl.a, h0, excl.b);     // the state entering chunk ck
+        Affine total = carry;
+        for (int w = 0; w < kWarps; w++) total = compose(s_warp[w], total);
+        carry = total;
+        __syncthreads();                              // s_warp is reused by the next tile
     }
 }
 

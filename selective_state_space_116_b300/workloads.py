@@ -109,7 +109,7 @@ def make_scan_inputs(w: Workload, seed: int = 0) -> dict:
         gain = rng.standard_normal(size=d, dtype=np.float32)
         hit = sym[None, :] == (np.arange(d) % 4)[:, None]            # (d, L)
         u = np.where(hit, gain[:, None], np.float32(0.0)).astype(np.float32)[None]
-        u = np.ascontiguousarray(np.broadcast_to(u, (b, d, L)))
+        u = np.broadcast_to(u, (b, d, L)).copy()
     else:
         u = _normal(rng, (b, d, L))
     delta = _normal(rng, (b, d, L), w.delta_mean)
