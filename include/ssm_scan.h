@@ -86,7 +86,8 @@ typedef enum ssm_status {
     SSM_ERR_ALIAS = -8,         /* an output overlaps an input */
     SSM_ERR_TIMEOUT = -9,       /* a bounded on-device wait gave up */
     SSM_ERR_TOO_LARGE = -10,    /* needs more scratch than ssm_scan_fwd_noalloc holds */
-    SSM_ERR_BAD_OPTION = -11    /* a field of ssm_scan_opts is out of range */
+    SSM_ERR_BAD_OPTION = -11,   /* a field of ssm_scan_opts is out of range */
+    SSM_ERR_DEVICE = -12        /* a -DSSM_DEBUG build's bounds check failed on the device */
 } ssm_status;
 
 typedef enum ssm_io_dtype { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
@@ -138,9 +139,9 @@ typedef struct ssm_dims {
  *                  separate workspaces.  The scan splits the token range of
  *                  some channel groups between two CTAs and hands the state
  *                  over through the workspace; that hand-over waits at most
- *                  about a second.  When the work has finished, the first
- *                  int32 of the workspace is SSM_OK, or SSM_ERR_TIMEOUT if a
- *                  hand-over gave up (the affected outputs are then NaN).
+ *                  about a second.  ssm_scan_fwd_status reports the outcome
+ *                  (SSM_OK, or SSM_ERR_TIMEOUT if a hand-over gave up; the
+ *                  affected outputs are then NaN).
  *   stream         cudaStream_t to enqueue on (NULL: the legacy default stream)
  *
  * Pointers of the I/O type must be aligned to the element size; the library
@@ -193,6 +194,16 @@ typedef struct ssm_scan_opts {
     /* (batch, dim, seqlen) I/O type output: the convolution's output u'
      * (rounded to the I/O type), or NULL to skip writing it. */
     void* u_out;
+    /* Polls (about 256 ns apart) a CTA makes for the state handed over by the
+     * CTA before it before giving up with SSM_ERR_TIMEOUT; 0: the default,
+     * 2^22 (about a second).  Must be >= 0. */
+    int32_t wait_limit;
+    /* Test hook, 0 in normal use: nonzero makes every CTA withhold the flag
+     * that publishes its hand-over, so that a CTA waiting for one gives up
+     * after wait_limit polls, writes NaN to the outputs of the channels it
+     * could not finish and leaves SSM_ERR_TIMEOUT for ssm_scan_fwd_status.
+     * Nothing faults or hangs; the device stays usable. */
+    int32_t test_skip_handoff;
 } ssm_scan_opts;
 
 /*
@@ -209,6 +220,19 @@ SSM_API int ssm_scan_fwd_ex(const ssm_dims* dims, const ssm_scan_opts* opts,
                  void* y, float* last_state,
                  void* workspace, size_t workspace_bytes,
                  void* stream);
+
+/*
+ * The device-side outcome of the last ssm_scan_fwd / ssm_scan_fwd_ex call
+ * that used `workspace` (workspace_bytes as passed to it).  Blocks: it
+ * synchronises `stream` (the call's stream), then reads the workspace's
+ * header.  Returns SSM_OK; SSM_ERR_TIMEOUT if a bounded hand-over wait gave
+ * up (the outputs of the affected channels are NaN); SSM_ERR_DEVICE if a
+ * -DSSM_DEBUG build's bounds check failed (that access was skipped); or
+ * SSM_ERR_CUDA if the synchronisation or the copy failed.  A call whose
+ * workspace size is 0 runs no bounded wait: pass workspace = NULL and
+ * get SSM_OK.
+ */
+SSM_API int ssm_scan_fwd_status(const void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace ssm_scan_fwd needs for these sizes (may be 0).
  * Returns SSM_OK or a negative ssm_status (bad dims). */
@@ -307,8 +331,8 @@ SSM_API int ssm_scan_fwd_host(const ssm_dims* dims,
  * whose work overlaps on the GPU (different streams, or host threads racing)
  * race on it and give wrong results, so serialise them, e.g. on one stream.
  * The call clears the part of the buffer that must start at zero, on
- * `stream`, before the scan reads it; the status word left there is not
- * readable from the host.  Arguments, outputs and errors are otherwise those
+ * `stream`, before the scan reads it; ssm_scan_fwd_noalloc_status reads the
+ * status it leaves there.  Arguments, outputs and errors are otherwise those
  * of ssm_scan_fwd.
  */
 SSM_API int ssm_scan_fwd_noalloc(const ssm_dims* dims,
@@ -319,6 +343,11 @@ SSM_API int ssm_scan_fwd_noalloc(const ssm_dims* dims,
 
 /* Size in bytes of ssm_scan_fwd_noalloc's built-in scratch buffer. */
 SSM_API size_t ssm_scan_fwd_noalloc_max_scratch(void);
+
+/* ssm_scan_fwd_status for the last ssm_scan_fwd_noalloc call on the current
+ * device (whose status lives in the built-in buffer): synchronises `stream`,
+ * then reads it.  Allocates nothing. */
+SSM_API int ssm_scan_fwd_noalloc_status(void* stream);
 
 /*
  * One token of recurrent (generation) mode: the same update with L = 1,

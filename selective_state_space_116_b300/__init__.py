@@ -19,7 +19,7 @@ import torch
 from . import _lib
 from ._lib import SSMError, ssm_dims
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "selective_scan", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
+__all__ = ["ssm_scan_fwd", "scan_status", "ssm_scan_bwd", "selective_scan", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
            "library_path", "version"]
 
 _IO = {torch.float32: _lib.SSM_IO_F32, torch.bfloat16: _lib.SSM_IO_BF16}
@@ -120,7 +120,8 @@ def _scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_l
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
                  return_last_state=True, y=None, last_state=None, workspace=None, chunk=0,
                  input_term="delta_b", h0=None, conv_weight=None, conv_bias=None,
-                 conv_state=None, u_out=None):
+                 conv_state=None, u_out=None, check=False, wait_limit=0,
+                 _test_skip_handoff=False):
     """Forward selective scan.
 
     u, delta, z: (batch, dim, L); B, C: (batch, L, N), all fp32 or all bf16.
@@ -134,9 +135,18 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     ``conv_weight``: (dim, K) fp32, K <= 4 -- then ``u`` is the input x of the
     fused short convolution u' = silu(conv(x) + conv_bias) and the scan runs
     on u'; ``conv_bias``: (dim,) fp32; ``conv_state``: (batch, dim, K - 1)
-    inputs before token 0; ``u_out``: (batch, dim, L) tensor to receive u'.
+    inputs before token 0; ``u_out``: (batch, dim, L) tensor to receive u';
+    ``wait_limit``: polls of a bounded hand-over wait (0: about a second).
+
+    ``check``: wait for the scan and raise SSMError if the device reported a
+    failure (a bounded wait that gave up: the affected outputs are NaN; a
+    failed bounds check of a debug build).  Without it the call returns as
+    soon as the work is enqueued; ``scan_status(workspace)`` reads the same
+    outcome later.  ``_test_skip_handoff`` is a test hook (see
+    ssm_scan_opts.test_skip_handoff).
     """
-    opts = input_term != "delta_b" or h0 is not None or conv_weight is not None
+    opts = (input_term != "delta_b" or h0 is not None or conv_weight is not None or
+            wait_limit != 0 or _test_skip_handoff)
     if u.device.type == "cpu":
         if opts:
             raise ValueError("scan options take CUDA tensors")
@@ -184,6 +194,8 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
         rc = lib.ssm_scan_fwd(ctypes.byref(d), *args)
         if rc != 0:
             raise SSMError(rc, "ssm_scan_fwd")
+        if check:
+            scan_status(workspace, raise_on_error=True)
         return y, (last_state if return_last_state else None)
     if input_term not in ("delta_b", "zoh"):
         raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
@@ -204,10 +216,30 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
         o.conv_state, o.u_out = _ptr(conv_state), _ptr(u_out)
     elif conv_bias is not None or conv_state is not None or u_out is not None:
         raise ValueError("conv_bias, conv_state and u_out need conv_weight")
+    o.wait_limit = int(wait_limit)
+    o.test_skip_handoff = 1 if _test_skip_handoff else 0
     rc = lib.ssm_scan_fwd_ex(ctypes.byref(d), ctypes.byref(o), *args)
     if rc != 0:
         raise SSMError(rc, "ssm_scan_fwd_ex")
+    if check:
+        scan_status(workspace, raise_on_error=True)
     return y, (last_state if return_last_state else None)
+
+
+def scan_status(workspace, raise_on_error=False) -> int:
+    """The device-side outcome of the last scan that used ``workspace`` (a
+    CUDA uint8 tensor, or None for a scan that needed none): waits for the
+    current stream, then returns 0 or a negative status (SSM_ERR_TIMEOUT,
+    SSM_ERR_DEVICE), raising SSMError instead when ``raise_on_error``."""
+    lib = _lib.load()
+    if workspace is None:
+        rc = 0
+    else:
+        rc = lib.ssm_scan_fwd_status(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(workspace.device))
+    if rc != 0 and raise_on_error:
+        raise SSMError(rc, "scan on the device")
+    return rc
 
 
 def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,

@@ -9,7 +9,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIBRARY = os.path.join(HERE, "libssm_scan.so")
+# The library built in-tree.  SSM_SCAN_LIBRARY may name another build of the
+# same sources, e.g. the -DSSM_DEBUG build (build.build(debug=True)).
+LIBRARY = os.environ.get("SSM_SCAN_LIBRARY") or os.path.join(HERE, "libssm_scan.so")
 
 # ssm_status codes (include/ssm_scan.h)
 SSM_OK = 0
@@ -24,6 +26,7 @@ SSM_ERR_ALIAS = -8
 SSM_ERR_TIMEOUT = -9
 SSM_ERR_TOO_LARGE = -10
 SSM_ERR_BAD_OPTION = -11
+SSM_ERR_DEVICE = -12
 
 SSM_INPUT_DELTA_B = 0
 SSM_INPUT_ZOH = 1
@@ -34,7 +37,8 @@ SSM_IO_BF16 = 1
 # every symbol include/ssm_scan.h declares
 EXPORTS = ("ssm_build_id", "ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_ex", "ssm_scan_fwd_host", "ssm_scan_fwd_noalloc",
-           "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_workspace_size", "ssm_state_step",
+           "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_noalloc_status",
+           "ssm_scan_fwd_status", "ssm_scan_fwd_workspace_size", "ssm_state_step",
            "ssm_status_string", "ssm_version")
 
 
@@ -48,7 +52,8 @@ class ssm_scan_opts(ctypes.Structure):
     _fields_ = [("input_term", ctypes.c_int32), ("conv_width", ctypes.c_int32),
                 ("h0", ctypes.c_void_p), ("conv_weight", ctypes.c_void_p),
                 ("conv_bias", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
-                ("u_out", ctypes.c_void_p)]
+                ("u_out", ctypes.c_void_p), ("wait_limit", ctypes.c_int32),
+                ("test_skip_handoff", ctypes.c_int32)]
 
 
 class SSMError(RuntimeError):
@@ -77,6 +82,10 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     lib.ssm_scan_fwd_ex.restype = i32
     lib.ssm_scan_fwd_ex.argtypes = [dims_p, ctypes.POINTER(ssm_scan_opts), vp, vp, vp, vp, vp, vp,
                                     vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.ssm_scan_fwd_status.restype = i32
+    lib.ssm_scan_fwd_status.argtypes = [vp, sz, vp]
+    lib.ssm_scan_fwd_noalloc_status.restype = i32
+    lib.ssm_scan_fwd_noalloc_status.argtypes = [vp]
     lib.ssm_scan_bwd.restype = i32
     lib.ssm_scan_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]

@@ -68,12 +68,21 @@ def built_id(path: str = LIBRARY):
     return out.stdout.strip() or None if out.returncode == 0 else None
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=(), jobs: int = 0) -> str:
+DEBUG_LIBRARY = os.path.join(HERE, "libssm_scan_debug.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), jobs: int = 0,
+          debug: bool = False) -> str:
     """Compile the library unless the one on disk was built from these exact
-    sources and flags; return its path."""
+    sources and flags; return its path.  debug: the -DSSM_DEBUG build (device
+    bounds checks recorded in the workspace header, see ssm_scan_fwd_status)
+    into libssm_scan_debug.so, for SSM_SCAN_LIBRARY."""
+    library = DEBUG_LIBRARY if debug else LIBRARY
+    if debug:
+        extra_flags = (*extra_flags, "-DSSM_DEBUG")
     want = source_hash(extra_flags)
-    if not force and built_id() == want:
-        return LIBRARY
+    if not force and built_id(library) == want:
+        return library
     nvcc = os.environ.get("NVCC", "nvcc")
     tmpdir = tempfile.mkdtemp(prefix="ssm_build_")
     try:
@@ -95,16 +104,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), jobs: int 
         n = jobs or max(1, min(len(sources()), os.cpu_count() or 1))
         with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
             objs = list(ex.map(compile_one, sources()))
-        tmp = LIBRARY + f".tmp{os.getpid()}"
+        tmp = library + f".tmp{os.getpid()}"
         cmd = [nvcc, *LINK_FLAGS, "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIBRARY)
+        os.replace(tmp, library)
     finally:
         shutil.rmtree(tmpdir, ignore_errors=True)
-    return LIBRARY
+    return library
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

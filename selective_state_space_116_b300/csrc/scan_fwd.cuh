@@ -66,8 +66,11 @@ struct ScanParams {
     int64_t groups_per_row;   // ceil(dim / channels per CTA)
     int64_t ngroups;          // batch * groups_per_row
     int64_t ntiles;           // ceil(L / tile)
-    // workspace: status word, one flag per group, one carried state per group
+    // workspace: a header of int32 words (kHdr*), one flag per group, one
+    // carried state per group
     int* status;
+    long wait_limit;          // spin iterations of a bounded wait (~256 ns each)
+    int skip_handoff;         // test hook: no CTA publishes its hand-over
     unsigned* flags;
     float* carry;
     // chunked (L-parallel) schedule: chunks of tiles_per_chunk tiles; per
@@ -88,9 +91,28 @@ struct PartIO {
     bool handoff;        // a part ending inside its group hands the state on (flag + carry)
 };
 
-// Value a kernel leaves in the workspace status word when a bounded wait
-// gives up (the ABI's SSM_ERR_TIMEOUT).
+// The workspace header (int32 words): the status a bounded wait that gave up
+// leaves (kStatusTimeout, the ABI's SSM_ERR_TIMEOUT), the ticket counter that
+// orders the persistent CTAs, and, in -DSSM_DEBUG builds, the first failed
+// bounds check (kStatusDevice, the ABI's SSM_ERR_DEVICE) and its site.
+constexpr int kHdrStatus = 0, kHdrTicket = 1, kHdrDebug = 2, kHdrDebugSite = 3;
 constexpr int kStatusTimeout = -9;
+constexpr int kStatusDevice = -12;
+
+// Bounds checks of the -DSSM_DEBUG build: a failed check records the site in
+// the workspace header and skips the access (no trap, no abort); release
+// builds compile them away.
+#ifdef SSM_DEBUG
+__device__ __forceinline__ bool debug_ok(bool ok, int* hdr, int site) {
+    if (!ok && hdr) {
+        if (atomicCAS(hdr + kHdrDebug, 0, kStatusDevice) == 0) atomicExch(hdr + kHdrDebugSite, site);
+    }
+    return ok;
+}
+#define SSM_INBOUNDS(cond, hdr, site) ::ssm::debug_ok((cond), (hdr), (site))
+#else
+#define SSM_INBOUNDS(cond, hdr, site) true
+#endif
 
 namespace seq {
 
@@ -217,7 +239,8 @@ template <> __device__ __forceinline__ float2 silu2<__nv_bfloat16>(float2 z) {
 // is either wholly inside or wholly outside the tensor.
 template <typename T, int CH, int RAW_ROW, bool VEC>
 __device__ __forceinline__ void load_plane(unsigned char* plane, const T* g, int64_t row0,
-                                           int rows, int64_t L, int64_t t0) {
+                                           int rows, int64_t L, int64_t t0,
+                                           int64_t nrows_total, int* hdr) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int CPR = kTL / EPC;  // chunks per row
     static_assert((CH * CPR) % kThreads == 0, "plane chunks must split evenly");
@@ -228,27 +251,33 @@ __device__ __forceinline__ void load_plane(unsigned char* plane, const T* g, int
         const int64_t t = t0 + (int64_t)c * EPC;
         unsigned char* dst = plane + r * RAW_ROW + c * 16;
         if constexpr (VEC) {
-            const bool ok = r < rows && t < L;
+            bool ok = r < rows && t < L;
+            if (ok) ok = SSM_INBOUNDS(row0 + r < nrows_total && t + EPC <= L, hdr, 1);
             cp_async16(dst, ok ? static_cast<const void*>(g + (row0 + r) * L + t) : g, ok ? 16 : 0);
         } else {
             T* d = reinterpret_cast<T*>(dst);
 #pragma unroll
-            for (int e = 0; e < EPC; e++)
-                d[e] = (r < rows && t + e < L) ? g[(row0 + r) * L + t + e] : io<T>::from_f32(0.0f);
+            for (int e = 0; e < EPC; e++) {
+                bool ok = r < rows && t + e < L;
+                if (ok) ok = SSM_INBOUNDS(row0 + r < nrows_total, hdr, 1);
+                d[e] = ok ? g[(row0 + r) * L + t + e] : io<T>::from_f32(0.0f);
+            }
         }
     }
 }
 
 // Copy tokens [t0, t0 + kTL) of one batch row of B or C (contiguous kTL*N run).
 template <typename T, int N, bool VEC>
-__device__ __forceinline__ void load_bc(unsigned char* dst, const T* g, int64_t L, int64_t t0) {
+__device__ __forceinline__ void load_bc(unsigned char* dst, const T* g, int64_t L, int64_t t0,
+                                        int* hdr) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int CHUNKS = kTL * N / EPC;
     const int64_t valid = (L - t0) * N;  // elements of this tile inside the tensor
     for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
         const int64_t e0 = (int64_t)i * EPC;
         if constexpr (VEC) {
-            const bool ok = e0 < valid;
+            bool ok = e0 < valid;
+            if (ok) ok = SSM_INBOUNDS(e0 + EPC <= valid && t0 >= 0, hdr, 2);
             cp_async16(dst + i * 16, ok ? static_cast<const void*>(g + t0 * N + e0) : g, ok ? 16 : 0);
         } else {
             T* d = reinterpret_cast<T*>(dst + i * 16);
@@ -554,10 +583,10 @@ __device__ __forceinline__ float2 softplus2_log2(float2 x, bool series) {
 }
 
 // Bounded wait for the carry of `group` (set by the CTA that scanned the
-// group's earlier tokens).  Returns false if the wait gave up.
-__device__ __forceinline__ bool wait_flag(const unsigned* flag) {
-    constexpr long kSpinLimit = 1l << 22;   // ~1 s with the back-off below
-    for (long it = 0; it < kSpinLimit; it++) {
+// group's earlier tokens): at most `limit` polls, 256 ns apart (the library
+// passes 2^22, about a second).  Returns false if the wait gave up.
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, long limit) {
+    for (long it = 0; it < limit; it++) {
         unsigned v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
         if (v) return true;
@@ -628,16 +657,20 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         }
     }
 
+    int* const hdr = p.status;             // workspace header (debug checks)
+    const int64_t nrows = p.batch * p.dim;
+    (void)hdr;
+    (void)nrows;
     auto load_tile = [&](int64_t tile, int slot) {
         unsigned char* buf = smem + slot * Sh::RAW_BUF;
         const int64_t t0 = tile * kTL;
-        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0);
-        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0);
+        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0, nrows, hdr);
+        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0, nrows, hdr);
         if (gate && !AGG)
-            load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0);
+            load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0, nrows, hdr);
         unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
-        load_bc<T, N, VEC>(bcraw, gB, L, t0);
-        load_bc<T, N, VEC>(bcraw + Sh::BC_RAW, gC, L, t0);
+        load_bc<T, N, VEC>(bcraw, gB, L, t0, hdr);
+        load_bc<T, N, VEC>(bcraw + Sh::BC_RAW, gC, L, t0, hdr);
     };
 
     // the first tile's copies overlap the wait for the carry
@@ -670,12 +703,13 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         for (int j = 0; j < S; j++) h[j] = 0.0f;
     } else if (part.init == 2 || part.init == 3) {
         const float* src = (part.init == 2 ? part.h0 + ch * N : p.h0 + (row0 + ch) * N) + g * S;
+        const bool ok = active && (part.init == 2 || SSM_INBOUNDS(row0 + ch < nrows, hdr, 3));
 #pragma unroll
-        for (int j = 0; j < S; j++) h[j] = active ? __ldcg(src + j) : 0.0f;
+        for (int j = 0; j < S; j++) h[j] = ok ? __ldcg(src + j) : 0.0f;
     } else {
         if (threadIdx.x == 0) {
-            const bool ok = wait_flag(p.flags + grp);
-            if (!ok) atomicExch(p.status, kStatusTimeout);
+            const bool ok = wait_flag(p.flags + grp, p.wait_limit);
+            if (!ok) atomicExch(p.status + kHdrStatus, kStatusTimeout);
             __threadfence();
             *s_ok = ok;
         }
@@ -737,7 +771,8 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
                 float4* us = reinterpret_cast<float4*>(smem + Sh::OFF_U + r * Sh::U_ROW + q * 32);
                 us[0] = make_float4(uv[0], uv[1], uv[2], uv[3]);
                 us[1] = make_float4(uv[4], uv[5], uv[6], uv[7]);
-                if (!AGG && p.u_out && r < rows && q * 8 < tvalid) {
+                if (!AGG && p.u_out && r < rows && q * 8 < tvalid &&
+                    SSM_INBOUNDS(row0 + r < nrows && t0 + q * 8 < L, hdr, 5)) {
                     T* dst = static_cast<T*>(p.u_out) + (row0 + r) * L + t0 + q * 8;
                     if (VEC && q * 8 + 8 <= tvalid) store8<T>(dst, uv);
                     else store_first<T>(dst, uv, tvalid - q * 8);
@@ -895,7 +930,8 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             float ys[8];
 #pragma unroll
             for (int e = 0; e < 4; e++) { ys[2 * e] = y2[e].x; ys[2 * e + 1] = y2[e].y; }
-            if (r < rows && q * 8 < tvalid) {
+            if (r < rows && q * 8 < tvalid &&
+                SSM_INBOUNDS(row0 + r < nrows && t0 + q * 8 < L, hdr, 4)) {
                 T* dst = gy + (row0 + r) * L + t0 + q * 8;
                 if (VEC && q * 8 + 8 <= tvalid) store8<T>(dst, ys);
                 else store_first<T>(dst, ys, tvalid - q * 8);
@@ -910,7 +946,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         for (int j = 0; j < S; j++) dst[j] = h[j];
         if (g == 0) part.dsum[ch] = dsum;
     } else if (te == p.ntiles) {
-        if (active && p.last_state) {
+        if (active && p.last_state && SSM_INBOUNDS(row0 + ch < nrows, hdr, 6)) {
             float* dst = p.last_state + (row0 + ch) * N + g * S;
 #pragma unroll
             for (int j = 0; j < S; j++) dst[j] = h[j];
@@ -922,7 +958,9 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         for (int j = 0; j < S; j++) __stcg(dst + j, h[j]);
         __threadfence();
         __syncthreads();
-        if (threadIdx.x == 0)
+        // (the test hook withholds the flag: the successor's bounded wait
+        // then runs out and reports SSM_ERR_TIMEOUT)
+        if (threadIdx.x == 0 && !p.skip_handoff)
             asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + grp), "r"(1u) : "memory");
     }
 }
@@ -953,12 +991,23 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
         }
         return;
     }
+    // The CTA's place in the schedule is a ticket taken on arrival, not its
+    // block index: the CTA whose range precedes this one took its ticket
+    // earlier, so it is running, and it publishes the state this CTA may wait
+    // for without waiting itself (its first part starts at a group's first
+    // tile).  Block indices carry no such guarantee of dispatch order.
+    __shared__ int64_t s_ticket;
+    if (threadIdx.x == 0)
+        s_ticket = p.status ? (int64_t)atomicAdd(reinterpret_cast<unsigned*>(p.status + kHdrTicket), 1u)
+                            : (int64_t)blockIdx.x;
+    __syncthreads();
+    const int64_t c = s_ticket;
     const int64_t W = p.ngroups * p.ntiles;
-    const int64_t s = W * blockIdx.x / gridDim.x;
-    const int64_t e = W * (blockIdx.x + 1) / gridDim.x;
+    const int64_t s = W * c / gridDim.x;
+    const int64_t e = W * (c + 1) / gridDim.x;
     if (s >= e) {   // empty sequence (or more CTAs than tiles): only last_state remains
         if (p.ntiles == 0 && p.last_state) {
-            for (int64_t grp = blockIdx.x; grp < p.ngroups; grp += gridDim.x) {
+            for (int64_t grp = c; grp < p.ngroups; grp += gridDim.x) {
                 const int64_t b = grp / p.groups_per_row;
                 const int64_t d0 = (grp % p.groups_per_row) * Sh::CH;
                 const int rows = (int)(p.dim - d0 < Sh::CH ? p.dim - d0 : Sh::CH);

@@ -14,6 +14,9 @@
 
 using namespace ssm_host;
 
+static_assert(ssm::kStatusTimeout == SSM_ERR_TIMEOUT, "device and host timeout codes agree");
+static_assert(ssm::kStatusDevice == SSM_ERR_DEVICE, "device and host debug codes agree");
+
 namespace {
 
 using bf16 = __nv_bfloat16;
@@ -58,7 +61,7 @@ int scan_fwd_impl(const ssm_dims* dims, const ssm_scan_opts* opts, const void* u
     const ssm_scan_opts none{};
     const ssm_scan_opts& o = opts ? *opts : none;
     if (o.input_term != SSM_INPUT_DELTA_B && o.input_term != SSM_INPUT_ZOH) return SSM_ERR_BAD_OPTION;
-    if (o.conv_width < 0 || o.conv_width > 4) return SSM_ERR_BAD_OPTION;
+    if (o.conv_width < 0 || o.conv_width > 4 || o.wait_limit < 0) return SSM_ERR_BAD_OPTION;
     const bool conv = o.conv_width > 0;
     if (conv && !o.conv_weight) return SSM_ERR_NULL_ARG;
     // With L = 0 the (batch, dim, L) and (batch, L, N) tensors are empty and
@@ -117,6 +120,8 @@ int scan_fwd_impl(const ssm_dims* dims, const ssm_scan_opts* opts, const void* u
     p.gate = z != nullptr;
     p.softplus = delta_softplus != 0;
     p.h0 = o.h0;
+    p.wait_limit = o.wait_limit > 0 ? o.wait_limit : (1l << 22);
+    p.skip_handoff = o.test_skip_handoff != 0;
     if (conv) {
         p.conv_w = o.conv_weight;
         p.conv_b = o.conv_bias;
@@ -155,6 +160,7 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_ALIAS: return "an output buffer overlaps an input buffer";
         case SSM_ERR_TIMEOUT: return "a bounded on-device wait gave up";
         case SSM_ERR_BAD_OPTION: return "an option of ssm_scan_opts is out of range";
+        case SSM_ERR_DEVICE: return "a bounds check of the debug build failed on the device";
         case SSM_ERR_TOO_LARGE:
             return "the problem needs more scratch than the library's built-in buffer holds";
     }
@@ -184,6 +190,29 @@ int ssm_scan_fwd(const ssm_dims* dims, const void* u, const void* delta, const f
                  void* workspace, size_t workspace_bytes, void* stream) {
     return scan_fwd_impl(dims, nullptr, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y,
                          last_state, workspace, workspace_bytes, stream, 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The outcome the scan left in a workspace header (see ssm_scan_fwd_status).
+int read_status(const void* header, cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SSM_ERR_CUDA;
+    int32_t w[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(w, header, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
+    if (w[ssm::kHdrDebug] != 0) return SSM_ERR_DEVICE;
+    return w[ssm::kHdrStatus] == ssm::kStatusTimeout ? SSM_ERR_TIMEOUT : SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_fwd_status(const void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace) return SSM_OK;
+    if (workspace_bytes < 16 || !aligned(workspace, 256)) return SSM_ERR_WORKSPACE;
+    return read_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
 int ssm_scan_fwd_ex(const ssm_dims* dims, const ssm_scan_opts* opts, const void* u,
@@ -539,5 +568,12 @@ int ssm_scan_fwd_noalloc(const ssm_dims* dims, const void* u, const void* delta,
 }
 
 size_t ssm_scan_fwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+int ssm_scan_fwd_noalloc_status(void* stream) {
+    void* scratch = nullptr;
+    const int rs = noalloc_scratch(&scratch);
+    if (rs != SSM_OK) return rs;
+    return read_status(scratch, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

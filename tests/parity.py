@@ -30,7 +30,8 @@ def gpu_scan(inp: dict, chunk: int = 0, return_last_state: bool = True, **opts):
     g = to_cuda(inp)
     y, h = ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                             delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
-                            return_last_state=return_last_state, chunk=chunk, **opts)
+                            return_last_state=return_last_state, chunk=chunk, check=True,
+                            **opts)
     torch.cuda.synchronize()
     return y, h
 

@@ -33,7 +33,7 @@ def gpu_ex(inp, chunk=0, **opts):
     o = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in opts.items()}
     y, h = ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                             delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
-                            chunk=chunk, **o)
+                            chunk=chunk, check=True, **o)
     torch.cuda.synchronize()
     return y, h
 
