@@ -28,7 +28,6 @@ import hashlib
 import io as _io
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -45,8 +44,8 @@ from selective_state_space_116_b300.workloads import (WORKLOADS, make_scan_input
                                                       make_step_inputs)
 
 METRIC = "selective-scan GB/s and elements(B*D*L)/s at 1 B300; % of HBM/SFU roofline"
-# MUFU ex2 results per clock per SM on B300 (sm_103a), measured by the throughput
-# probe summarised in profiles/mufu_ex2_rate.md.
+# MUFU ex2 results per clock per SM on B300 (sm_103a), measured by the library's
+# ssm_probe_ex2 throughput probe (python bench.py --probe-only).
 EX2_PER_CLK_PER_SM = 32
 L2_BYTES = 126 * 1024 * 1024
 
@@ -62,6 +61,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the generation-step line")
+    p.add_argument("--only", choices=["step", "bwd", "conv", "zoh"], default=None,
+                   help="time one part alone and print its line (for profiling commands)")
     p.add_argument("--probe-only", action="store_true",
                    help="only measure the special-function unit's 2^x rate")
     return p.parse_args()
@@ -135,17 +136,17 @@ def kernel_source_hash() -> str:
 
 
 def committed_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"scan_fwd_{workload}_ncu.md")
+    """DRAM bytes per launch of the forward kernel at this workload, from the
+    ncu capture recorded in profiles/traffic.json, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
-    m_src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+    with open(path) as f:
+        rec = json.load(f).get(f"scan_fwd/{workload}")
+    if not rec or rec.get("kernel_source_sha256") != kernel_source_hash():
         return None
-    return float(m_tr.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 # --------------------------------------------------------------------------- clocks
@@ -268,10 +269,12 @@ def launches_per_scan(w) -> int:
     return 3 if groups < 64 and tiles >= 64 else 1
 
 
-def time_other(name, reps=20):
+def time_other(name, reps=20, variant=None):
     """Kernel time of one scan of another workload: `reps` scans captured in
     one CUDA graph (so that host-side call overhead, which dominates the tiny
-    workload, is not counted), L2 flushed before each scan."""
+    workload, is not counted), L2 flushed before each scan.  variant: None;
+    "conv" (the fused short convolution, width 4, on the block input x);
+    "zoh" (the exact zero-order-hold input term)."""
     import selective_state_space_116_b300 as ssm
     w = WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -281,13 +284,23 @@ def time_other(name, reps=20):
     last = torch.empty(w.batch, w.dim, w.dstate, device=dev) if w.last_state else None
     nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, g["u"].dtype)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    _, io_bytes, _ = scan_work(w)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
+    opts = {}
+    if variant == "conv":
+        gen = torch.Generator(device=dev).manual_seed(0)
+        opts = dict(conv_weight=torch.randn(w.dim, 4, device=dev, generator=gen) * 0.5,
+                    conv_bias=torch.randn(w.dim, device=dev, generator=gen) * 0.5)
+        io_bytes += w.dim * 5 * 4
+    elif variant == "zoh":
+        opts = dict(input_term="zoh")
 
     def scan():
         ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                          delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
-                         return_last_state=w.last_state, y=y, last_state=last, workspace=ws)
+                         return_last_state=w.last_state, y=y, last_state=last, workspace=ws,
+                         **opts)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -315,16 +328,53 @@ def time_other(name, reps=20):
     c.record(cur)
     torch.cuda.synchronize(dev)
     t = max(a.elapsed_time(b) - b.elapsed_time(c), 1e-6) * 1e-3 / reps
-    elems, io_bytes, exps = scan_work(w)
+    elems, _, exps = scan_work(w)
     pk = peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     t_sfu = exps / (EX2_PER_CLK_PER_SM * sms * pk["sm_max_mhz"] * 1e6)
     t_hbm = io_bytes / (pk["hbm_gbs"] * 1e9)
+    label = {None: "", "conv": ", fused short convolution (width 4) + SiLU prologue",
+             "zoh": ", exact zero-order-hold input term"}[variant]
+    del g, y, last, ws, flush
+    torch.cuda.empty_cache()
     return {"workload": f"{w.name}: batch={w.batch}, D={w.dim}, N={w.dstate}, L={w.seqlen}, "
-                        f"{w.io} I/O", "kernel_time_us": t * 1e6, "elements_per_s": elems / t,
+                        f"{w.io} I/O{label}", "kernel_time_us": t * 1e6, "elements_per_s": elems / t,
+            "bytes_per_launch": io_bytes, "exps_per_launch": exps,
             "roofline_time_us": max(t_sfu, t_hbm) * 1e6, "bound": "alu" if t_sfu >= t_hbm else "hbm",
             "frac": max(t_sfu, t_hbm) / t, "launches_per_scan": launches_per_scan(w),
             "timing": f"{reps} scans in a CUDA graph, L2 flushed before each; flush time subtracted"}
+
+
+def time_selective_copy(local, gap=1024, n_seq=400):
+    """The selective-copying experiment (a target scalar, then `gap` Gaussian
+    distractors; fixed step 0.25 against a selective 6 / 0.002) through the
+    scan with the exact zero-order-hold input term: the mean recall error of
+    each memory and the time of one scan of the 400 sequences."""
+    import selective_state_space_116_b300 as ssm
+    from selective_state_space_116_b300.workloads import selective_copy_inputs
+    dev = torch.device("cuda", local)
+    out = {"workload": f"selective copying: {n_seq} sequences, gap {gap}, N=1, A=-1, B=C=1, "
+                       "exact zero-order hold"}
+    for selective in (False, True):
+        inp = selective_copy_inputs(gap, n_seq=n_seq, seed=gap, selective=selective)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+        def scan():
+            return ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], input_term="zoh")
+        for _ in range(3):
+            y, _ = scan()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(20):
+            scan()
+        b.record()
+        torch.cuda.synchronize(dev)
+        key = "selective" if selective else "fixed"
+        out[f"recall_error_{key}"] = float((y[0, :, -1] - g["target"]).abs().mean().item())
+        out[f"us_per_scan_{key}"] = a.elapsed_time(b) * 1e3 / 20
+    out["timing"] = "20 calls through the Python binding, CUDA events (latency-bound: 400 x 1025 tokens)"
+    return out
 
 
 def time_e2e(w, inp, steps, warmup, local):
@@ -614,7 +664,11 @@ def run_ours(args, world, rank, local):
     if not args.no_step and rank == 0:
         out["state_step"] = time_state_step(local)
         out["scan_bwd"] = time_scan_bwd(w, local)
-        out["other_workloads"] = [time_other("m130"), time_other("tiny")]
+        out["other_workloads"] = [time_other("m130"), time_other("tiny"),
+                                  time_other("dna", reps=5),
+                                  time_other(args.workload, variant="conv"),
+                                  time_other(args.workload, variant="zoh")]
+        out["selective_copy"] = time_selective_copy(local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_rate(w, res["host_inputs"])
     if rank == 0:
@@ -627,6 +681,14 @@ def main():
     if args.probe_only:
         if rank == 0:
             print(json.dumps({"sfu_probe": probe_ex2(local)}), flush=True)
+    elif args.only:
+        if rank == 0:
+            w = WORKLOADS[args.workload]
+            part = {"step": lambda: time_state_step(local),
+                    "bwd": lambda: time_scan_bwd(w, local),
+                    "conv": lambda: time_other(args.workload, variant="conv"),
+                    "zoh": lambda: time_other(args.workload, variant="zoh")}[args.only]()
+            print(json.dumps({args.only: part}), flush=True)
     elif args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -8,7 +8,8 @@
 // any arithmetic, and the per-channel inputs (x, delta, z) and per-batch-row
 // B, C rows are loaded alongside.  The kG partial sums of C.h are combined
 // with warp shuffles inside the group; the group's first lane writes y.
-// VEC: the state rows are 16-byte aligned, so 4 entries move as one float4.
+// VEC: the state and A rows are 16-byte aligned, so 4 entries move as one
+// float4.
 #pragma once
 
 #include "common.cuh"
@@ -69,13 +70,24 @@ __device__ __forceinline__ void step_item(const StepParams& p, int64_t gid) {
     const T* Bb = static_cast<const T*>(p.B) + b * N + n0;
     const T* Cb = static_cast<const T*>(p.C) + b * N + n0;
     const float* Ad = p.A + d * N + n0;
-    // (scalar loads: 16-byte vector loads of these small rows measured slower)
+    // B and C rows: scalar loads (a warp's lanes read two rows, so each load
+    // is one broadcast); A rows differ per channel: 16-byte loads where the
+    // rows are aligned (a warp-wide scalar load of A touches 16 channels' rows)
     float Bv[kS], Cv[kS], Av[kS];
 #pragma unroll
     for (int k = 0; k < kS; k++) {
         Bv[k] = io<T>::load(Bb, k);
         Cv[k] = io<T>::load(Cb, k);
-        Av[k] = Ad[k];
+    }
+    if constexpr (VEC && kS % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < kS; k += 4) {
+            const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ad + k));
+            Av[k] = a4.x; Av[k + 1] = a4.y; Av[k + 2] = a4.z; Av[k + 3] = a4.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kS; k++) Av[k] = Ad[k];
     }
 
     const float v = dl + bias;
@@ -110,9 +122,19 @@ __device__ __forceinline__ void step_item(const StepParams& p, int64_t gid) {
 
 // One (channel, slice) item per thread.  (A persistent grid-stride variant
 // measured slower: it serialises each thread's items.)
+//
+// Launched with programmatic dependent launch: a token's step is scheduled
+// while the previous kernel on the stream (typically the previous token's
+// step) drains, and waits at griddepcontrol.wait until that kernel has
+// completed and its writes are visible, so the state it reads is the state
+// the previous step wrote.  Each CTA signals its own dependents once its
+// stores are issued.  Without a programmatic predecessor the wait returns at
+// once.
 template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool VEC>
 __global__ void __launch_bounds__(kStepThreads) state_step_kernel(StepParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     step_item<T, N, HAS_Z, SOFTPLUS, VEC>(p, (int64_t)blockIdx.x * kStepThreads + threadIdx.x);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace ssm

@@ -10,7 +10,18 @@ int launch_step(const ssm::StepParams& p, cudaStream_t stream) {
     const int64_t threads = p.batch * p.dim * kG;
     const int64_t blocks = (threads + ssm::kStepThreads - 1) / ssm::kStepThreads;
     if (blocks > INT32_MAX) return SSM_ERR_BAD_DIMS;
-    ssm::state_step_kernel<T, N, Z, SP, VEC><<<(unsigned)blocks, ssm::kStepThreads, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(ssm::kStepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see state_step_kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, ssm::state_step_kernel<T, N, Z, SP, VEC>, p) != cudaSuccess)
+        return SSM_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
