@@ -247,7 +247,7 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
     if (overlap(out_y, io_h)) return SSM_ERR_ALIAS;
 
     ssm::StepParams p{state, x, delta, A, B, C, D, z, delta_bias, y, dims->batch, dims->dim};
-    const bool vec = aligned(state, 16) && aligned(A, 16);
+    const bool vec = aligned(state, 16) && aligned(A, 16) && aligned(B, 16) && aligned(C, 16);
     const bool sp = delta_softplus != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int n = (int)dims->dstate;

@@ -74,10 +74,21 @@ __device__ __forceinline__ void step_item(const StepParams& p, int64_t gid) {
     // is one broadcast); A rows differ per channel: 16-byte loads where the
     // rows are aligned (a warp-wide scalar load of A touches 16 channels' rows)
     float Bv[kS], Cv[kS], Av[kS];
+    if constexpr (VEC && kS == 8 && sizeof(T) == 2) {   // one 16-byte load per row
+        const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(Bb));
+        const uint4 c4 = __ldg(reinterpret_cast<const uint4*>(Cb));
+        const unsigned bw[4] = {b4.x, b4.y, b4.z, b4.w}, cw[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-    for (int k = 0; k < kS; k++) {
-        Bv[k] = io<T>::load(Bb, k);
-        Cv[k] = io<T>::load(Cb, k);
+        for (int k = 0; k < 4; k++) {
+            Bv[2 * k] = __uint_as_float(bw[k] << 16); Bv[2 * k + 1] = __uint_as_float(bw[k] & 0xffff0000u);
+            Cv[2 * k] = __uint_as_float(cw[k] << 16); Cv[2 * k + 1] = __uint_as_float(cw[k] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kS; k++) {
+            Bv[k] = io<T>::load(Bb, k);
+            Cv[k] = io<T>::load(Cb, k);
+        }
     }
     if constexpr (VEC && kS % 4 == 0) {
 #pragma unroll
