@@ -261,12 +261,13 @@ def time_scan(w, steps, warmup, world, rank, local):
 
 def launches_per_scan(w) -> int:
     """Kernels one scan launches: three for the chunked schedule the library
-    picks for long sequences over few channels (fewer than 64 groups of the
-    state-split kernel and at least 64 tiles of 32 tokens), else one."""
-    ch = 128 // (w.dstate // min(w.dstate, 8))
+    picks for long sequences over few channels (channel groups of the
+    state-split kernel covering fewer than 4096 channels, and at least 64
+    tiles of 32 tokens), else one."""
+    ch = 32 if w.dstate == 16 else 128   # channels per CTA (8 states per thread at N = 16)
     groups = w.batch * -(-w.dim // ch)
     tiles = -(-w.seqlen // 32)
-    return 3 if groups < 64 and tiles >= 64 else 1
+    return 3 if groups * ch < 4096 and tiles >= 64 else 1
 
 
 def time_other(name, reps=20, variant=None):

@@ -323,7 +323,7 @@ SSM_API int ssm_scan_fwd_host(const ssm_dims* dims,
  * cudaMalloc, cudaFree or allocating library routine.  Problems whose
  * ssm_scan_fwd_workspace_size() exceeds the buffer are refused with
  * SSM_ERR_TOO_LARGE before anything is enqueued (at N = 16 the buffer holds
- * about 1000 groups of 64 channels, e.g. batch 4 x 16000 channels).
+ * the carries of about 64,000 channels, e.g. batch 4 x 16000 channels).
  *
  * The first call on a device looks up the buffer's device address on that
  * device (cudaGetSymbolAddress, with the device current); make that first

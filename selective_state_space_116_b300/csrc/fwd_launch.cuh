@@ -20,7 +20,8 @@ int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int
     auto agg = scan_chunk_agg_kernel<T, N, S, ZOH, CONV, VEC>;
     auto full = scan_fwd_kernel<T, N, S, ZOH, CONV, VEC>;
     static std::atomic<int> occ_agg[64], occ_full[64];
-    const int oa = occupancy(agg, Sh::SMEM, occ_agg), of = occupancy(full, Sh::SMEM, occ_full);
+    const int oa = occupancy(agg, Sh::NT, Sh::SMEM, occ_agg),
+              of = occupancy(full, Sh::NT, Sh::SMEM, occ_full);
     if (oa < 1 || of < 1) return SSM_ERR_CUDA;
     p.groups_per_row = (p.dim + Sh::CH - 1) / Sh::CH;
     p.ngroups = p.batch * p.groups_per_row;
@@ -34,12 +35,12 @@ int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int
     const int64_t units = p.ngroups * p.nchunks;
     if (cudaMemsetAsync(ws, 0, wl.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     const int64_t ga = units < (int64_t)oa * sms ? units : (int64_t)oa * sms;
-    agg<<<(unsigned)ga, kThreads, Sh::SMEM, stream>>>(p);
+    agg<<<(unsigned)ga, Sh::NT, Sh::SMEM, stream>>>(p);
     const int64_t nseq = p.ngroups * Sh::CH * N;   // one CTA per (group, channel, state)
     if (nseq > INT32_MAX) return SSM_ERR_BAD_DIMS;
     scan_chunk_carry_kernel<N, Sh::CH><<<(unsigned)nseq, kCarryThreads, 0, stream>>>(p);
     const int64_t gf = units < (int64_t)of * sms ? units : (int64_t)of * sms;
-    full<<<(unsigned)gf, kThreads, Sh::SMEM, stream>>>(p);
+    full<<<(unsigned)gf, Sh::NT, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -58,7 +59,7 @@ int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
     if (occ == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
                 cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, Sh::SMEM) !=
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Sh::NT, Sh::SMEM) !=
                 cudaSuccess)
             return SSM_ERR_CUDA;
         if (occ < 1) return SSM_ERR_CUDA;
@@ -87,7 +88,7 @@ int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
         p.carry = reinterpret_cast<float*>(ws + own.carry_off);
         if (cudaMemsetAsync(ws, 0, own.clear_bytes, stream) != cudaSuccess) return SSM_ERR_CUDA;
     }
-    kern<<<(unsigned)ctas, kThreads, Sh::SMEM, stream>>>(p);
+    kern<<<(unsigned)ctas, Sh::NT, Sh::SMEM, stream>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

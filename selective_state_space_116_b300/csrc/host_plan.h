@@ -98,11 +98,11 @@ inline int device_sms(int* sms) {
 }
 
 // Channels one CTA of the state-split kernel scans with S states per thread.
-constexpr int seq_channels(int n, int s) { return ssm::seq::kThreads / (n / s); }
+constexpr int seq_channels(int n, int s) { return ssm::seq::seq_threads(n / s) / (n / s); }
 
 // States per thread for N = 16: 8 (two thread groups per channel, less
-// shared-memory traffic per element) when the problem has enough 64-channel
-// groups to give every SM two of them, else 4 (twice the CTAs).
+// shared-memory traffic per element) when the problem has at least 128
+// channels per SM, else 4 (twice the threads per channel).
 inline int n16_split(const ssm_dims* d, int sms) {
     const int64_t groups8 = d->batch * ((d->dim + 63) / 64);
     return groups8 >= 2 * (int64_t)sms ? 8 : 4;
@@ -125,8 +125,9 @@ inline ScanWorkspace scan_workspace_for(const ssm_dims* d, int ch) {
     return w;
 }
 
-// The chunked (L-parallel) schedule: for problems with fewer than 64 groups
-// of the state-split kernel and at least 64 tiles per group, or whenever the
+// The chunked (L-parallel) schedule: for problems whose channel groups of the
+// state-split kernel cover fewer than 4096 channels and that have at least 64
+// tiles per group, or whenever the
 // caller's `chunk` is below seqlen.  The plan depends only on the sizes, so
 // that the workspace size does too.  N = 16 uses 8 states per thread here
 // (the chunks supply the parallelism).
@@ -145,7 +146,7 @@ inline ChunkPlan chunk_plan(const ssm_dims* d) {
     c.ntiles = (d->seqlen + ssm::seq::kTL - 1) / ssm::seq::kTL;
     if (d->chunk > 0 && d->chunk < d->seqlen) {
         c.tpc = (d->chunk + ssm::seq::kTL - 1) / ssm::seq::kTL;
-    } else if (d->chunk == 0 && c.groups < 64 && c.ntiles >= 64) {
+    } else if (d->chunk == 0 && c.groups * c.ch < 64 * 64 && c.ntiles >= 64) {
         const int64_t want_units = 2048;
         c.tpc = (c.ntiles * c.groups + want_units - 1) / want_units;
         if (c.tpc < 8) c.tpc = 8;
@@ -185,14 +186,14 @@ inline ScanWorkspace scan_workspace(const ssm_dims* d) {
 
 // Number of CTAs of `kern` that fit on one SM (queried once per device).
 template <typename K>
-inline int occupancy(K kern, int smem, std::atomic<int>* cache) {
+inline int occupancy(K kern, int threads, int smem, std::atomic<int>* cache) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
     int occ = cache[dev].load();
     if (occ == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, ssm::seq::kThreads, smem) !=
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) !=
                 cudaSuccess || occ < 1)
             return -1;
         cache[dev].store(occ);

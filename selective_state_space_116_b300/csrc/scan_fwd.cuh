@@ -116,7 +116,11 @@ __device__ __forceinline__ bool debug_ok(bool ok, int* hdr, int site) {
 
 namespace seq {
 
-constexpr int kThreads = 128;   // 4 warps
+// Threads per CTA for G thread groups per channel: with the state split over
+// G = 2 or 4 lanes a CTA scans 32 channels (2 or 4 warps); with one thread per
+// channel, 128 channels.  Two-warp CTAs at G = 2 let more, smaller CTAs share
+// an SM, so one CTA's tile prologue overlaps another's recurrence.
+constexpr int seq_threads(int g) { return g == 2 ? 64 : 128; }
 constexpr int kTL = 32;         // tokens per tile
 
 // Shared-memory layout.  Row paddings of 16 bytes make every access pattern
@@ -125,7 +129,8 @@ constexpr int kTL = 32;         // tokens per tile
 template <typename T, int N, int S, bool CONV>
 struct Shape {
     static constexpr int G = N / S;                    // thread groups per channel
-    static constexpr int CH = kThreads / G;            // channels per CTA
+    static constexpr int NT = seq_threads(G);          // threads per CTA
+    static constexpr int CH = NT / G;                  // channels per CTA
     static constexpr int ES = (int)sizeof(T);
     static constexpr int EPC = 16 / ES;                // elements per 16-byte chunk
     static constexpr int RAW_ROW = kTL * ES + 16;      // one channel's tokens, raw
@@ -147,9 +152,9 @@ struct Shape {
     static constexpr int SMEM = CONV ? OFF_HALO + 2 * CH * 16 : END_Y;
     // (row, 8-token chunk) work items of the prologue / epilogue per thread
     static constexpr int CHUNKS = CH * kTL / 8;
-    static constexpr int CHUNK_ITERS = CHUNKS / kThreads;
+    static constexpr int CHUNK_ITERS = CHUNKS / NT;
     static_assert(N % S == 0 && CH % 32 == 0, "bad state split");
-    static_assert(CHUNKS % kThreads == 0 && kTL % 32 == 0, "bad tile");
+    static_assert(CHUNKS % NT == 0 && kTL % 32 == 0, "bad tile");
     static_assert(RAW_BUF % 16 == 0 && OFF_BC % 16 == 0 && OFF_Y % 16 == 0 && OFF_U % 16 == 0,
                   "alignment");
 };
@@ -165,10 +170,10 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 
 // The (row, chunk) item a thread handles in prologue / epilogue iteration `it`:
 // a warp covers 8 rows x 4 consecutive 8-token chunks, lanes 0..7 on rows 0..7.
-template <int CH>
+template <int CH, int NT>
 __device__ __forceinline__ void chunk_of(int it, int& r, int& q) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int blk = it * (kThreads / 32) + warp;
+    const int blk = it * (NT / 32) + warp;
     constexpr int RB = CH / 8;
     r = (blk % RB) * 8 + (lane & 7);
     q = (blk / RB) * 4 + (lane >> 3);
@@ -237,16 +242,16 @@ template <> __device__ __forceinline__ float2 silu2<__nv_bfloat16>(float2 z) {
 // Copy tile [t0, t0 + kTL) of CH rows of a (rows, L) tensor into a raw plane.
 // VEC: rows are 16-byte aligned and L is a multiple of EPC, so a 16-byte chunk
 // is either wholly inside or wholly outside the tensor.
-template <typename T, int CH, int RAW_ROW, bool VEC>
+template <typename T, int CH, int NT, int RAW_ROW, bool VEC>
 __device__ __forceinline__ void load_plane(unsigned char* plane, const T* g, int64_t row0,
                                            int rows, int64_t L, int64_t t0,
                                            int64_t nrows_total, int* hdr) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int CPR = kTL / EPC;  // chunks per row
-    static_assert((CH * CPR) % kThreads == 0, "plane chunks must split evenly");
+    static_assert((CH * CPR) % NT == 0, "plane chunks must split evenly");
 #pragma unroll
-    for (int k = 0; k < CH * CPR / kThreads; k++) {
-        const int i = k * kThreads + threadIdx.x;
+    for (int k = 0; k < CH * CPR / NT; k++) {
+        const int i = k * NT + threadIdx.x;
         const int r = i / CPR, c = i % CPR;
         const int64_t t = t0 + (int64_t)c * EPC;
         unsigned char* dst = plane + r * RAW_ROW + c * 16;
@@ -267,13 +272,13 @@ __device__ __forceinline__ void load_plane(unsigned char* plane, const T* g, int
 }
 
 // Copy tokens [t0, t0 + kTL) of one batch row of B or C (contiguous kTL*N run).
-template <typename T, int N, bool VEC>
+template <typename T, int N, int NT, bool VEC>
 __device__ __forceinline__ void load_bc(unsigned char* dst, const T* g, int64_t L, int64_t t0,
                                         int* hdr) {
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int CHUNKS = kTL * N / EPC;
     const int64_t valid = (L - t0) * N;  // elements of this tile inside the tensor
-    for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
+    for (int i = threadIdx.x; i < CHUNKS; i += NT) {
         const int64_t e0 = (int64_t)i * EPC;
         if constexpr (VEC) {
             bool ok = e0 < valid;
@@ -644,7 +649,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 #pragma unroll
     for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
         int r, q;
-        chunk_of<CH>(it, r, q);
+        chunk_of<CH, Sh::NT>(it, r, q);
         const float bv = (p.bias && r < rows) ? p.bias[d0 + r] : 0.0f;
         bias_r[it] = softplus ? bv * kLog2e : bv;
         D_r[it] = (p.D && r < rows) ? p.D[d0 + r] : 0.0f;
@@ -664,13 +669,13 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     auto load_tile = [&](int64_t tile, int slot) {
         unsigned char* buf = smem + slot * Sh::RAW_BUF;
         const int64_t t0 = tile * kTL;
-        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0, nrows, hdr);
-        load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0, nrows, hdr);
+        load_plane<T, CH, Sh::NT, Sh::RAW_ROW, VEC>(buf, gu, row0, rows, L, t0, nrows, hdr);
+        load_plane<T, CH, Sh::NT, Sh::RAW_ROW, VEC>(buf + Sh::RAW_PLANE, gdl, row0, rows, L, t0, nrows, hdr);
         if (gate && !AGG)
-            load_plane<T, CH, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0, nrows, hdr);
+            load_plane<T, CH, Sh::NT, Sh::RAW_ROW, VEC>(buf + 2 * Sh::RAW_PLANE, gz, row0, rows, L, t0, nrows, hdr);
         unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
-        load_bc<T, N, VEC>(bcraw, gB, L, t0, hdr);
-        load_bc<T, N, VEC>(bcraw + Sh::BC_RAW, gC, L, t0, hdr);
+        load_bc<T, N, Sh::NT, VEC>(bcraw, gB, L, t0, hdr);
+        load_bc<T, N, Sh::NT, VEC>(bcraw + Sh::BC_RAW, gC, L, t0, hdr);
     };
 
     // the first tile's copies overlap the wait for the carry
@@ -681,7 +686,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         const int64_t t0 = tb * kTL;
         const int K = p.conv_k;
         const T* gs = static_cast<const T*>(p.conv_state);
-        for (int r = threadIdx.x; r < CH; r += kThreads) {
+        for (int r = threadIdx.x; r < CH; r += Sh::NT) {
             float hv[3] = {0.0f, 0.0f, 0.0f};
             if (r < rows) {
 #pragma unroll
@@ -736,7 +741,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 #pragma unroll
         for (int it = 0; it < Sh::CHUNK_ITERS; it++) {
             int r, q;
-            chunk_of<CH>(it, r, q);
+            chunk_of<CH, Sh::NT>(it, r, q);
             float uv[8], dv[8];
             if constexpr (CONV) {
                 // inputs t-3 .. t+7 for the chunk's tokens t = 8q .. 8q+7: the
@@ -823,7 +828,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             float* bcf = reinterpret_cast<float*>(smem + Sh::OFF_BC);
             if constexpr (N % 4 == 0 && S % 4 == 0) {
                 // 4 consecutive n of one token lie in one thread group: one 16-byte store
-                for (int i = threadIdx.x; i < 2 * kTL * N / 4; i += kThreads) {
+                for (int i = threadIdx.x; i < 2 * kTL * N / 4; i += Sh::NT) {
                     const int which = i / (kTL * N / 4);           // 0: B, 1: C
                     const int e0 = (i % (kTL * N / 4)) * 4;
                     const int t = e0 / N, n = e0 % N;
@@ -836,7 +841,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             } else {
                 const T* rb = reinterpret_cast<const T*>(bcraw);
                 const T* rc = reinterpret_cast<const T*>(bcraw + Sh::BC_RAW);
-                for (int i = threadIdx.x; i < kTL * N; i += kThreads) {
+                for (int i = threadIdx.x; i < kTL * N; i += Sh::NT) {
                     const int t = i / N, n = i % N;
                     float* o = bcf + (t * G + n / S) * 2 * S + n % S;
                     o[0] = io<T>::to_f32(rb[i]);
@@ -893,7 +898,7 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 #pragma unroll
         for (int it = 0; it < (AGG ? 0 : Sh::CHUNK_ITERS); it++) {
             int r, q;
-            chunk_of<CH>(it, r, q);
+            chunk_of<CH, Sh::NT>(it, r, q);
             // pairs of tokens in packed fp32 arithmetic, the partial sums
             // added in group order
             float2 y2[4];
@@ -974,7 +979,8 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 // continuation of its first group last, so the state it needs has long been
 // published when it gets there.  With P <= ngroups no group is split twice.
 template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false>
-__global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
+__global__ void __launch_bounds__(Shape<T, N, S, CONV>::NT, 256 / Shape<T, N, S, CONV>::NT)
+scan_fwd_kernel(ScanParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
     using Sh = Shape<T, N, S, CONV>;
@@ -1012,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
                 const int64_t d0 = (grp % p.groups_per_row) * Sh::CH;
                 const int rows = (int)(p.dim - d0 < Sh::CH ? p.dim - d0 : Sh::CH);
                 const int64_t base = (b * p.dim + d0) * N;
-                for (int i = threadIdx.x; i < rows * N; i += kThreads)
+                for (int i = threadIdx.x; i < rows * N; i += Sh::NT)
                     p.last_state[base + i] = p.h0 ? p.h0[base + i] : 0.0f;
             }
         }
@@ -1045,7 +1051,8 @@ __global__ void __launch_bounds__(kThreads, 2) scan_fwd_kernel(ScanParams p) {
 // Passes 1 and 3 are independent over units: grid-stride loops of
 // persistent CTAs.  The price is a second pass over the inputs (no z, no y).
 template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2) scan_chunk_agg_kernel(ScanParams p) {
+__global__ void __launch_bounds__(Shape<T, N, S, CONV>::NT, 256 / Shape<T, N, S, CONV>::NT)
+scan_chunk_agg_kernel(ScanParams p) {
     using Sh = Shape<T, N, S, CONV>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
