@@ -3,30 +3,40 @@
 // The forward pass keeps no state for the backward pass; the backward pass
 // recomputes the forward states on chip instead of reading an expanded state
 // from memory ("State Spaces, Selectively - Mamba", papermap, "The
-// hardware-aware scan").  Per channel, G = N / S adjacent lanes of a warp
-// hold S states each (S = min(N, 4)); the sums over a channel's states
-// (the output s_t, dDelta_t, dx_t) are warp shuffles within the G lanes:
+// hardware-aware scan").  Per channel and token t (Delta_t after bias and
+// softplus, a_tn = exp(Delta_t A_n), x = u):
 //
-//   pass 1  the forward recurrence over the whole sequence, writing only the
-//           state at the start of every 8-token tile to the workspace
-//           (batch x dim x ceil(L/8) x N fp32 checkpoints);
-//   (each 8-token tile's inputs are staged in shared memory by the whole CTA
-//   with coalesced loads, Delta computed once per element; the loads of the
-//   next tile are issued into registers while the current tile computes)
-//   pass 2  the tiles in reverse order: the tile's states are recomputed
-//           from its checkpoint into shared memory, then the adjoint
-//           recurrence runs backwards through the tile:
-//             ds_t = dy_t silu(z_t), dz_t = dy_t s_t silu'(z_t)
-//             g_n += ds_t C_tn                       (adjoint of h_tn)
-//             dDelta_t = sum_n g_n (A_n a_tn h_(t-1)n + B_tn x_t)
-//             dx_t = ds_t D + sum_n g_n Delta_t B_tn
-//             dA_n += g_n Delta_t a_tn h_(t-1)n,     g_n *= a_tn
-//           with dB_tn = g_n Delta_t x_t and dC_tn = ds_t h_tn summed over
-//           the CTA's channels at the end of the tile (from the tile's
-//           states and adjoints kept in shared memory) and added to the
-//           batch row's dB, dC with one atomic per (t, n) per CTA.
-//   dA, dD and delta_bias's gradient are summed per thread over the
-//   sequence and added per CTA with atomics; gradients are fp32.
+//   forward   h_tn = a_tn h_(t-1)n + Delta_t x_t B_tn,   s_t = sum_n C_tn h_tn
+//             y_t = (s_t + D x_t) silu(z_t)
+//   adjoint   ds_t = dy_t silu(z_t);  g_tn = ds_t C_tn + a_(t+1)n g_(t+1)n
+//             (g = dLoss/dh_t, started from dLoss/dlast_state)
+//   gradients dx_t = ds_t D + Delta_t q_t,          q_t = sum_n g_tn B_tn
+//             dDelta_t = r_t + x_t q_t,             r_t = sum_n A_n g_tn a_tn h_(t-1)n
+//             dA_n = sum_t Delta_t g_tn a_tn h_(t-1)n
+//             dB_tn = sum_channels g_tn Delta_t x_t, dC_tn = sum_channels ds_t h_tn
+//             dz_t = dy_t (s_t + D x_t) silu'(z_t),  dD = sum_t ds_t x_t
+//
+// Work split.  A thread holds S = min(N, 4) states of K channels (the same
+// batch row); the G = N / S adjacent lanes of a "slot" hold the whole state of
+// those K channels.  A CTA of 64 threads covers SLOTS = 64 / G slots, i.e.
+// CH = SLOTS K channels, through the whole sequence in 8-token tiles:
+//
+//   pass 1  the forward recurrence, writing the state at the start of every
+//           tile to the workspace (batch x dim x ceil(L/8) x N fp32);
+//   pass 2  the tiles in reverse: the tile's 9 states (the one before it and
+//           its 8) are recomputed into registers from the checkpoint, then
+//           the adjoint runs backwards through them.
+//
+// The sums of a token run in three places.  Over a channel's states (s, q,
+// r): within the thread, then over the G lanes through per-lane partials in
+// shared memory.  Over channels (dB, dC): within the thread over its K
+// channels, then per tile through shared memory over the CTA's slots, then
+// one 16-byte atomic add per 4 states into the batch row.  Over tokens (dA):
+// in registers for the whole sequence.  Everything per element (softplus,
+// the gate and its derivative, the input and output of every (channel,
+// token)) is done once per element by the thread that stages it: each thread
+// stages EPT consecutive tokens of one channel, copied in by cp.async while
+// the tile before computes, and writes their gradients with vector stores.
 #pragma once
 
 #include "common.cuh"
@@ -34,7 +44,7 @@
 namespace ssm {
 namespace bwd {
 
-constexpr int kThreads = 64;    // threads per CTA (more, smaller CTAs: more warps per SM)
+constexpr int kThreads = 64;    // threads per CTA
 constexpr int kTT = 8;          // tokens per tile
 
 struct BwdParams {
@@ -61,268 +71,436 @@ struct BwdParams {
     int64_t batch, dim, L, ntiles;
 };
 
-template <int N> struct BwdShape {
-    static constexpr int S = N < 4 ? N : 4;    // states per thread
-    static constexpr int G = N / S;            // threads per channel
-    static constexpr int CH = kThreads / G;    // channels per CTA
-    // [kTT + 1][kThreads][S]: row 0 the state before the tile, then the
-    // tile's states; the adjoints used for dB in rows 0 .. kTT-1 of a second
-    // such array; then ds_t and Delta_t x_t per channel and token
-    static constexpr int TILE = (kTT + 1) * kThreads * S * 4;
-    static constexpr int OFF_G = TILE;
-    static constexpr int OFF_DS = 2 * TILE;
-    static constexpr int OFF_DX = OFF_DS + kTT * CH * 4;
-    // the tile's inputs, staged with coalesced loads: per channel a row of
-    // kTT + 1 floats (x = u, Delta, v = delta + bias, z, dy), and B, C rows
-    static constexpr int ROW = kTT + 1;
-    static constexpr int OFF_IN = OFF_DX + kTT * CH * 4;
-    static constexpr int IN_PLANE = CH * ROW * 4;
-    static constexpr int OFF_BC = OFF_IN + 5 * IN_PLANE;
-    static constexpr int SMEM = OFF_BC + 2 * kTT * N * 4;
+
+// K: channels per thread (2 at N = 16, 1 otherwise).
+template <typename T, int N, int K> struct BwdShape {
+    static constexpr int S = N < 4 ? N : 4;     // states per thread and channel
+    static constexpr int G = N / S;             // lanes per slot
+    static constexpr int SLOTS = kThreads / G;  // slots per CTA
+    static constexpr int CH = SLOTS * K;        // channels per CTA
+    static constexpr int SK = S * K;            // states per thread
+    static constexpr int ES = (int)sizeof(T);
+    // staging: thread tid takes tokens [(tid % TPR) EPT, +EPT) of channel tid / TPR
+    static constexpr int EPT = CH * kTT / kThreads;
+    static constexpr int TPR = kTT / EPT;
+    // (Delta, Delta x, ds, 0) per (channel, token); rows padded by 16 bytes so
+    // that the 32 / G channels a warp reads at once fall in distinct banks
+    static constexpr int REC_ROW = kTT * 16 + 16;
+    static constexpr int OFF_W = 0;
+    // per (channel, token, lane) the lane's partial (s, q, r, 0); rows padded
+    // to 64 bytes mod 128
+    static constexpr int R_ROW = kTT * G * 16 + 64;
+    static constexpr int OFF_R = OFF_W + CH * REC_ROW;
+    static constexpr int OFF_BC = OFF_R + CH * R_ROW;     // fp32 B[kTT][N], C[kTT][N]
+    // per slot and token the K-channel sums of g Delta x (dB) and ds h (dC);
+    // rows padded to 16 words mod 32 (conflict-free 16-byte stores)
+    static constexpr int P_ROW = kTT * 2 * N + 16;        // floats
+    static constexpr int OFF_P = OFF_BC + 2 * kTT * N * 4;
+    // the next tile's raw inputs: u, delta, z as [CH][kTT] of T, dy as
+    // [CH][kTT] fp32, B and C as [kTT][N] of T
+    static constexpr int RAW_PLANE = CH * kTT * ES;
+    static constexpr int OFF_RAW = OFF_P + SLOTS * P_ROW * 4;
+    static constexpr int OFF_DY = OFF_RAW + 3 * RAW_PLANE;
+    static constexpr int OFF_RB = OFF_DY + CH * kTT * 4;
+    static constexpr int OFF_RC = OFF_RB + kTT * N * ES;
+    static constexpr int SMEM = OFF_RC + kTT * N * ES;
+    static_assert(EPT * kThreads == CH * kTT && kTT % EPT == 0, "staging split");
+    static_assert(N % S == 0 && 32 % G == 0, "state split");
+    static_assert(OFF_R % 16 == 0 && OFF_P % 16 == 0 && OFF_RAW % 16 == 0 && OFF_DY % 16 == 0 &&
+                  OFF_RB % 16 == 0 && OFF_RC % 16 == 0, "alignment");
 };
 
 __device__ __forceinline__ float sigmoid(float v) { return rcp(1.0f + ex2(-v * kLog2e)); }
 
-// sum over the G lanes of a channel (adjacent, G a power of two)
-template <int G>
-__device__ __forceinline__ float chan_sum(float v) {
+// S consecutive floats from / to shared or (16-byte aligned) global memory:
+// one 16-byte access when S = 4
+template <int S>
+__device__ __forceinline__ void ld4(const float* p, float* v) {
+    if constexpr (S == 4) {
+        const float4 q = *reinterpret_cast<const float4*>(p);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
 #pragma unroll
-    for (int off = 1; off < G; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
+        for (int i = 0; i < S; i++) v[i] = p[i];
+    }
+}
+template <int S>
+__device__ __forceinline__ void st4(float* p, const float* v) {
+    if constexpr (S == 4) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < S; i++) p[i] = v[i];
+    }
 }
 
-template <typename T, int N, bool HAS_Z, bool SOFTPLUS>
-__global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdParams p) {
-    using Sh = BwdShape<N>;
-    constexpr int S = Sh::S, G = Sh::G, CH = Sh::CH;
+// cp.async of `bytes` (4, 8, 16 or 32) from global to shared memory, both
+// aligned to min(bytes, 16); src_ok false fills zeros
+template <int BYTES>
+__device__ __forceinline__ void cp_async_bytes(void* smem, const void* gmem, bool src_ok) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    if constexpr (BYTES == 32) {
+        cp_async_bytes<16>(smem, gmem, src_ok);
+        cp_async_bytes<16>(static_cast<char*>(smem) + 16, static_cast<const char*>(gmem) + 16, src_ok);
+    } else if constexpr (BYTES == 16) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+                     "r"(src_ok ? 16 : 0) : "memory");
+    } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;\n" ::"r"(s), "l"(gmem),
+                     "n"(BYTES), "r"(src_ok ? BYTES : 0) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// E consecutive elements of type T in shared memory -> fp32 (16-byte aligned
+// when E * sizeof(T) >= 16, else E * sizeof(T)-aligned)
+template <typename T, int E>
+__device__ __forceinline__ void lds_row(const unsigned char* p, float* v) {
+    if constexpr (sizeof(T) == 2 && E % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < E / 4; q++) {
+            const uint2 w = reinterpret_cast<const uint2*>(p)[q];
+            v[4 * q] = __uint_as_float(w.x << 16);
+            v[4 * q + 1] = __uint_as_float(w.x & 0xffff0000u);
+            v[4 * q + 2] = __uint_as_float(w.y << 16);
+            v[4 * q + 3] = __uint_as_float(w.y & 0xffff0000u);
+        }
+    } else if constexpr (sizeof(T) == 4 && E % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < E / 4; q++) {
+            const float4 w = reinterpret_cast<const float4*>(p)[q];
+            v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e++) v[e] = io<T>::to_f32(reinterpret_cast<const T*>(p)[e]);
+    }
+}
+
+// E consecutive fp32 to global memory: 16-byte stores when VEC (dst aligned)
+template <int E, bool VEC>
+__device__ __forceinline__ void stg_row(float* dst, const float* v, int valid) {
+    if constexpr (VEC && E % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < E / 4; q++)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            if (e < valid) dst[e] = v[e];
+    }
+}
+
+// VEC: L % 8 == 0 and every tensor 16-byte aligned (cp.async staging, vector
+// stores); otherwise bounds-checked scalar copies.
+template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC>
+__global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
+    using Sh = BwdShape<T, N, K>;
+    constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH, SK = Sh::SK;
+    constexpr int EPT = Sh::EPT, TPR = Sh::TPR, ES = Sh::ES;
     extern __shared__ __align__(16) unsigned char smem[];
-    float* Hs = reinterpret_cast<float*>(smem);
-    float* Gs = reinterpret_cast<float*>(smem + Sh::OFF_G);
-    float* DS = reinterpret_cast<float*>(smem + Sh::OFF_DS);     // [kTT][CH]
-    float* DX = reinterpret_cast<float*>(smem + Sh::OFF_DX);     // [kTT][CH]
-    float* XU = reinterpret_cast<float*>(smem + Sh::OFF_IN);                    // [CH][ROW] x
-    float* DT = reinterpret_cast<float*>(smem + Sh::OFF_IN + Sh::IN_PLANE);     // Delta
-    float* VV = reinterpret_cast<float*>(smem + Sh::OFF_IN + 2 * Sh::IN_PLANE); // delta + bias
-    float* ZZ = reinterpret_cast<float*>(smem + Sh::OFF_IN + 3 * Sh::IN_PLANE); // z
-    float* DY = reinterpret_cast<float*>(smem + Sh::OFF_IN + 4 * Sh::IN_PLANE); // dy
-    float* BB = reinterpret_cast<float*>(smem + Sh::OFF_BC);                    // [kTT][N]
+    float* BB = reinterpret_cast<float*>(smem + Sh::OFF_BC);   // [kTT][N]
     float* CC = BB + kTT * N;
-    constexpr int ROW = Sh::ROW;
+    float* P = reinterpret_cast<float*>(smem + Sh::OFF_P);     // [SLOTS][P_ROW]
+    auto wrec = [&](int c, int j) -> float4& {
+        return *reinterpret_cast<float4*>(smem + Sh::OFF_W + c * Sh::REC_ROW + j * 16);
+    };
+    auto rrec = [&](int c, int j, int lane) -> float4& {
+        return *reinterpret_cast<float4*>(smem + Sh::OFF_R + c * Sh::R_ROW + (j * G + lane) * 16);
+    };
 
     const int tid = threadIdx.x;
-    const int lc = tid / G, gi = tid % G;          // channel within the CTA, state slice
-    const int n0 = gi * S;
+    const int slot = tid / G, gi = tid % G, n0 = gi * S;
     const int64_t b = blockIdx.y;
-    const int64_t d = (int64_t)blockIdx.x * CH + lc;
-    const bool active = d < p.dim;
-    const int64_t dd = active ? d : 0;
-    const int64_t c = b * p.dim + dd;     // flat channel
-    const int64_t L = p.L;
-    float* ck = p.ckpt + c * p.ntiles * N + n0;
-
-    float A[S], A2[S];
-#pragma unroll
-    for (int n = 0; n < S; n++) {
-        A[n] = active ? p.A[dd * N + n0 + n] : 0.0f;
-        A2[n] = A[n] * kLog2e;
-    }
-    const float Dv = (active && p.D) ? p.D[dd] : 0.0f;
-    // stage tokens [t0, t0 + nt) of the CTA's channels: consecutive threads
-    // take consecutive tokens of a row; `full` also stages z, dy and C
     const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int64_t L = p.L;
+    // recurrence role: channels slot + k SLOTS of the CTA, states n0 .. n0+S-1
+    bool act[K];
+    int64_t crow[K];                 // flat channel b * dim + d (0 when inactive)
+    float A2[SK], g[SK], dA[SK], h[SK];
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        const int64_t d = d0 + slot + k * SLOTS;
+        act[k] = d < p.dim;
+        crow[k] = act[k] ? b * p.dim + d : 0;
+#pragma unroll
+        for (int i = 0; i < S; i++) {
+            A2[k * S + i] = act[k] ? p.A[d * N + n0 + i] * kLog2e : 0.0f;
+            g[k * S + i] = (act[k] && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
+            dA[k * S + i] = 0.0f;
+            h[k * S + i] = 0.0f;
+        }
+    }
+    // staging role: tokens sj .. sj+EPT-1 of channel sc of the CTA
+    const int sc = tid / TPR, sj = (tid % TPR) * EPT;
+    const bool okc = d0 + sc < p.dim;
+    const int64_t srow = (b * p.dim + (okc ? d0 + sc : 0)) * L;   // row start in (batch, dim, L)
+    const float bias_c = (p.bias && okc) ? p.bias[d0 + sc] : 0.0f;
+    const float D_c = (p.D && okc) ? p.D[d0 + sc] : 0.0f;
     const T* bu = static_cast<const T*>(p.u);
     const T* bdl = static_cast<const T*>(p.delta);
     const T* bz = static_cast<const T*>(p.z);
     const T* bB = static_cast<const T*>(p.B) + b * L * N;
     const T* bC = static_cast<const T*>(p.C) + b * L * N;
-    // A tile's inputs are fetched into registers (`fetch`, global loads in
-    // flight while the previous tile computes) and written to shared memory
-    // later (`put`).
-    constexpr int E = (CH * kTT + kThreads - 1) / kThreads;   // elements per thread
-    constexpr int EB = (kTT * N + kThreads - 1) / kThreads;
-    float rx[E], rv[E], rz[E], rd[E], rb[EB], rc[EB];
-    auto fetch = [&](int64_t t0, int nt, bool full) {
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            const int i = tid + e * kThreads;
-            const int cl = i / kTT, j = i % kTT;
-            const bool ok = i < CH * kTT && d0 + cl < p.dim && j < nt;
-            const int64_t gi2 = ((b * p.dim + d0 + cl) * L + t0 + j);
-            rx[e] = ok ? io<T>::load(bu, gi2) : 0.0f;
-            rv[e] = ok ? io<T>::load(bdl, gi2) + ((p.bias) ? p.bias[d0 + cl] : 0.0f) : 0.0f;
-            rz[e] = (full && ok && HAS_Z) ? io<T>::load(bz, gi2) : 0.0f;
-            rd[e] = (full && ok) ? p.dy[gi2] : 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < EB; e++) {
-            const int i = tid + e * kThreads;
-            const bool ok = i < kTT * N && i / N < nt;
-            rb[e] = ok ? io<T>::load(bB, t0 * N + i) : 0.0f;
-            rc[e] = (full && ok) ? io<T>::load(bC, t0 * N + i) : 0.0f;
-        }
-    };
-    auto put = [&](int nt, bool full) {
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            const int i = tid + e * kThreads;
-            if (i < CH * kTT) {
-                const int cl = i / kTT, j = i % kTT;
-                const bool ok = d0 + cl < p.dim && j < nt;
-                XU[cl * ROW + j] = rx[e];
-                VV[cl * ROW + j] = rv[e];
-                DT[cl * ROW + j] = ok ? (SOFTPLUS ? softplus(rv[e]) : rv[e]) : 0.0f;
-                if (full) {
-                    ZZ[cl * ROW + j] = rz[e];
-                    DY[cl * ROW + j] = rd[e];
-                }
+    unsigned char* raw = smem + Sh::OFF_RAW + (sc * kTT + sj) * ES;
+    float* rawdy = reinterpret_cast<float*>(smem + Sh::OFF_DY) + sc * kTT + sj;
+
+    // Copy tile [t0, t0 + kTT)'s inputs into the raw buffers (asynchronously
+    // when VEC); `full` adds z, dy and C.
+    auto load_tile = [&](int64_t t0, bool full) {
+        if constexpr (VEC) {
+            const int64_t g0 = srow + t0 + sj;
+            cp_async_bytes<EPT * ES>(raw, bu + g0, okc);
+            cp_async_bytes<EPT * ES>(raw + Sh::RAW_PLANE, bdl + g0, okc);
+            if (full && HAS_Z) cp_async_bytes<EPT * ES>(raw + 2 * Sh::RAW_PLANE, bz + g0, okc);
+            if (full) cp_async_bytes<EPT * 4>(rawdy, p.dy + g0, okc);
+            constexpr int BCQ = kTT * N * ES / 16;   // 16-byte chunks of one tile of B
+            for (int i = tid; i < (full ? 2 : 1) * BCQ; i += kThreads) {
+                const int which = i / BCQ, q = i % BCQ;
+                cp_async_bytes<16>(smem + (which ? Sh::OFF_RC : Sh::OFF_RB) + q * 16,
+                                   (which ? bC : bB) + t0 * N + q * (16 / ES), true);
             }
-        }
+        } else {
+            T* ru = reinterpret_cast<T*>(raw);
 #pragma unroll
-        for (int e = 0; e < EB; e++) {
-            const int i = tid + e * kThreads;
-            if (i < kTT * N) {
-                BB[i] = rb[e];
-                if (full) CC[i] = rc[e];
+            for (int e = 0; e < EPT; e++) {
+                const int64_t t = t0 + sj + e;
+                const bool ok = okc && t < L;
+                ru[e] = ok ? bu[srow + t] : io<T>::from_f32(0.0f);
+                reinterpret_cast<T*>(raw + Sh::RAW_PLANE)[e] = ok ? bdl[srow + t] : io<T>::from_f32(0.0f);
+                if (full && HAS_Z)
+                    reinterpret_cast<T*>(raw + 2 * Sh::RAW_PLANE)[e] = ok ? bz[srow + t] : io<T>::from_f32(0.0f);
+                if (full) rawdy[e] = ok ? p.dy[srow + t] : 0.0f;
+            }
+            for (int i = tid; i < (full ? 2 : 1) * kTT * N; i += kThreads) {
+                const int which = i / (kTT * N), q = i % (kTT * N);
+                const bool ok = t0 + q / N < L;
+                reinterpret_cast<T*>(smem + (which ? Sh::OFF_RC : Sh::OFF_RB))[q] =
+                    ok ? (which ? bC : bB)[t0 * N + q] : io<T>::from_f32(0.0f);
             }
         }
     };
 
-    // ---- pass 1: forward, checkpoint every tile ----
-    float h[S];
+    // Raw tile -> the records the recurrence reads.  Outside the sequence or
+    // the channel range everything is 0: Delta = 0 makes a = 1 and the input
+    // term 0, and ds = 0 adds nothing to g, so padded tokens leave the state
+    // and the adjoint unchanged.  `ex` keeps (x, dz factor, softplus') of the
+    // thread's own elements for its epilogue.
+    auto put = [&](int64_t t0, bool full, float (&ex)[EPT][3]) {
+        float xr[EPT], vr[EPT], zr[EPT], dyr[EPT];
+        lds_row<T, EPT>(raw, xr);
+        lds_row<T, EPT>(raw + Sh::RAW_PLANE, vr);
+        if (full && HAS_Z) lds_row<T, EPT>(raw + 2 * Sh::RAW_PLANE, zr);
+        if (full) lds_row<float, EPT>(reinterpret_cast<const unsigned char*>(rawdy), dyr);
 #pragma unroll
-    for (int n = 0; n < S; n++) h[n] = 0.0f;
-    if (p.ntiles > 0) fetch(0, (int)(L < kTT ? L : kTT), false);
-    for (int64_t k = 0; k < p.ntiles; k++) {
-        const int64_t t0 = k * kTT;
-        const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
-        if (active) {
-#pragma unroll
-            for (int n = 0; n < S; n++) ck[k * N + n] = h[n];
+        for (int e = 0; e < EPT; e++) {
+            const bool ok = okc && t0 + sj + e < L;
+            const float v = vr[e] + bias_c;
+            const float dt = ok ? (SOFTPLUS ? softplus(v) : v) : 0.0f;
+            float ds = full ? dyr[e] : 0.0f, dzf = 0.0f;
+            if (full && HAS_Z) {
+                const float sg = sigmoid(zr[e]);
+                ds = dyr[e] * zr[e] * sg;
+                dzf = dyr[e] * sg * fmaf(zr[e], 1.0f - sg, 1.0f);
+            }
+            wrec(sc, sj + e) = make_float4(dt, dt * xr[e], ds, 0.0f);
+            if (full) {
+                ex[e][0] = xr[e];
+                ex[e][1] = dzf;
+                ex[e][2] = (SOFTPLUS && ok) ? sigmoid(v) : 1.0f;
+            }
         }
-        put(nt, false);
+        const T* rb = reinterpret_cast<const T*>(smem + Sh::OFF_RB);
+        const T* rc = reinterpret_cast<const T*>(smem + Sh::OFF_RC);
+        for (int i = tid; i < kTT * N; i += kThreads) {
+            BB[i] = io<T>::to_f32(rb[i]);
+            if (full) CC[i] = io<T>::to_f32(rc[i]);
+        }
+    };
+    float ex[EPT][3];
+
+    // ---- pass 1: forward, checkpoint at the start of every tile ----
+    if (p.ntiles > 0) load_tile(0, false);
+    for (int64_t kt = 0; kt < p.ntiles; kt++) {
+        const int64_t t0 = kt * kTT;
+#pragma unroll
+        for (int k = 0; k < K; k++)
+            if (act[k]) st4<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, h + k * S);
+        if constexpr (VEC) cp_async_wait_all();
+        __syncthreads();                 // raw tile complete, previous tile's records consumed
+        put(t0, false, ex);
         __syncthreads();
-        if (k + 1 < p.ntiles) {
-            const int64_t t1 = t0 + kTT;
-            fetch(t1, (int)(L - t1 < kTT ? L - t1 : kTT), false);
-        }
-        for (int j = 0; j < nt; j++) {
-            const float dt = DT[lc * ROW + j];
-            const float dtx = dt * XU[lc * ROW + j];
+        if (kt + 1 < p.ntiles) load_tile(t0 + kTT, false);
 #pragma unroll
-            for (int n = 0; n < S; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], dtx * BB[j * N + n0 + n]);
+        for (int j = 0; j < kTT; j++) {
+            float Bv[S];
+            ld4<S>(BB + j * N + n0, Bv);
+#pragma unroll
+            for (int k = 0; k < K; k++) {
+                const float4 w = wrec(slot + k * SLOTS, j);
+#pragma unroll
+                for (int i = 0; i < S; i++)
+                    h[k * S + i] = fmaf(ex2(w.x * A2[k * S + i]), h[k * S + i], w.y * Bv[i]);
+            }
         }
-        __syncthreads();
     }
 
     // ---- pass 2: tiles in reverse ----
-    float g[S], dA[S];
+    float dD_acc = 0.0f, db_acc = 0.0f;
+    const bool vec_red = N % 4 == 0 &&
+        ((reinterpret_cast<uintptr_t>(p.dB) | reinterpret_cast<uintptr_t>(p.dC)) & 15) == 0;
+    float hc[SK];   // the checkpoint of the tile processed next
+    auto load_ckpt = [&](int64_t kt) {
 #pragma unroll
-    for (int n = 0; n < S; n++) {
-        g[n] = (active && p.dlast) ? p.dlast[c * N + n0 + n] : 0.0f;
-        dA[n] = 0.0f;
-    }
-    float dD = 0.0f, dbias = 0.0f;
-    if (p.ntiles > 0) {
-        const int64_t tl = (p.ntiles - 1) * kTT;
-        fetch(tl, (int)(L - tl < kTT ? L - tl : kTT), true);
-    }
-    for (int64_t k = p.ntiles - 1; k >= 0; k--) {
-        const int64_t t0 = k * kTT;
-        const int nt = (int)(L - t0 < kTT ? L - t0 : kTT);
-        put(nt, true);
-        // recompute the tile's states (row 0: the state before the tile)
+        for (int k = 0; k < K; k++) {
+            if (act[k]) {
+                ld4<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, hc + k * S);
+            } else {
 #pragma unroll
-        for (int n = 0; n < S; n++) Hs[tid * S + n] = h[n] = active ? ck[k * N + n] : 0.0f;
-        __syncthreads();
-        if (k > 0) fetch(t0 - kTT, kTT, true);   // the next tile back, in flight during this one
-        for (int j = 0; j < nt; j++) {
-            const float dt = DT[lc * ROW + j];
-            const float dtx = dt * XU[lc * ROW + j];
-            float* hs = Hs + ((j + 1) * kThreads + tid) * S;
-#pragma unroll
-            for (int n = 0; n < S; n++) {
-                h[n] = fmaf(ex2(dt * A2[n]), h[n], dtx * BB[j * N + n0 + n]);
-                hs[n] = h[n];
+                for (int i = 0; i < S; i++) hc[k * S + i] = 0.0f;
             }
         }
-        // adjoint recurrence, backwards through the tile
-        for (int j = nt - 1; j >= 0; j--) {
-            const int64_t t = t0 + j;
-            const float v = VV[lc * ROW + j];
-            const float dt = DT[lc * ROW + j];
-            const float x = XU[lc * ROW + j];
-            const float* ht = Hs + ((j + 1) * kThreads + tid) * S;
-            const float* hp = Hs + (j * kThreads + tid) * S;
-            float Cv[S], Bv[S];
-            float sp = 0.0f;
+    };
+    if (p.ntiles > 0) {
+        load_tile((p.ntiles - 1) * kTT, true);
+        load_ckpt(p.ntiles - 1);
+    }
+    for (int64_t kt = p.ntiles - 1; kt >= 0; kt--) {
+        const int64_t t0 = kt * kTT;
+        if constexpr (VEC) cp_async_wait_all();
+        __syncthreads();                 // raw tile complete, the previous tile's epilogue done
+        put(t0, true, ex);
+        float hs[kTT + 1][SK];           // the state before the tile, then after each token
 #pragma unroll
-            for (int n = 0; n < S; n++) {
-                Cv[n] = CC[j * N + n0 + n];
-                Bv[n] = BB[j * N + n0 + n];
-                sp = fmaf(Cv[n], ht[n], sp);
-            }
-            const float s = fmaf(Dv, x, chan_sum<G>(sp));
-            const float dyv = DY[lc * ROW + j];
-            float ds = dyv;
-            if constexpr (HAS_Z) {
-                const float zv = ZZ[lc * ROW + j];
-                const float sg = sigmoid(zv);
-                ds = dyv * zv * sg;
-                if (active && gi == 0) p.dz[c * L + t] = dyv * s * sg * fmaf(zv, 1.0f - sg, 1.0f);
-            }
-            float dxp = 0.0f, ddtp = 0.0f;
-            float* gs = Gs + (j * kThreads + tid) * S;
+        for (int q = 0; q < SK; q++) hs[0][q] = hc[q];
+        __syncthreads();
+        if (kt > 0) {                    // the tile before, in flight while this one computes
+            load_tile(t0 - kTT, true);
+            load_ckpt(kt - 1);
+        }
 #pragma unroll
-            for (int n = 0; n < S; n++) {
-                const float a = ex2(dt * A2[n]);
-                g[n] = fmaf(ds, Cv[n], g[n]);
-                gs[n] = g[n];
-                const float gah = g[n] * a * hp[n];
-                ddtp = fmaf(A[n], gah, fmaf(g[n], Bv[n] * x, ddtp));
-                dxp = fmaf(g[n] * dt, Bv[n], dxp);
-                dA[n] = fmaf(dt, gah, dA[n]);
-                g[n] *= a;
-            }
-            const float ddt = chan_sum<G>(ddtp);
-            const float dx = fmaf(ds, Dv, chan_sum<G>(dxp));
-            const float dv = SOFTPLUS ? ddt * sigmoid(v) : ddt;
-            if (gi == 0) {
-                DS[j * CH + lc] = ds;
-                DX[j * CH + lc] = dt * x;
-                dD = fmaf(ds, x, dD);
-                dbias += dv;
-                if (active) {
-                    p.du[c * L + t] = dx;
-                    p.ddelta[c * L + t] = dv;
+        for (int j = 0; j < kTT; j++) {
+            float Bv[S];
+            ld4<S>(BB + j * N + n0, Bv);
+#pragma unroll
+            for (int k = 0; k < K; k++) {
+                const float4 w = wrec(slot + k * SLOTS, j);
+#pragma unroll
+                for (int i = 0; i < S; i++) {
+                    const int q = k * S + i;
+                    hs[j + 1][q] = fmaf(ex2(w.x * A2[q]), hs[j][q], w.y * Bv[i]);
                 }
             }
         }
-        __syncthreads();
-        // dB_tn = sum_c g_n Delta_t x_t, dC_tn = sum_c ds_t h_tn over the CTA's channels
-        for (int o = tid; o < nt * N; o += kThreads) {
-            const int j = o / N, n = o % N;
-            const int gn = n / S, sn = n % S;
-            float sb = 0.0f, sc = 0.0f;
-            for (int cc = 0; cc < CH; cc++) {
-                const int th = cc * G + gn;
-                sb = fmaf(Gs[(j * kThreads + th) * S + sn], DX[j * CH + cc], sb);
-                sc = fmaf(DS[j * CH + cc], Hs[((j + 1) * kThreads + th) * S + sn], sc);
+        // the adjoint, backwards through the tile
+#pragma unroll
+        for (int j = kTT - 1; j >= 0; j--) {
+            float Bv[S], Cv[S], pb[S], pc[S];
+            ld4<S>(BB + j * N + n0, Bv);
+            ld4<S>(CC + j * N + n0, Cv);
+#pragma unroll
+            for (int k = 0; k < K; k++) {
+                const float4 w = wrec(slot + k * SLOTS, j);   // Delta, Delta x, ds
+                float sa = 0.0f, qa = 0.0f, ra = 0.0f;
+#pragma unroll
+                for (int i = 0; i < S; i++) {
+                    const int q = k * S + i;
+                    const float a = ex2(w.x * A2[q]);
+                    g[q] = fmaf(w.z, Cv[i], g[q]);
+                    if constexpr (HAS_Z) sa = fmaf(Cv[i], hs[j + 1][q], sa);
+                    qa = fmaf(g[q], Bv[i], qa);
+                    pc[i] = k == 0 ? w.z * hs[j + 1][q] : fmaf(w.z, hs[j + 1][q], pc[i]);
+                    pb[i] = k == 0 ? g[q] * w.y : fmaf(g[q], w.y, pb[i]);
+                    const float ga = g[q] * a;
+                    const float pp = ga * hs[j][q];   // g a h_(t-1)
+                    ra = fmaf(A2[q], pp, ra);
+                    dA[q] = fmaf(w.x, pp, dA[q]);
+                    g[q] = ga;
+                }
+                rrec(slot + k * SLOTS, j, gi) = make_float4(sa, qa, ra, 0.0f);
             }
-            atomicAdd(p.dB + (b * L + t0 + j) * N + n, sb);
-            atomicAdd(p.dC + (b * L + t0 + j) * N + n, sc);
+            st4<S>(P + slot * Sh::P_ROW + j * 2 * N + n0, pb);
+            st4<S>(P + slot * Sh::P_ROW + j * 2 * N + N + n0, pc);
         }
         __syncthreads();
-    }
-    if (active) {
-#pragma unroll
-        for (int n = 0; n < S; n++) atomicAdd(p.dA + dd * N + n0 + n, dA[n]);
-        if (gi == 0) {
-            if (p.dD) atomicAdd(p.dD + dd, dD);
-            if (p.dbias) atomicAdd(p.dbias + dd, dbias);
+        // dB, dC of the tile: the sums over the CTA's slots, added to the batch row
+        if (vec_red) {
+            constexpr int NQ = N / 4, NV = kTT * 2 * NQ;
+            for (int o = tid; o < NV; o += kThreads) {
+                const int j = o / (2 * NQ), which = (o / NQ) % 2, qd = o % NQ;
+                const float* src = P + j * 2 * N + which * N + qd * 4;
+                float4 acc = *reinterpret_cast<const float4*>(src);
+#pragma unroll 4
+                for (int sl = 1; sl < SLOTS; sl++) {
+                    const float4 v = *reinterpret_cast<const float4*>(src + sl * Sh::P_ROW);
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                if (t0 + j < L) {
+                    float* dst = (which ? p.dC : p.dB) + (b * L + t0 + j) * N + qd * 4;
+                    atomicAdd(reinterpret_cast<float4*>(dst), acc);
+                }
+            }
+        } else {
+            for (int o = tid; o < kTT * 2 * N; o += kThreads) {
+                const int j = o / (2 * N), which = (o / N) % 2, n = o % N;
+                const float* src = P + j * 2 * N + which * N + n;
+                float acc = 0.0f;
+                for (int sl = 0; sl < SLOTS; sl++) acc += src[sl * Sh::P_ROW];
+                if (t0 + j < L) atomicAdd((which ? p.dC : p.dB) + (b * L + t0 + j) * N + n, acc);
+            }
         }
-        if (p.dh0)
+        // the thread's own elements: du, ddelta, dz, and the dD, delta_bias sums
+        {
+            float dxo[EPT], dvo[EPT], dzo[EPT];
 #pragma unroll
-            for (int n = 0; n < S; n++) p.dh0[c * N + n0 + n] = g[n];
+            for (int e = 0; e < EPT; e++) {
+                const int j = sj + e;
+                float4 rs = rrec(sc, j, 0);
+#pragma unroll
+                for (int l = 1; l < G; l++) {
+                    const float4 v = rrec(sc, j, l);
+                    rs.x += v.x; rs.y += v.y; rs.z += v.z;
+                }
+                const float4 w = wrec(sc, j);
+                dxo[e] = fmaf(w.z, D_c, w.x * rs.y);                           // ds D + Delta q
+                dvo[e] = fmaf(ex[e][0], rs.y, rs.z * kLn2) * ex[e][2];         // (r + x q) softplus'
+                dzo[e] = ex[e][1] * fmaf(D_c, ex[e][0], rs.x);                 // dy (s + D x) silu'
+                if (okc && t0 + j < L) {
+                    dD_acc = fmaf(w.z, ex[e][0], dD_acc);
+                    db_acc += dvo[e];
+                }
+            }
+            if (okc) {
+                const int64_t rem = L - (t0 + sj);
+                const int valid = rem < EPT ? (int)rem : EPT;
+                stg_row<EPT, VEC>(p.du + srow + t0 + sj, dxo, valid);
+                stg_row<EPT, VEC>(p.ddelta + srow + t0 + sj, dvo, valid);
+                if constexpr (HAS_Z) stg_row<EPT, VEC>(p.dz + srow + t0 + sj, dzo, valid);
+            }
+        }
+    }
+
+    // ---- per-channel and per-state sums ----
+#pragma unroll
+    for (int off = 1; off < TPR; off <<= 1) {   // the TPR adjacent lanes staging one channel
+        dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, off);
+        db_acc += __shfl_xor_sync(0xffffffffu, db_acc, off);
+    }
+    if (tid % TPR == 0 && okc) {
+        if (p.dD) atomicAdd(p.dD + d0 + sc, dD_acc);
+        if (p.dbias) atomicAdd(p.dbias + d0 + sc, db_acc);
+    }
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        if (!act[k]) continue;
+        const int64_t d = d0 + slot + k * SLOTS;
+#pragma unroll
+        for (int i = 0; i < S; i++) {
+            atomicAdd(p.dA + d * N + n0 + i, dA[k * S + i]);
+            if (p.dh0) p.dh0[crow[k] * N + n0 + i] = g[k * S + i];
+        }
     }
 }
 
