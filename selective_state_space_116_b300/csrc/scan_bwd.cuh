@@ -78,7 +78,6 @@ template <typename T, int N, int K> struct BwdShape {
     static constexpr int G = N / S;             // lanes per slot
     static constexpr int SLOTS = kThreads / G;  // slots per CTA
     static constexpr int CH = SLOTS * K;        // channels per CTA
-    static constexpr int SK = S * K;            // states per thread
     static constexpr int ES = (int)sizeof(T);
     // staging: thread tid takes tokens [(tid % TPR) EPT, +EPT) of channel tid / TPR
     static constexpr int EPT = CH * kTT / kThreads;
@@ -87,9 +86,12 @@ template <typename T, int N, int K> struct BwdShape {
     // that the 32 / G channels a warp reads at once fall in distinct banks
     static constexpr int REC_ROW = kTT * 16 + 16;
     static constexpr int OFF_W = 0;
-    // per (channel, token, lane) the lane's partial (s, q, r, 0); rows padded
-    // to 64 bytes mod 128
-    static constexpr int R_ROW = kTT * G * 16 + 64;
+    // per (channel, lane, token) the lane's partial (s, q, r, 0): 16-byte unit
+    // c R_ROW/16 + lane kTT + (token ^ lane kTT/G), with R_ROW/16 = 1 mod 8.
+    // The lanes writing one token (2 or more channels x G lanes) and the
+    // threads reading one lane's partials (4 channels x 2 token halves) then
+    // each hit 8 distinct 16-byte bank groups per quarter-warp.
+    static constexpr int R_ROW = (G * kTT + 1) * 16;
     static constexpr int OFF_R = OFF_W + CH * REC_ROW;
     static constexpr int OFF_BC = OFF_R + CH * R_ROW;     // fp32 B[kTT][N], C[kTT][N]
     // per slot and token the K-channel sums of g Delta x (dB) and ds h (dC);
@@ -112,27 +114,34 @@ template <typename T, int N, int K> struct BwdShape {
 
 __device__ __forceinline__ float sigmoid(float v) { return rcp(1.0f + ex2(-v * kLog2e)); }
 
-// S consecutive floats from / to shared or (16-byte aligned) global memory:
-// one 16-byte access when S = 4
+// The S states a thread holds for one channel, as (S + 1) / 2 pairs for the
+// paired fp32 instructions; with S = 1 the pair's second lane is padding,
+// loaded as 0 and never stored.  Rows are aligned to 4 S bytes.
 template <int S>
-__device__ __forceinline__ void ld4(const float* p, float* v) {
+__device__ __forceinline__ void ld_pairs(const float* p, float2* v) {
     if constexpr (S == 4) {
         const float4 q = *reinterpret_cast<const float4*>(p);
-        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        v[0] = make_float2(q.x, q.y);
+        v[1] = make_float2(q.z, q.w);
+    } else if constexpr (S == 2) {
+        v[0] = *reinterpret_cast<const float2*>(p);
     } else {
-#pragma unroll
-        for (int i = 0; i < S; i++) v[i] = p[i];
+        v[0] = make_float2(p[0], 0.0f);
     }
 }
 template <int S>
-__device__ __forceinline__ void st4(float* p, const float* v) {
+__device__ __forceinline__ void st_pairs(float* p, const float2* v) {
     if constexpr (S == 4) {
-        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    } else if constexpr (S == 2) {
+        *reinterpret_cast<float2*>(p) = v[0];
     } else {
-#pragma unroll
-        for (int i = 0; i < S; i++) p[i] = v[i];
+        p[0] = v[0].x;
     }
 }
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+// 2^x of both lanes on the special-function unit
+__device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
 
 // cp.async of `bytes` (4, 8, 16 or 32) from global to shared memory, both
 // aligned to min(bytes, 16); src_ok false fills zeros
@@ -198,8 +207,9 @@ __device__ __forceinline__ void stg_row(float* dst, const float* v, int valid) {
 template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC>
 __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<T, N, K>;
-    constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH, SK = Sh::SK;
+    constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH;
     constexpr int EPT = Sh::EPT, TPR = Sh::TPR, ES = Sh::ES;
+    constexpr int SP = (S + 1) / 2, KP = K * SP;   // state pairs per channel, per thread
     extern __shared__ __align__(16) unsigned char smem[];
     float* BB = reinterpret_cast<float*>(smem + Sh::OFF_BC);   // [kTT][N]
     float* CC = BB + kTT * N;
@@ -208,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         return *reinterpret_cast<float4*>(smem + Sh::OFF_W + c * Sh::REC_ROW + j * 16);
     };
     auto rrec = [&](int c, int j, int lane) -> float4& {
-        return *reinterpret_cast<float4*>(smem + Sh::OFF_R + c * Sh::R_ROW + (j * G + lane) * 16);
+        return *reinterpret_cast<float4*>(smem + Sh::OFF_R + c * Sh::R_ROW +
+                                          (lane * kTT + (j ^ (lane * (kTT / G)))) * 16);
     };
 
     const int tid = threadIdx.x;
@@ -219,18 +230,21 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
     // recurrence role: channels slot + k SLOTS of the CTA, states n0 .. n0+S-1
     bool act[K];
     int64_t crow[K];                 // flat channel b * dim + d (0 when inactive)
-    float A2[SK], g[SK], dA[SK], h[SK];
+    float2 A2[KP], g[KP], dA[KP], h[KP];   // A log2(e), adjoint, dA sums, state
 #pragma unroll
     for (int k = 0; k < K; k++) {
         const int64_t d = d0 + slot + k * SLOTS;
         act[k] = d < p.dim;
         crow[k] = act[k] ? b * p.dim + d : 0;
+        auto a2 = [&](int i) { return (act[k] && i < S) ? p.A[d * N + n0 + i] * kLog2e : 0.0f; };
+        auto g0 = [&](int i) {
+            return (act[k] && i < S && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
+        };
 #pragma unroll
-        for (int i = 0; i < S; i++) {
-            A2[k * S + i] = act[k] ? p.A[d * N + n0 + i] * kLog2e : 0.0f;
-            g[k * S + i] = (act[k] && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
-            dA[k * S + i] = 0.0f;
-            h[k * S + i] = 0.0f;
+        for (int pi = 0; pi < SP; pi++) {
+            A2[k * SP + pi] = make_float2(a2(2 * pi), a2(2 * pi + 1));
+            g[k * SP + pi] = make_float2(g0(2 * pi), g0(2 * pi + 1));
+            dA[k * SP + pi] = h[k * SP + pi] = f2(0.0f);
         }
     }
     // staging role: tokens sj .. sj+EPT-1 of channel sc of the CTA
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         const int64_t t0 = kt * kTT;
 #pragma unroll
         for (int k = 0; k < K; k++)
-            if (act[k]) st4<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, h + k * S);
+            if (act[k]) st_pairs<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, h + k * SP);
         if constexpr (VEC) cp_async_wait_all();
         __syncthreads();                 // raw tile complete, previous tile's records consumed
         put(t0, false, ex);
@@ -335,14 +349,17 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         if (kt + 1 < p.ntiles) load_tile(t0 + kTT, false);
 #pragma unroll
         for (int j = 0; j < kTT; j++) {
-            float Bv[S];
-            ld4<S>(BB + j * N + n0, Bv);
+            float2 Bv[SP];
+            ld_pairs<S>(BB + j * N + n0, Bv);
 #pragma unroll
             for (int k = 0; k < K; k++) {
                 const float4 w = wrec(slot + k * SLOTS, j);
 #pragma unroll
-                for (int i = 0; i < S; i++)
-                    h[k * S + i] = fmaf(ex2(w.x * A2[k * S + i]), h[k * S + i], w.y * Bv[i]);
+                for (int pi = 0; pi < SP; pi++) {
+                    const int q = k * SP + pi;
+                    const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
+                    h[q] = __ffma2_rn(a, h[q], __fmul2_rn(f2(w.y), Bv[pi]));
+                }
             }
         }
     }
@@ -351,15 +368,15 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
     float dD_acc = 0.0f, db_acc = 0.0f;
     const bool vec_red = N % 4 == 0 &&
         ((reinterpret_cast<uintptr_t>(p.dB) | reinterpret_cast<uintptr_t>(p.dC)) & 15) == 0;
-    float hc[SK];   // the checkpoint of the tile processed next
+    float2 hc[KP];   // the checkpoint of the tile processed next
     auto load_ckpt = [&](int64_t kt) {
 #pragma unroll
         for (int k = 0; k < K; k++) {
             if (act[k]) {
-                ld4<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, hc + k * S);
+                ld_pairs<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, hc + k * SP);
             } else {
 #pragma unroll
-                for (int i = 0; i < S; i++) hc[k * S + i] = 0.0f;
+                for (int pi = 0; pi < SP; pi++) hc[k * SP + pi] = f2(0.0f);
             }
         }
     };
@@ -372,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         if constexpr (VEC) cp_async_wait_all();
         __syncthreads();                 // raw tile complete, the previous tile's epilogue done
         put(t0, true, ex);
-        float hs[kTT + 1][SK];           // the state before the tile, then after each token
+        float2 hs[kTT + 1][KP];          // the state before the tile, then after each token
 #pragma unroll
-        for (int q = 0; q < SK; q++) hs[0][q] = hc[q];
+        for (int q = 0; q < KP; q++) hs[0][q] = hc[q];
         __syncthreads();
         if (kt > 0) {                    // the tile before, in flight while this one computes
             load_tile(t0 - kTT, true);
@@ -382,47 +399,49 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         }
 #pragma unroll
         for (int j = 0; j < kTT; j++) {
-            float Bv[S];
-            ld4<S>(BB + j * N + n0, Bv);
+            float2 Bv[SP];
+            ld_pairs<S>(BB + j * N + n0, Bv);
 #pragma unroll
             for (int k = 0; k < K; k++) {
                 const float4 w = wrec(slot + k * SLOTS, j);
 #pragma unroll
-                for (int i = 0; i < S; i++) {
-                    const int q = k * S + i;
-                    hs[j + 1][q] = fmaf(ex2(w.x * A2[q]), hs[j][q], w.y * Bv[i]);
+                for (int pi = 0; pi < SP; pi++) {
+                    const int q = k * SP + pi;
+                    const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
+                    hs[j + 1][q] = __ffma2_rn(a, hs[j][q], __fmul2_rn(f2(w.y), Bv[pi]));
                 }
             }
         }
         // the adjoint, backwards through the tile
 #pragma unroll
         for (int j = kTT - 1; j >= 0; j--) {
-            float Bv[S], Cv[S], pb[S], pc[S];
-            ld4<S>(BB + j * N + n0, Bv);
-            ld4<S>(CC + j * N + n0, Cv);
+            float2 Bv[SP], Cv[SP], pb[SP], pc[SP];
+            ld_pairs<S>(BB + j * N + n0, Bv);
+            ld_pairs<S>(CC + j * N + n0, Cv);
 #pragma unroll
             for (int k = 0; k < K; k++) {
                 const float4 w = wrec(slot + k * SLOTS, j);   // Delta, Delta x, ds
-                float sa = 0.0f, qa = 0.0f, ra = 0.0f;
+                const float2 dt = f2(w.x), dtx = f2(w.y), ds = f2(w.z);
+                float2 sa = f2(0.0f), qa = f2(0.0f), ra = f2(0.0f);
 #pragma unroll
-                for (int i = 0; i < S; i++) {
-                    const int q = k * S + i;
-                    const float a = ex2(w.x * A2[q]);
-                    g[q] = fmaf(w.z, Cv[i], g[q]);
-                    if constexpr (HAS_Z) sa = fmaf(Cv[i], hs[j + 1][q], sa);
-                    qa = fmaf(g[q], Bv[i], qa);
-                    pc[i] = k == 0 ? w.z * hs[j + 1][q] : fmaf(w.z, hs[j + 1][q], pc[i]);
-                    pb[i] = k == 0 ? g[q] * w.y : fmaf(g[q], w.y, pb[i]);
-                    const float ga = g[q] * a;
-                    const float pp = ga * hs[j][q];   // g a h_(t-1)
-                    ra = fmaf(A2[q], pp, ra);
-                    dA[q] = fmaf(w.x, pp, dA[q]);
+                for (int pi = 0; pi < SP; pi++) {
+                    const int q = k * SP + pi;
+                    const float2 a = ex2x2(__fmul2_rn(dt, A2[q]));
+                    g[q] = __ffma2_rn(ds, Cv[pi], g[q]);                      // + ds C
+                    if constexpr (HAS_Z) sa = __ffma2_rn(Cv[pi], hs[j + 1][q], sa);
+                    qa = __ffma2_rn(g[q], Bv[pi], qa);
+                    pc[pi] = k == 0 ? __fmul2_rn(ds, hs[j + 1][q]) : __ffma2_rn(ds, hs[j + 1][q], pc[pi]);
+                    pb[pi] = k == 0 ? __fmul2_rn(g[q], dtx) : __ffma2_rn(g[q], dtx, pb[pi]);
+                    const float2 ga = __fmul2_rn(g[q], a);
+                    const float2 pp = __fmul2_rn(ga, hs[j][q]);              // g a h_(t-1)
+                    ra = __ffma2_rn(A2[q], pp, ra);
+                    dA[q] = __ffma2_rn(dt, pp, dA[q]);
                     g[q] = ga;
                 }
-                rrec(slot + k * SLOTS, j, gi) = make_float4(sa, qa, ra, 0.0f);
+                rrec(slot + k * SLOTS, j, gi) = make_float4(sa.x + sa.y, qa.x + qa.y, ra.x + ra.y, 0.0f);
             }
-            st4<S>(P + slot * Sh::P_ROW + j * 2 * N + n0, pb);
-            st4<S>(P + slot * Sh::P_ROW + j * 2 * N + N + n0, pc);
+            st_pairs<S>(P + slot * Sh::P_ROW + j * 2 * N + n0, pb);
+            st_pairs<S>(P + slot * Sh::P_ROW + j * 2 * N + N + n0, pc);
         }
         __syncthreads();
         // dB, dC of the tile: the sums over the CTA's slots, added to the batch row
@@ -498,8 +517,9 @@ __global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
         const int64_t d = d0 + slot + k * SLOTS;
 #pragma unroll
         for (int i = 0; i < S; i++) {
-            atomicAdd(p.dA + d * N + n0 + i, dA[k * S + i]);
-            if (p.dh0) p.dh0[crow[k] * N + n0 + i] = g[k * S + i];
+            const float2 da = dA[k * SP + i / 2], gg = g[k * SP + i / 2];
+            atomicAdd(p.dA + d * N + n0 + i, i % 2 ? da.y : da.x);
+            if (p.dh0) p.dh0[crow[k] * N + n0 + i] = i % 2 ? gg.y : gg.x;
         }
     }
 }
