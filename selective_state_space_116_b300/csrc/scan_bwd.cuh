@@ -18,7 +18,7 @@
 //
 // Work split.  A thread holds S = min(N, 4) states of K channels (the same
 // batch row); the G = N / S adjacent lanes of a "slot" hold the whole state of
-// those K channels.  A CTA of 64 threads covers SLOTS = 64 / G slots, i.e.
+// those K channels.  A CTA of one warp covers SLOTS = 32 / G slots, i.e.
 // CH = SLOTS K channels, through the whole sequence in 8-token tiles:
 //
 //   pass 1  the forward recurrence, writing the state at the start of every
@@ -44,7 +44,7 @@
 namespace ssm {
 namespace bwd {
 
-constexpr int kThreads = 64;    // threads per CTA
+constexpr int kThreads = 32;    // threads per CTA (one warp: the finest split of the channels)
 constexpr int kTT = 8;          // tokens per tile
 
 struct BwdParams {
@@ -205,7 +205,7 @@ __device__ __forceinline__ void stg_row(float* dst, const float* v, int valid) {
 // VEC: L % 8 == 0 and every tensor 16-byte aligned (cp.async staging, vector
 // stores); otherwise bounds-checked scalar copies.
 template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC>
-__global__ void __launch_bounds__(kThreads, 6) scan_bwd_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<T, N, K>;
     constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH;
     constexpr int EPT = Sh::EPT, TPR = Sh::TPR, ES = Sh::ES;
