@@ -86,12 +86,13 @@ template <typename T, int N, int K> struct BwdShape {
     // that the 32 / G channels a warp reads at once fall in distinct banks
     static constexpr int REC_ROW = kTT * 16 + 16;
     static constexpr int OFF_W = 0;
-    // per (channel, lane, token) the lane's partial (s, q, r, 0): 16-byte unit
-    // c R_ROW/16 + lane kTT + (token ^ lane kTT/G), with R_ROW/16 = 1 mod 8.
-    // The lanes writing one token (2 or more channels x G lanes) and the
-    // threads reading one lane's partials (4 channels x 2 token halves) then
-    // each hit 8 distinct 16-byte bank groups per quarter-warp.
-    static constexpr int R_ROW = (G * kTT + 1) * 16;
+    // per (channel, lane, token) the lane's partial (s, q, r, 0), at 16-byte
+    // unit c R_ROW/16 + lane (kTT + 8 / G) + token with R_ROW/16 = 1 mod 8:
+    // the lanes storing one token (2 or more channels x G lanes) and the
+    // threads reading one lane's partials (4 channels x 2 token halves) each
+    // hit 8 distinct 16-byte bank groups per quarter-warp
+    static constexpr int LANE_U = kTT + 8 / G;
+    static constexpr int R_ROW = (G * LANE_U + 1) * 16;
     static constexpr int OFF_R = OFF_W + CH * REC_ROW;
     static constexpr int OFF_BC = OFF_R + CH * R_ROW;     // fp32 B[kTT][N], C[kTT][N]
     // per slot and token the K-channel sums of g Delta x (dB) and ds h (dC);
@@ -107,7 +108,7 @@ template <typename T, int N, int K> struct BwdShape {
     static constexpr int OFF_RC = OFF_RB + kTT * N * ES;
     static constexpr int SMEM = OFF_RC + kTT * N * ES;
     static_assert(EPT * kThreads == CH * kTT && kTT % EPT == 0, "staging split");
-    static_assert(N % S == 0 && 32 % G == 0, "state split");
+    static_assert(N % S == 0 && 32 % G == 0 && R_ROW / 16 % 8 == 1, "state split");
     static_assert(OFF_R % 16 == 0 && OFF_P % 16 == 0 && OFF_RAW % 16 == 0 && OFF_DY % 16 == 0 &&
                   OFF_RB % 16 == 0 && OFF_RC % 16 == 0, "alignment");
 };
@@ -217,9 +218,10 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     auto wrec = [&](int c, int j) -> float4& {
         return *reinterpret_cast<float4*>(smem + Sh::OFF_W + c * Sh::REC_ROW + j * 16);
     };
+    constexpr int LANE_U = Sh::LANE_U;
     auto rrec = [&](int c, int j, int lane) -> float4& {
         return *reinterpret_cast<float4*>(smem + Sh::OFF_R + c * Sh::R_ROW +
-                                          (lane * kTT + (j ^ (lane * (kTT / G)))) * 16);
+                                          (lane * LANE_U + j) * 16);
     };
 
     const int tid = threadIdx.x;
@@ -230,12 +232,14 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     // recurrence role: channels slot + k SLOTS of the CTA, states n0 .. n0+S-1
     bool act[K];
     int64_t crow[K];                 // flat channel b * dim + d (0 when inactive)
+    float* ckp[K];
     float2 A2[KP], g[KP], dA[KP], h[KP];   // A log2(e), adjoint, dA sums, state
 #pragma unroll
     for (int k = 0; k < K; k++) {
         const int64_t d = d0 + slot + k * SLOTS;
         act[k] = d < p.dim;
         crow[k] = act[k] ? b * p.dim + d : 0;
+        ckp[k] = p.ckpt + crow[k] * p.ntiles * N + n0;
         auto a2 = [&](int i) { return (act[k] && i < S) ? p.A[d * N + n0 + i] * kLog2e : 0.0f; };
         auto g0 = [&](int i) {
             return (act[k] && i < S && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         const int64_t t0 = kt * kTT;
 #pragma unroll
         for (int k = 0; k < K; k++)
-            if (act[k]) st_pairs<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, h + k * SP);
+            if (act[k]) st_pairs<S>(ckp[k] + kt * N, h + k * SP);
         if constexpr (VEC) cp_async_wait_all();
         __syncthreads();                 // raw tile complete, previous tile's records consumed
         put(t0, false, ex);
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
         for (int k = 0; k < K; k++) {
             if (act[k]) {
-                ld_pairs<S>(p.ckpt + (crow[k] * p.ntiles + kt) * N + n0, hc + k * SP);
+                ld_pairs<S>(ckp[k] + kt * N, hc + k * SP);
             } else {
 #pragma unroll
                 for (int pi = 0; pi < SP; pi++) hc[k * SP + pi] = f2(0.0f);
@@ -450,12 +454,15 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             for (int o = tid; o < NV; o += kThreads) {
                 const int j = o / (2 * NQ), which = (o / NQ) % 2, qd = o % NQ;
                 const float* src = P + j * 2 * N + which * N + qd * 4;
-                float4 acc = *reinterpret_cast<const float4*>(src);
-#pragma unroll 4
+                float4 v = *reinterpret_cast<const float4*>(src);
+                float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
+#pragma unroll
                 for (int sl = 1; sl < SLOTS; sl++) {
-                    const float4 v = *reinterpret_cast<const float4*>(src + sl * Sh::P_ROW);
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                    v = *reinterpret_cast<const float4*>(src + sl * Sh::P_ROW);
+                    lo = __fadd2_rn(lo, make_float2(v.x, v.y));
+                    hi = __fadd2_rn(hi, make_float2(v.z, v.w));
                 }
+                const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
                 if (t0 + j < L) {
                     float* dst = (which ? p.dC : p.dB) + (b * L + t0 + j) * N + qd * 4;
                     atomicAdd(reinterpret_cast<float4*>(dst), acc);
