@@ -264,7 +264,7 @@ def launches_per_scan(w) -> int:
     picks for long sequences over few channels (channel groups of the
     state-split kernel covering fewer than 4096 channels, and at least 64
     tiles of 32 tokens), else one."""
-    ch = 32 if w.dstate == 16 else 128   # channels per CTA (8 states per thread at N = 16)
+    ch = 128 // (w.dstate // min(w.dstate, 8))   # channels per CTA of the chunked schedule
     groups = w.batch * -(-w.dim // ch)
     tiles = -(-w.seqlen // 32)
     return 3 if groups * ch < 4096 and tiles >= 64 else 1

@@ -16,9 +16,10 @@ template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC>
 int launch_chunked(ssm::ScanParams p, const ChunkPlan& c, unsigned char* ws, int sms,
                    cudaStream_t stream) {
     using namespace ssm::seq;
-    using Sh = Shape<T, N, S, CONV>;
-    auto agg = scan_chunk_agg_kernel<T, N, S, ZOH, CONV, VEC>;
-    auto full = scan_fwd_kernel<T, N, S, ZOH, CONV, VEC>;
+    constexpr int NT = kSeqThreads;
+    using Sh = Shape<T, N, S, CONV, NT>;
+    auto agg = scan_chunk_agg_kernel<T, N, S, NT, ZOH, CONV, VEC>;
+    auto full = scan_fwd_kernel<T, N, S, NT, ZOH, CONV, VEC>;
     static std::atomic<int> occ_agg[64], occ_full[64];
     const int oa = occupancy(agg, Sh::NT, Sh::SMEM, occ_agg),
               of = occupancy(full, Sh::NT, Sh::SMEM, occ_full);
@@ -48,8 +49,9 @@ template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = fal
 int launch_scan(ssm::ScanParams p, int64_t chunk, unsigned char* ws, int sms,
                 cudaStream_t stream) {
     using namespace ssm::seq;
-    using Sh = Shape<T, N, S, CONV>;
-    auto kern = scan_fwd_kernel<T, N, S, ZOH, CONV, VEC, GS>;
+    constexpr int NT = scan_threads(N / S, ZOH);
+    using Sh = Shape<T, N, S, CONV, NT>;
+    auto kern = scan_fwd_kernel<T, N, S, NT, ZOH, CONV, VEC, GS>;
     // per kernel instance: raise its shared-memory limit and ask how many
     // CTAs fit on an SM, once
     static std::atomic<int> occ_cache[64];   // per device: the attribute is per context

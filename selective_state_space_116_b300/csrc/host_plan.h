@@ -97,8 +97,9 @@ inline int device_sms(int* sms) {
     return SSM_OK;
 }
 
-// Channels one CTA of the state-split kernel scans with S states per thread.
-constexpr int seq_channels(int n, int s) { return ssm::seq::seq_threads(n / s) / (n / s); }
+// Channels one CTA of the state-split kernel scans with S states per thread
+// and NT threads.
+constexpr int seq_channels(int n, int s, int nt) { return nt / (n / s); }
 
 // States per thread for N = 16: 8 (two thread groups per channel, less
 // shared-memory traffic per element) when the problem has at least 128
@@ -141,7 +142,7 @@ inline ChunkPlan chunk_plan(const ssm_dims* d) {
     ChunkPlan c;
     if (d->seqlen <= 0) return c;
     const int n = (int)d->dstate;
-    c.ch = seq_channels(n, n <= 8 ? n : 8);
+    c.ch = seq_channels(n, n <= 8 ? n : 8, ssm::seq::kSeqThreads);
     c.groups = d->batch * ((d->dim + c.ch - 1) / c.ch);
     c.ntiles = (d->seqlen + ssm::seq::kTL - 1) / ssm::seq::kTL;
     if (d->chunk > 0 && d->chunk < d->seqlen) {
@@ -174,9 +175,12 @@ inline ScanWorkspace chunk_workspace(const ChunkPlan& c, int n) {
 // The workspace covers whichever kernel and split the call selects.
 inline ScanWorkspace scan_workspace(const ssm_dims* d) {
     const int n = (int)d->dstate;
-    ScanWorkspace w = scan_workspace_for(d, seq_channels(n, n <= 8 ? n : 8));
+    const int s = n <= 8 ? n : 8;
+    ScanWorkspace w = scan_workspace_for(d, seq_channels(n, s, ssm::seq::scan_threads(n / s, true)));
+    const ScanWorkspace wf = scan_workspace_for(d, seq_channels(n, s, ssm::seq::scan_threads(n / s, false)));
+    if (wf.total > w.total) w = wf;
     if (n == 16) {
-        const ScanWorkspace w4 = scan_workspace_for(d, seq_channels(16, 4));
+        const ScanWorkspace w4 = scan_workspace_for(d, seq_channels(16, 4, ssm::seq::scan_threads(4, false)));
         if (w4.total > w.total) w = w4;
     }
     const ScanWorkspace cw = chunk_workspace(chunk_plan(d), n);

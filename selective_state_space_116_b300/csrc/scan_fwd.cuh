@@ -116,20 +116,23 @@ __device__ __forceinline__ bool debug_ok(bool ok, int* hdr, int site) {
 
 namespace seq {
 
-// Threads per CTA for G thread groups per channel: with the state split over
-// G = 2 or 4 lanes a CTA scans 32 channels (2 or 4 warps); with one thread per
-// channel, 128 channels.  Two-warp CTAs at G = 2 let more, smaller CTAs share
-// an SM, so one CTA's tile prologue overlaps another's recurrence.
-constexpr int seq_threads(int g) { return g == 2 ? 64 : 128; }
+// Threads per CTA.  The single-pass scan with the first-order input term and
+// the state split over G = 2 lanes uses 2-warp CTAs of 32 channels: more,
+// smaller CTAs share an SM, so one CTA's tile prologue overlaps another's
+// recurrence.  Everything else (other splits, the exact-ZOH term, the
+// chunked schedule) uses 4-warp CTAs: there the larger shared memory and
+// register footprint would leave fewer 2-warp CTAs resident than warps lost.
+constexpr int kSeqThreads = 128;
+constexpr int scan_threads(int g, bool zoh) { return (g == 2 && !zoh) ? 64 : kSeqThreads; }
 constexpr int kTL = 32;         // tokens per tile
 
 // Shared-memory layout.  Row paddings of 16 bytes make every access pattern
 // below free of bank conflicts (each quarter-warp touches 8 distinct 16-byte
 // bank groups).
-template <typename T, int N, int S, bool CONV>
+template <typename T, int N, int S, bool CONV, int NT_>
 struct Shape {
     static constexpr int G = N / S;                    // thread groups per channel
-    static constexpr int NT = seq_threads(G);          // threads per CTA
+    static constexpr int NT = NT_;                     // threads per CTA
     static constexpr int CH = NT / G;                  // channels per CTA
     static constexpr int ES = (int)sizeof(T);
     static constexpr int EPC = 16 / ES;                // elements per 16-byte chunk
@@ -603,10 +606,11 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag, long limit) {
 // Tiles [tb, te) of channel group `grp`.  AGG: the aggregate pass of the
 // chunked schedule (no output; the final state and the sum of Delta go to
 // part.hout / part.dsum).
-template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false, bool AGG = false>
+template <typename T, int N, int S, int NT, bool ZOH, bool CONV, bool VEC, bool GS = false,
+          bool AGG = false>
 __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* smem, int64_t grp,
                                           int64_t tb, int64_t te, int* s_ok, const PartIO& part) {
-    using Sh = Shape<T, N, S, CONV>;
+    using Sh = Shape<T, N, S, CONV, NT>;
     constexpr int G = Sh::G, CH = Sh::CH;
     constexpr int QLAST = kTL / 8 - 1;   // the last 8-token chunk of a tile
     constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
@@ -978,12 +982,11 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
 // head first (publishing that state), then its whole groups, and the
 // continuation of its first group last, so the state it needs has long been
 // published when it gets there.  With P <= ngroups no group is split twice.
-template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC, bool GS = false>
-__global__ void __launch_bounds__(Shape<T, N, S, CONV>::NT, 256 / Shape<T, N, S, CONV>::NT)
-scan_fwd_kernel(ScanParams p) {
+template <typename T, int N, int S, int NT, bool ZOH, bool CONV, bool VEC, bool GS = false>
+__global__ void __launch_bounds__(NT, 256 / NT) scan_fwd_kernel(ScanParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
-    using Sh = Shape<T, N, S, CONV>;
+    using Sh = Shape<T, N, S, CONV, NT>;
     if (p.nchunks > 0) {   // pass 3 of the chunked schedule (see scan_chunk_agg_kernel)
         const int64_t units = p.ngroups * p.nchunks;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
@@ -992,7 +995,7 @@ scan_fwd_kernel(ScanParams p) {
             const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
             // every chunk starts from its carry-in (the first: the initial state)
             const PartIO io{2, p.agg + u * Sh::CH * N, nullptr, nullptr, false};
-            scan_part<T, N, S, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
+            scan_part<T, N, S, NT, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
             __syncthreads();
         }
         return;
@@ -1031,7 +1034,7 @@ scan_fwd_kernel(ScanParams p) {
         const int64_t te = (e < lo + p.ntiles ? e : lo + p.ntiles) - lo;
         const int init = tb > 0 ? 1 : (p.h0 ? 3 : 0);
         const PartIO io{init, nullptr, nullptr, nullptr, true};
-        scan_part<T, N, S, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
+        scan_part<T, N, S, NT, ZOH, CONV, VEC, GS>(p, smem, grp, tb, te, &s_ok, io);
     }
 }
 
@@ -1050,10 +1053,9 @@ scan_fwd_kernel(ScanParams p) {
 //           p.nchunks > 0).
 // Passes 1 and 3 are independent over units: grid-stride loops of
 // persistent CTAs.  The price is a second pass over the inputs (no z, no y).
-template <typename T, int N, int S, bool ZOH, bool CONV, bool VEC>
-__global__ void __launch_bounds__(Shape<T, N, S, CONV>::NT, 256 / Shape<T, N, S, CONV>::NT)
-scan_chunk_agg_kernel(ScanParams p) {
-    using Sh = Shape<T, N, S, CONV>;
+template <typename T, int N, int S, int NT, bool ZOH, bool CONV, bool VEC>
+__global__ void __launch_bounds__(NT, 256 / NT) scan_chunk_agg_kernel(ScanParams p) {
+    using Sh = Shape<T, N, S, CONV, NT>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok;
     const int64_t units = p.ngroups * p.nchunks;
@@ -1062,7 +1064,7 @@ scan_chunk_agg_kernel(ScanParams p) {
         const int64_t tb = ck * p.tiles_per_chunk;
         const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
         const PartIO io{0, nullptr, p.agg + u * Sh::CH * N, p.dsum + u * Sh::CH, false};
-        scan_part<T, N, S, ZOH, CONV, VEC, false, true>(p, smem, grp, tb, te, &s_ok, io);
+        scan_part<T, N, S, NT, ZOH, CONV, VEC, false, true>(p, smem, grp, tb, te, &s_ok, io);
         __syncthreads();
     }
 }

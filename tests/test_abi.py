@@ -150,7 +150,7 @@ def test_scan_workspace_checks(lib):
     assert need.value == 0
 
 
-@pytest.mark.parametrize("N,ch", [(1, 128), (2, 128), (4, 128), (8, 128), (16, 32)])
+@pytest.mark.parametrize("N,ch", [(1, 128), (2, 128), (4, 128), (8, 128), (16, 64)])
 def test_scan_workspace_size_formula(lib, N, ch):
     """256-byte header, one flag per channel group, one carried state per group
     (a group is the channels one CTA scans together)."""
@@ -168,7 +168,7 @@ def test_noalloc_refuses_problems_beyond_its_buffer(lib):
     would not fit its built-in buffer; bad sizes get the usual errors."""
     cap = lib.ssm_scan_fwd_noalloc_max_scratch()
     assert cap == 4 << 20
-    big = dims(batch=4, dim=64 * 2000, dstate=16, seqlen=128)   # 16000 groups x 2 KiB of state
+    big = dims(batch=4, dim=64 * 2000, dstate=16, seqlen=128)   # 8000 groups x 4 KiB of state
     need = ctypes.c_size_t(0)
     assert lib.ssm_scan_fwd_workspace_size(ctypes.byref(big), ctypes.byref(need)) == _lib.SSM_OK
     assert need.value > cap
