@@ -126,10 +126,11 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the forward scan's sources (the kernel the headline times)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_116_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.startswith(("scan_fwd", "fwd_", "common", "host_plan")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
