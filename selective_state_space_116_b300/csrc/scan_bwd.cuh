@@ -22,7 +22,8 @@
 // CH = SLOTS K channels, through the whole sequence in 8-token tiles:
 //
 //   pass 1  the forward recurrence, writing the state at the start of every
-//           tile to the workspace (batch x dim x ceil(L/8) x N fp32);
+//           8-token tile to the workspace (batch x dim x ceil(L/8) x N fp32);
+//           it stages 32 tokens at a time in the same shared memory;
 //   pass 2  the tiles in reverse: the tile's 9 states (the one before it and
 //           its 8) are recomputed into registers from the checkpoint, then
 //           the adjoint runs backwards through them.
@@ -106,8 +107,26 @@ template <typename T, int N, int K> struct BwdShape {
     static constexpr int OFF_DY = OFF_RAW + 3 * RAW_PLANE;
     static constexpr int OFF_RB = OFF_DY + CH * kTT * 4;
     static constexpr int OFF_RC = OFF_RB + kTT * N * ES;
-    static constexpr int SMEM = OFF_RC + kTT * N * ES;
+    static constexpr int SMEM2 = OFF_RC + kTT * N * ES;
     static_assert(EPT * kThreads == CH * kTT && kTT % EPT == 0, "staging split");
+    // Pass 1 stages T1 = 4 kTT tokens at a time in its own layout over the
+    // same shared memory (it ends before pass 2 starts): (Delta, Delta x) per
+    // (channel, token), fp32 B rows, and the raw u, delta and B of the next
+    // tile.  Thread tid stages tokens [(tid % TPR1) EPT1, +EPT1) of channel
+    // tid / TPR1.
+    static constexpr int T1 = 4 * kTT;
+    static constexpr int EPT1 = CH * T1 / kThreads;
+    static constexpr int TPR1 = T1 / EPT1;
+    static constexpr int W1_ROW = T1 * 8 + 8;
+    static constexpr int OFF1_W = 0;
+    static constexpr int OFF1_B = (CH * W1_ROW + 15) / 16 * 16;     // fp32 B[T1][N]
+    static constexpr int OFF1_RAW = OFF1_B + T1 * N * 4;            // u, delta: [CH][T1] of T
+    static constexpr int RAW1_PLANE = CH * T1 * ES;
+    static constexpr int OFF1_RB = OFF1_RAW + 2 * RAW1_PLANE;       // B: [T1][N] of T
+    static constexpr int SMEM1 = OFF1_RB + (T1 * N * ES + 15) / 16 * 16;
+    static constexpr int SMEM = SMEM1 > SMEM2 ? SMEM1 : SMEM2;
+    static_assert(EPT1 * kThreads == CH * T1 && T1 % EPT1 == 0 && EPT1 % 8 == 0, "pass-1 staging split");
+    static_assert(OFF1_RAW % 16 == 0 && OFF1_RB % 16 == 0 && RAW1_PLANE % 16 == 0, "pass-1 alignment");
     static_assert(N % S == 0 && 32 % G == 0 && R_ROW / 16 % 8 == 1, "state split");
     static_assert(OFF_R % 16 == 0 && OFF_P % 16 == 0 && OFF_RAW % 16 == 0 && OFF_DY % 16 == 0 &&
                   OFF_RB % 16 == 0 && OFF_RC % 16 == 0, "alignment");
@@ -339,33 +358,103 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     };
     float ex[EPT][3];
 
-    // ---- pass 1: forward, checkpoint at the start of every tile ----
-    if (p.ntiles > 0) load_tile(0, false);
-    for (int64_t kt = 0; kt < p.ntiles; kt++) {
-        const int64_t t0 = kt * kTT;
+    // ---- pass 1: forward over T1-token tiles, checkpoint at every kTT tokens ----
+    {
+        constexpr int T1 = Sh::T1, EPT1 = Sh::EPT1, TPR1 = Sh::TPR1;
+        const int sc1 = tid / TPR1, sj1 = (tid % TPR1) * EPT1;
+        const bool okc1 = d0 + sc1 < p.dim;
+        const int64_t goff1 = (b * p.dim + (okc1 ? d0 + sc1 : 0)) * L + sj1;
+        const float bias1 = (p.bias && okc1) ? p.bias[d0 + sc1] : 0.0f;
+        unsigned char* raw1 = smem + Sh::OFF1_RAW + (sc1 * T1 + sj1) * ES;
+        float2* w1 = reinterpret_cast<float2*>(smem + Sh::OFF1_W);   // [CH] rows of T1 (Delta, Delta x)
+        auto w1rec = [&](int c, int j) -> float2& {
+            return *reinterpret_cast<float2*>(smem + Sh::OFF1_W + c * Sh::W1_ROW + j * 8);
+        };
+        (void)w1;
+        auto load1 = [&](int64_t t0) {
+            const int64_t gt = goff1 + t0;
+            if constexpr (VEC) {
+                // 16-byte pieces of the thread's EPT1 tokens; with L % kTT == 0
+                // each piece lies wholly inside or wholly past the sequence
+                constexpr int PE = 16 / ES;   // elements per piece
 #pragma unroll
-        for (int k = 0; k < K; k++)
-            if (act[k]) st_pairs<S>(ckp[k] + kt * N, h + k * SP);
-        if constexpr (VEC) cp_async_wait_all();
-        __syncthreads();                 // raw tile complete, previous tile's records consumed
-        put(t0, false, ex);
-        __syncthreads();
-        if (kt + 1 < p.ntiles) load_tile(t0 + kTT, false);
+                for (int q = 0; q < EPT1 / PE; q++) {
+                    const bool ok = okc1 && t0 + sj1 + q * PE < L;
+                    cp_async_bytes<16>(raw1 + q * 16, bu + (ok ? gt + q * PE : 0), ok);
+                    cp_async_bytes<16>(raw1 + Sh::RAW1_PLANE + q * 16, bdl + (ok ? gt + q * PE : 0), ok);
+                }
+                constexpr int BCQ1 = T1 * N * ES / 16;
+                for (int i = tid; i < BCQ1; i += kThreads) {
+                    const bool ok = t0 + (int64_t)i * (16 / ES) / N < L;
+                    cp_async_bytes<16>(smem + Sh::OFF1_RB + i * 16, bB + (ok ? t0 * N + i * (16 / ES) : 0), ok);
+                }
+            } else {
+                const T zero = io<T>::from_f32(0.0f);
+#pragma unroll 8
+                for (int e = 0; e < EPT1; e++) {
+                    const bool ok = okc1 && t0 + sj1 + e < L;
+                    reinterpret_cast<T*>(raw1)[e] = ok ? bu[gt + e] : zero;
+                    reinterpret_cast<T*>(raw1 + Sh::RAW1_PLANE)[e] = ok ? bdl[gt + e] : zero;
+                }
+                for (int i = tid; i < T1 * N; i += kThreads) {
+                    const bool ok = t0 + i / N < L;
+                    reinterpret_cast<T*>(smem + Sh::OFF1_RB)[i] = ok ? bB[t0 * N + i] : zero;
+                }
+            }
+        };
+        auto put1 = [&](int64_t t0) {
 #pragma unroll
-        for (int j = 0; j < kTT; j++) {
-            float2 Bv[SP];
-            ld_pairs<S>(BB + j * N + n0, Bv);
+            for (int e0 = 0; e0 < EPT1; e0 += 8) {
+                float xr[8], vr[8];
+                lds_row<T, 8>(raw1 + e0 * ES, xr);
+                lds_row<T, 8>(raw1 + Sh::RAW1_PLANE + e0 * ES, vr);
 #pragma unroll
-            for (int k = 0; k < K; k++) {
-                const float4 w = wrec(slot + k * SLOTS, j);
+                for (int e = 0; e < 8; e++) {
+                    const bool ok = okc1 && t0 + sj1 + e0 + e < L;
+                    const float v = vr[e] + bias1;
+                    const float dt = ok ? (SOFTPLUS ? softplus(v) : v) : 0.0f;
+                    w1rec(sc1, sj1 + e0 + e) = make_float2(dt, dt * xr[e]);
+                }
+            }
+            const T* rb = reinterpret_cast<const T*>(smem + Sh::OFF1_RB);
+            float* bb1 = reinterpret_cast<float*>(smem + Sh::OFF1_B);
+            for (int i = tid; i < T1 * N; i += kThreads) bb1[i] = io<T>::to_f32(rb[i]);
+        };
+        const float* bb1 = reinterpret_cast<const float*>(smem + Sh::OFF1_B);
+        const int64_t ntiles1 = (L + T1 - 1) / T1;
+        if (ntiles1 > 0) load1(0);
+        for (int64_t k1 = 0; k1 < ntiles1; k1++) {
+            const int64_t t0 = k1 * T1;
+            if constexpr (VEC) cp_async_wait_all();
+            __syncthreads();             // raw tile complete, previous tile's records consumed
+            put1(t0);
+            __syncthreads();
+            if (k1 + 1 < ntiles1) load1(t0 + T1);
 #pragma unroll
-                for (int pi = 0; pi < SP; pi++) {
-                    const int q = k * SP + pi;
-                    const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
-                    h[q] = __ffma2_rn(a, h[q], __fmul2_rn(f2(w.y), Bv[pi]));
+            for (int j = 0; j < T1; j++) {
+                if (j % kTT == 0) {      // the state before each kTT-token tile
+                    const int64_t kt = t0 / kTT + j / kTT;
+                    if (kt < p.ntiles) {
+#pragma unroll
+                        for (int k = 0; k < K; k++)
+                            if (act[k]) st_pairs<S>(ckp[k] + kt * N, h + k * SP);
+                    }
+                }
+                float2 Bv[SP];
+                ld_pairs<S>(bb1 + j * N + n0, Bv);
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    const float2 w = w1rec(slot + k * SLOTS, j);
+#pragma unroll
+                    for (int pi = 0; pi < SP; pi++) {
+                        const int q = k * SP + pi;
+                        const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
+                        h[q] = __ffma2_rn(a, h[q], __fmul2_rn(f2(w.y), Bv[pi]));
+                    }
                 }
             }
         }
+        __syncthreads();                 // pass 1's buffers overlap pass 2's
     }
 
     // ---- pass 2: tiles in reverse ----
@@ -450,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         __syncthreads();
         // dB, dC of the tile: the sums over the CTA's slots, added to the batch row
         if (vec_red) {
-            constexpr int NQ = N / 4, NV = kTT * 2 * NQ;
+            constexpr int NQ = N % 4 == 0 ? N / 4 : 1, NV = kTT * 2 * NQ;
             for (int o = tid; o < NV; o += kThreads) {
                 const int j = o / (2 * NQ), which = (o / NQ) % 2, qd = o % NQ;
                 const float* src = P + j * 2 * N + which * N + qd * 4;
