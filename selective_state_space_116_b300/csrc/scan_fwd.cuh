@@ -281,7 +281,10 @@ __device__ __forceinline__ void load_bc(unsigned char* dst, const T* g, int64_t 
     constexpr int EPC = 16 / (int)sizeof(T);
     constexpr int CHUNKS = kTL * N / EPC;
     const int64_t valid = (L - t0) * N;  // elements of this tile inside the tensor
-    for (int i = threadIdx.x; i < CHUNKS; i += NT) {
+#pragma unroll
+    for (int rr = 0; rr < (CHUNKS + NT - 1) / NT; rr++) {
+        const int i = threadIdx.x + rr * NT;
+        if (CHUNKS % NT != 0 && i >= CHUNKS) break;
         const int64_t e0 = (int64_t)i * EPC;
         if constexpr (VEC) {
             bool ok = e0 < valid;
@@ -831,16 +834,28 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             const unsigned char* bcraw = buf + Sh::NPLANES * Sh::RAW_PLANE;
             float* bcf = reinterpret_cast<float*>(smem + Sh::OFF_BC);
             if constexpr (N % 4 == 0 && S % 4 == 0) {
-                // 4 consecutive n of one token lie in one thread group: one 16-byte store
-                for (int i = threadIdx.x; i < 2 * kTL * N / 4; i += Sh::NT) {
-                    const int which = i / (kTL * N / 4);           // 0: B, 1: C
-                    const int e0 = (i % (kTL * N / 4)) * 4;
-                    const int t = e0 / N, n = e0 % N;
-                    const T* src = reinterpret_cast<const T*>(bcraw + which * Sh::BC_RAW) + e0;
-                    float4 v;
-                    v.x = io<T>::to_f32(src[0]); v.y = io<T>::to_f32(src[1]);
-                    v.z = io<T>::to_f32(src[2]); v.w = io<T>::to_f32(src[3]);
-                    *reinterpret_cast<float4*>(bcf + (t * G + n / S) * 2 * S + which * S + n % S) = v;
+                // 4 consecutive n of one token lie in one thread group: one
+                // 8- or 16-byte load and one 16-byte store per group (a loop
+                // of fixed trip count, so that the indices fold)
+                constexpr int Q = 2 * kTL * N / 4;              // 4-element groups of B and C
+#pragma unroll
+                for (int r = 0; r < (Q + Sh::NT - 1) / Sh::NT; r++) {
+                    const int i = threadIdx.x + r * Sh::NT;
+                    if (Q % Sh::NT == 0 || i < Q) {
+                        const int which = i / (kTL * N / 4);           // 0: B, 1: C
+                        const int e0 = (i % (kTL * N / 4)) * 4;
+                        const int t = e0 / N, n = e0 % N;
+                        const unsigned char* src = bcraw + which * Sh::BC_RAW + e0 * Sh::ES;
+                        float4 v;
+                        if constexpr (sizeof(T) == 2) {
+                            const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+                            const float2 lo = bf2_to_f2(w2.x), hi = bf2_to_f2(w2.y);
+                            v = make_float4(lo.x, lo.y, hi.x, hi.y);
+                        } else {
+                            v = *reinterpret_cast<const float4*>(src);
+                        }
+                        *reinterpret_cast<float4*>(bcf + (t * G + n / S) * 2 * S + which * S + n % S) = v;
+                    }
                 }
             } else {
                 const T* rb = reinterpret_cast<const T*>(bcraw);
