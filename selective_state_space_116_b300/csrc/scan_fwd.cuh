@@ -170,6 +170,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // The (row, chunk) item a thread handles in prologue / epilogue iteration `it`:
 // a warp covers 8 rows x 4 consecutive 8-token chunks, lanes 0..7 on rows 0..7.
@@ -534,6 +535,45 @@ __device__ __forceinline__ float scan_tokens_state(const float4* __restrict__ wr
     return tsum;
 }
 
+// The aggregate pass's token loop run backwards from the end of a chunk (the
+// chunk's tokens in reverse, NT at a time): the chunk's state from zero is
+// sum_t (prod_(s>t) a_s) b_t, so with W the product of the decays of the
+// tokens already passed, each token adds W b_t and multiplies W by its a_t.
+// Returns the tile's sum of Delta.  Once every W is below 2^-40 the tokens
+// further back change the chunk's state by less than 2^-40 of their own
+// contributions (which the decays keep geometrically bounded), and the
+// caller stops.
+template <int S, int BCT, int NT, bool ZOH>
+__device__ __forceinline__ float scan_tokens_tail(const float4* __restrict__ wrow,
+                                                  const float* __restrict__ bcf, float (&acc)[S],
+                                                  float (&W)[S], const float (&A2)[S],
+                                                  const float (&ia)[S]) {
+    static_assert(S % 2 == 0 && NT % 2 == 0, "scan_tokens_tail takes even S and NT");
+    float tsum = 0.0f;
+#pragma unroll
+    for (int t = NT - 1; t >= 0; t--) {
+        const float4 wq = wrow[t / 2];
+        const float dt = t % 2 ? wq.z : wq.x, xs = t % 2 ? wq.w : wq.y;
+        if (t % 2 == 0) tsum += wq.x + wq.z;
+        const float* bc = bcf + t * BCT;
+        const float2 dt2 = make_float2(dt, dt);
+#pragma unroll
+        for (int n = 0; n < S; n += 2) {
+            const float2 e = __fmul2_rn(dt2, make_float2(A2[n], A2[n + 1]));
+            const float2 a = make_float2(ex2(e.x), ex2(e.y));
+            const float2 bb = input_term2<ZOH>(a, e, dt, xs, make_float2(bc[n], bc[n + 1]),
+                                               make_float2(ia[n], ia[n + 1]));
+            const float2 w2 = make_float2(W[n], W[n + 1]);
+            const float2 s2 = __ffma2_rn(w2, bb, make_float2(acc[n], acc[n + 1]));
+            const float2 wn = __fmul2_rn(w2, a);
+            acc[n] = s2.x; acc[n + 1] = s2.y;
+            W[n] = wn.x; W[n + 1] = wn.y;
+        }
+    }
+    return tsum;
+}
+constexpr float kTailCut = 9.094947e-13f;   // 2^-40
+
 // One token for one thread (S = 1 or 2): advance S states; with WITH_Y,
 // return the partial C.h.
 template <int S, bool ZOH, bool WITH_Y>
@@ -610,7 +650,7 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag, long limit) {
 // chunked schedule (no output; the final state and the sum of Delta go to
 // part.hout / part.dsum).
 template <typename T, int N, int S, int NT, bool ZOH, bool CONV, bool VEC, bool GS = false,
-          bool AGG = false>
+          bool AGG = false, bool TAIL = false>
 __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* smem, int64_t grp,
                                           int64_t tb, int64_t te, int* s_ok, const PartIO& part) {
     using Sh = Shape<T, N, S, CONV, NT>;
@@ -685,8 +725,10 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
         load_bc<T, N, Sh::NT, VEC>(bcraw + Sh::BC_RAW, gC, L, t0, hdr);
     };
 
-    // the first tile's copies overlap the wait for the carry
-    load_tile(tb, 0);
+    // the first tile's copies overlap the wait for the carry (TAIL: the
+    // aggregate pass walks the part's tiles from its last one backwards)
+    static_assert(!TAIL || (AGG && !CONV && S % 2 == 0), "the tail walk is an aggregate pass");
+    load_tile(TAIL ? te - 1 : tb, 0);
     cp_async_commit();
 
     if constexpr (CONV) {   // the three inputs before the part's first token
@@ -733,9 +775,13 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
     }
 
     float dsum = 0.0f, dcomp = 0.0f;   // sum of Delta over the part (compensated)
-    for (int64_t tile = tb; tile < te; tile++) {
-        const int slot = (int)((tile - tb) & 1);
-        if (tile + 1 < te) load_tile(tile + 1, slot ^ 1);
+    float W[S];                        // TAIL: the decay products of the tokens passed
+#pragma unroll
+    for (int j = 0; j < S; j++) W[j] = 1.0f;
+    for (int64_t step = 0; step < te - tb; step++) {
+        const int64_t tile = TAIL ? te - 1 - step : tb + step;
+        const int slot = (int)(step & 1);
+        if (step + 1 < te - tb) load_tile(TAIL ? tile - 1 : tile + 1, slot ^ 1);
         cp_async_commit();
         cp_async_wait_1();
         __syncthreads();
@@ -875,7 +921,12 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             const float4* wrow = reinterpret_cast<const float4*>(smem + Sh::OFF_W + ch * Sh::W_ROW);
             const float* bcf = reinterpret_cast<const float*>(smem + Sh::OFF_BC) + g * 2 * S;
             float* yrow = reinterpret_cast<float*>(smem + Sh::OFF_Y + (g * CH + ch) * Sh::Y_ROW);
-            if constexpr (AGG && S % 4 == 0) {
+            if constexpr (TAIL) {
+                const float tsum = scan_tokens_tail<S, G * 2 * S, kTL, ZOH>(wrow, bcf, h, W, A2, ia);
+                const float yk = tsum - dcomp, tk = dsum + yk;
+                dcomp = (tk - dsum) - yk;
+                dsum = tk;
+            } else if constexpr (AGG && S % 4 == 0) {
                 const float tsum = scan_tokens_state<S, G * 2 * S, kTL, ZOH>(wrow, bcf, h, A2, ia);
                 const float yk = tsum - dcomp, tk = dsum + yk;
                 dcomp = (tk - dsum) - yk;
@@ -962,6 +1013,17 @@ __device__ __forceinline__ void scan_part(const ScanParams& p, unsigned char* sm
             }
         }
         __syncthreads();
+        if constexpr (TAIL) {   // stop once every decay product of the CTA is below the cut
+            float wmax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < S; j++) wmax = fmaxf(wmax, W[j]);
+            const bool live = active && !(wmax < kTailCut);   // NaN keeps walking
+            if (!__syncthreads_or(live)) {
+                cp_async_commit();
+                cp_async_wait_0();   // the copy of the next tile is still in flight
+                break;
+            }
+        }
     }
 
     if (part.hout) {   // chunk aggregate: final state from zero and the Delta sum
@@ -1079,7 +1141,11 @@ __global__ void __launch_bounds__(NT, 256 / NT) scan_chunk_agg_kernel(ScanParams
         const int64_t tb = ck * p.tiles_per_chunk;
         const int64_t te = tb + p.tiles_per_chunk < p.ntiles ? tb + p.tiles_per_chunk : p.ntiles;
         const PartIO io{0, nullptr, p.agg + u * Sh::CH * N, p.dsum + u * Sh::CH, false};
-        scan_part<T, N, S, NT, ZOH, CONV, VEC, false, true>(p, smem, grp, tb, te, &s_ok, io);
+        // without the convolution (whose inputs reach back across tiles) the
+        // chunk is walked from its end and the walk stops when the decays
+        // have made the earlier tokens negligible
+        constexpr bool kTail = !CONV && S % 2 == 0;
+        scan_part<T, N, S, NT, ZOH, CONV, VEC, false, true, kTail>(p, smem, grp, tb, te, &s_ok, io);
         __syncthreads();
     }
 }
