@@ -107,12 +107,15 @@ typedef struct ssm_dims {
                         channel's arithmetic is unchanged: outputs are bitwise
                         equal to the default schedule's.
                         0 < chunk < seqlen: the chunked schedule, with chunks of
-                        chunk tokens (rounded up to 32): the chunks of a
-                        sequence are scanned in parallel from zero, their affine
-                        maps composed into carry-ins, and scanned again from
-                        those; outputs agree up to fp32 rounding order.  The
-                        default schedule takes it by itself for long sequences
-                        over few channels. */
+                        chunk tokens (rounded up to 32): every chunk's affine
+                        map is computed in parallel by walking the chunk back
+                        from its end (the walk stops once the product of the
+                        decays passed is below 2^-40 for every state, where
+                        the earlier tokens no longer change the fp32 result),
+                        the maps are composed into carry-ins, and the chunks
+                        are scanned from those; outputs agree up to fp32
+                        rounding order.  The default schedule takes it by
+                        itself for long sequences over few channels. */
 } ssm_dims;
 
 /*

@@ -1119,9 +1119,12 @@ __global__ void __launch_bounds__(NT, 256 / NT) scan_fwd_kernel(ScanParams p) {
 // fill the GPU (a long sequence over few channels).  The token range of every
 // group is cut into chunks, and the affine maps h -> a h + b of the steps
 // compose associatively ((a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2)), so:
-//   pass 1  every (group, chunk) unit scans its chunk from a zero state: the
-//           final state is the chunk's b; its a is exp(A sum Delta)
-//           (scan_chunk_agg_kernel)
+//   pass 1  every (group, chunk) unit finds its chunk's map: b, the state the
+//           chunk reaches from zero, and a = exp(A sum Delta)
+//           (scan_chunk_agg_kernel).  Without the convolution it walks the
+//           chunk from its end (scan_tokens_tail) and stops once the decay
+//           products are negligible, so for decaying states it reads only the
+//           chunk's last tokens; with it, it scans the chunk forward.
 //   pass 2  per (channel, state) an exclusive scan of the chunks' maps under
 //           composition (lanes, warps, tiles of chunks) gives each chunk's
 //           carry-in from the initial state (scan_chunk_carry_kernel)
@@ -1129,7 +1132,7 @@ __global__ void __launch_bounds__(NT, 256 / NT) scan_fwd_kernel(ScanParams p) {
 //           and, for the last chunk, last_state (scan_fwd_kernel with
 //           p.nchunks > 0).
 // Passes 1 and 3 are independent over units: grid-stride loops of
-// persistent CTAs.  The price is a second pass over the inputs (no z, no y).
+// persistent CTAs.  The price is pass 1's reading of the chunks' tails.
 template <typename T, int N, int S, int NT, bool ZOH, bool CONV, bool VEC>
 __global__ void __launch_bounds__(NT, 256 / NT) scan_chunk_agg_kernel(ScanParams p) {
     using Sh = Shape<T, N, S, CONV, NT>;

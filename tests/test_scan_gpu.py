@@ -327,8 +327,9 @@ CHUNKED = Workload("chunked", 2, 70, 16, 1000, "f32", bias_range=(-4.0, -2.0),
 @pytest.mark.parametrize("N", [1, 4, 16])
 @pytest.mark.parametrize("chunk", [32, 96, 300])
 def test_chunked_matches_oracle(io, N, chunk):
-    """chunk < L: the chunks are scanned from zero in parallel, composed into
-    carry-ins by a sequential pass over the chunks, and scanned again."""
+    """chunk < L: the chunks' maps are found in parallel (each chunk walked
+    back from its end), composed into carry-ins, and the chunks scanned from
+    those."""
     w = CHUNKED.scaled(io=io, dstate=N)
     inp = make_scan_inputs(w, seed=N + chunk)
     y, h = gpu_scan(inp, chunk=chunk)
@@ -350,6 +351,30 @@ def test_chunked_options(gate, softplus, skip):
     y_ref, h_ref = oracle_scan(inp)
     assert_close(as64(y), y_ref, torch.float32, "y")
     assert_close(as64(h), h_ref, torch.float32, "last_state")
+
+
+@pytest.mark.parametrize("decay", ["zero_and_slow", "fast"])
+def test_chunked_aggregate_walk(decay):
+    """The chunked schedule's aggregate pass walks each chunk backwards from
+    its end and stops once every decay product is below 2^-40.  zero_and_slow:
+    states with A = 0 and A = -1e-4 (n + 1) never get there, so every chunk is
+    walked to its start; fast: A = -20 makes the products negligible within
+    the first tile, so the walk stops with the next tile's copy in flight."""
+    w = CHUNKED.scaled(seqlen=1000)
+    inp = make_scan_inputs(w, seed=41)
+    A = inp["A"].clone()
+    if decay == "zero_and_slow":
+        A[:, ::3] = 0.0
+        slow = -1e-4 * torch.arange(1, w.dstate + 1, dtype=torch.float32)
+        A[1::2, 1::3] = slow[1::3]
+    else:
+        A[:] = -20.0
+    inp["A"] = A
+    for chunk in (64, 256):
+        y, h = gpu_scan(inp, chunk=chunk)
+        y_ref, h_ref = oracle_scan(inp)
+        assert_close(as64(y), y_ref, torch.float32, f"y, chunk {chunk}")
+        assert_close(as64(h), h_ref, torch.float32, f"last_state, chunk {chunk}")
 
 
 def test_chunked_by_default_for_long_sequences():
