@@ -366,11 +366,10 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         const int64_t goff1 = (b * p.dim + (okc1 ? d0 + sc1 : 0)) * L + sj1;
         const float bias1 = (p.bias && okc1) ? p.bias[d0 + sc1] : 0.0f;
         unsigned char* raw1 = smem + Sh::OFF1_RAW + (sc1 * T1 + sj1) * ES;
-        float2* w1 = reinterpret_cast<float2*>(smem + Sh::OFF1_W);   // [CH] rows of T1 (Delta, Delta x)
+        // (Delta, Delta x) of channel c, token j of the tile
         auto w1rec = [&](int c, int j) -> float2& {
             return *reinterpret_cast<float2*>(smem + Sh::OFF1_W + c * Sh::W1_ROW + j * 8);
         };
-        (void)w1;
         auto load1 = [&](int64_t t0) {
             const int64_t gt = goff1 + t0;
             if constexpr (VEC) {
