@@ -233,7 +233,8 @@ int oracle_state_step(int64_t batch, int64_t dim, int64_t dstate, int io, int pi
  * For one channel (b, d), with x_t = u_t, v_t = delta_t + bias,
  * Delta_t = softplus(v_t) (or v_t), a_tn = exp(Delta_t A_n),
  * h_tn = a_tn h_(t-1)n + Delta_t B_tn x_t, s_t = sum_n C_tn h_tn + D x_t and
- * y_t = s_t silu(z_t) (or s_t), let g_n be the adjoint of h_tn.  Going from
+ * y_t = s_t silu(z_t) (or s_t), let g_n be the adjoint of h_tn.  The forward
+ * starts from h_(-1) = h0 (zero when no initial state is given).  Going from
  * t = L-1 down to 0, starting from g = dlast:
  *
  *   ds_t   = dy_t silu(z_t)           dz_t = dy_t s_t silu'(z_t)
@@ -258,6 +259,7 @@ typedef struct {
     const void *u, *delta, *A, *B, *C, *D, *z, *bias;
     int softplus_on;
     const double *dy, *dlast;   /* (batch, dim, L), (batch, dim, N) (dlast may be NULL) */
+    const double* h0;           /* (batch, dim, N) initial state, or NULL for zero */
     double *du, *ddelta, *dz, *dA, *dD, *dbias, *dBc, *dCc, *dh0;
     const int64_t* chan;        /* flat channel ids, or NULL for all */
     int64_t nchan, next;
@@ -275,8 +277,8 @@ static void bwd_channel(const bwd_job* j, int64_t k, double* hs, double* g) {
     const int64_t row = c * L, bc_row = b * L * N;
     const double bias = j->bias ? load(j->pio, j->bias, d) : 0.0;
     const double Dskip = j->D ? load(j->pio, j->D, d) : 0.0;
-    /* forward: hs[(t + 1) * N + n] = h_tn, hs[n] = h_(-1)n = 0 */
-    for (int64_t n = 0; n < N; n++) hs[n] = 0.0;
+    /* forward: hs[(t + 1) * N + n] = h_tn, hs[n] = h_(-1)n = h0 (or 0) */
+    for (int64_t n = 0; n < N; n++) hs[n] = j->h0 ? j->h0[c * N + n] : 0.0;
     for (int64_t t = 0; t < L; t++) {
         const double v = load(j->io, j->delta, row + t) + bias;
         const double dt = j->softplus_on ? softplus(v) : v;
@@ -361,7 +363,8 @@ static void* bwd_worker(void* arg) {
  * Backward selective scan over the channels listed in `chan` (flat ids
  * b*dim + d; NULL means every channel in order, and then nchan must equal
  * batch*dim); see the comment above.  Inputs as for oracle_scan_fwd; dy is
- * (batch, dim, L) fp64 and dlast (batch, dim, N) fp64 or NULL, both full.
+ * (batch, dim, L) fp64, dlast (batch, dim, N) fp64 or NULL and h0, the
+ * forward's initial state, (batch, dim, N) fp64 or NULL, all full.
  * Outputs (fp64, compact, one row per listed channel): du, ddelta, dz
  * (nchan x L; dz may be NULL when z is), dA (nchan x N: the channel's
  * share, summed over the batch by the caller), dD, dbias (nchan), dBc, dCc
@@ -371,7 +374,7 @@ static void* bwd_worker(void* arg) {
 int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io, int pio,
                     const void* u, const void* delta, const void* A, const void* B,
                     const void* C, const void* D, const void* z, const void* delta_bias,
-                    int delta_softplus, const double* dy, const double* dlast,
+                    int delta_softplus, const double* dy, const double* dlast, const double* h0,
                     const int64_t* chan, int64_t nchan, double* du, double* ddelta, double* dz,
                     double* dA, double* dD, double* dbias, double* dBc, double* dCc, double* dh0,
                     int nthreads) {
@@ -391,7 +394,7 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
     j.io = io; j.pio = pio;
     j.u = u; j.delta = delta; j.A = A; j.B = B; j.C = C; j.D = D; j.z = z;
     j.bias = delta_bias; j.softplus_on = delta_softplus;
-    j.dy = dy; j.dlast = dlast;
+    j.dy = dy; j.dlast = dlast; j.h0 = h0;
     j.du = du; j.ddelta = ddelta; j.dz = dz; j.dA = dA; j.dD = dD; j.dbias = dbias;
     j.dBc = dBc; j.dCc = dCc; j.dh0 = dh0;
     j.chan = chan;

@@ -80,6 +80,51 @@ def test_backward_oracle_matches_finite_differences(opts, shape):
         assert abs(fd - got) <= RTOL * (1 + abs(fd)), ("h0", int(i), fd, got)
 
 
+@pytest.mark.parametrize("opts", [
+    dict(z=True, softplus=True, bias=True, skip=True),
+    dict(z=False, softplus=False, bias=False, skip=False),
+])
+def test_backward_oracle_with_initial_state_matches_finite_differences(opts):
+    """The forward run from a nonzero initial state h0: every gradient,
+    including dh0 around that h0 and the dA, dDelta terms that h0 feeds
+    through h_(-1), against central differences of the forward oracle."""
+    b, d, L, N = 2, 3, 9, 4
+    rng = np.random.default_rng(23)
+    x = make(rng, b, d, L, N, **opts)
+    sp = opts["softplus"]
+    Wy = rng.standard_normal((b, d, L))
+    Wh = rng.standard_normal((b, d, N))
+    h0 = rng.standard_normal((b * d, N)) * 2.0
+    g = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], Wy, D=x["D"], z=x["z"],
+                        delta_bias=x["delta_bias"], delta_softplus=sp, dlast=Wh,
+                        h0=h0.reshape(b, d, N))
+    g0 = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], Wy, D=x["D"], z=x["z"],
+                         delta_bias=x["delta_bias"], delta_softplus=sp, dlast=Wh)
+    assert not np.allclose(g["dA"], g0["dA"])   # h0 reaches dA
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    for name, gname in names.items():
+        if x[name] is None:
+            continue
+        flat = x[name].reshape(-1)
+        for i in rng.choice(flat.size, size=min(flat.size, 10), replace=False):
+            keep = flat[i]
+            flat[i] = keep + EPS
+            lp = loss(x, sp, Wy, Wh, h0)
+            flat[i] = keep - EPS
+            lm = loss(x, sp, Wy, Wh, h0)
+            flat[i] = keep
+            fd = (lp - lm) / (2 * EPS)
+            got = g[gname].reshape(-1)[i]
+            assert abs(fd - got) <= RTOL * (1 + abs(fd)), (name, int(i), fd, got)
+    for i in rng.choice(h0.size, size=8, replace=False):
+        hp = h0.copy(); hp.reshape(-1)[i] += EPS
+        hm = h0.copy(); hm.reshape(-1)[i] -= EPS
+        fd = (loss(x, sp, Wy, Wh, hp) - loss(x, sp, Wy, Wh, hm)) / (2 * EPS)
+        got = g["dh0"].reshape(-1)[i]
+        assert abs(fd - got) <= RTOL * (1 + abs(fd)), ("h0", int(i), fd, got)
+
+
 def test_backward_oracle_zero_gradient_and_linearity():
     rng = np.random.default_rng(3)
     x = make(rng, 2, 2, 9, 4, z=False, softplus=True, bias=True, skip=True)
