@@ -40,7 +40,7 @@
  * none synchronises the device.  Outputs must not alias inputs (state, the
  * only in/out buffer, excepted).  The library prints nothing.
  * Allocation and state kept by the library:
- *   - ssm_scan_fwd, ssm_scan_fwd_ex, ssm_scan_bwd, ssm_state_step and
+ *   - ssm_scan_fwd, ssm_scan_fwd_ex, ssm_scan_bwd, ssm_scan_bwd_ex, ssm_state_step,
  *     ssm_scan_fwd_noalloc allocate nothing; their scratch is the caller's
  *     workspace (ssm_scan_fwd_noalloc: a fixed buffer inside the library).
  *   - ssm_scan_fwd_host allocates its device staging buffers on the caller's
@@ -280,6 +280,26 @@ SSM_API int ssm_scan_bwd(const ssm_dims* dims,
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus,
                  const float* dy, const float* dlast_state,
+                 float* du, float* ddelta, float* dz, float* dA,
+                 float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ssm_scan_bwd for a forward scan that started from the initial state h0
+ * (batch, dim, dstate) fp32 (device; NULL: zero, i.e. ssm_scan_bwd), the
+ * state ssm_scan_fwd_ex takes in ssm_scan_opts.h0 ("Mamba remembers by
+ * forgetting, read closely", interactiveml.org: the selective_scan
+ * recurrence started from a given state).  The recomputed forward states
+ * start from h0, so every gradient includes its effect (dA and ddelta
+ * through h_(-1)); dh0 is the gradient with respect to h0.  The first-order
+ * input term only (the ZOH term and the fused convolution have no backward
+ * here).  Other arguments, workspace and errors as for ssm_scan_bwd.
+ */
+SSM_API int ssm_scan_bwd_ex(const ssm_dims* dims,
+                 const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus,
+                 const float* dy, const float* dlast_state, const float* h0,
                  float* du, float* ddelta, float* dz, float* dA,
                  float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
                  void* workspace, size_t workspace_bytes, void* stream);

@@ -277,14 +277,15 @@ def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
-                 dlast_state=None, return_dh0=False, workspace=None):
+                 dlast_state=None, return_dh0=False, workspace=None, h0=None):
     """Backward selective scan (CUDA tensors): the gradients of a loss with
     dLoss/dy = ``dy`` (and dLoss/dlast_state = ``dlast_state``) with respect
-    to the inputs of ``ssm_scan_fwd`` (zero initial state).  The forward
-    states are recomputed inside the kernel.  Returns a dict of fp32
-    tensors: du, ddelta (gradient of the raw delta), dz (None without z),
-    dA, dB, dC, dD (None without D), ddelta_bias (None without delta_bias)
-    and dh0 (None unless ``return_dh0``).
+    to the inputs of ``ssm_scan_fwd`` run from the initial state ``h0``
+    ((batch, dim, N) fp32, or None for zero; the first-order input term).
+    The forward states are recomputed inside the kernel.  Returns a dict of
+    fp32 tensors: du, ddelta (gradient of the raw delta), dz (None without
+    z), dA, dB, dC, dD (None without D), ddelta_bias (None without
+    delta_bias) and dh0 (None unless ``return_dh0``).
     """
     device = u.device
     if device.type != "cuda":
@@ -304,6 +305,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     _check(delta_bias, "delta_bias", (dim,), torch.float32, device, optional=True)
     _check(dy, "dy", (batch, dim, L), torch.float32, device)
     _check(dlast_state, "dlast_state", (batch, dim, N), torch.float32, device, optional=True)
+    _check(h0, "h0", (batch, dim, N), torch.float32, device, optional=True)
     f32 = dict(dtype=torch.float32, device=device)
     g = {"du": torch.empty((batch, dim, L), **f32), "ddelta": torch.empty((batch, dim, L), **f32),
          "dz": torch.empty((batch, dim, L), **f32) if z is not None else None,
@@ -321,14 +323,14 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     if workspace is None and need.value > 0:
         workspace = torch.empty(need.value, dtype=torch.uint8, device=device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.ssm_scan_bwd(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                          _ptr(D), _ptr(z), _ptr(delta_bias), 1 if delta_softplus else 0,
-                          _ptr(dy), _ptr(dlast_state), _ptr(g["du"]), _ptr(g["ddelta"]),
-                          _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-                          _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
-                          _ptr(workspace), ws_bytes, _stream(device))
+    rc = lib.ssm_scan_bwd_ex(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), _ptr(delta_bias), 1 if delta_softplus else 0,
+                             _ptr(dy), _ptr(dlast_state), _ptr(h0), _ptr(g["du"]),
+                             _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                             _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+                             _ptr(workspace), ws_bytes, _stream(device))
     if rc != 0:
-        raise SSMError(rc, "ssm_scan_bwd")
+        raise SSMError(rc, "ssm_scan_bwd_ex")
     return g
 
 
@@ -337,30 +339,35 @@ class _SelectiveScan(torch.autograd.Function):
     recomputes the forward states; nothing but the inputs is saved)."""
 
     @staticmethod
-    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus):
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0):
         y, last = ssm_scan_fwd(u, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
-                               delta_softplus=delta_softplus, return_last_state=True)
-        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
+                               delta_softplus=delta_softplus, return_last_state=True, h0=h0)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0)
         ctx.delta_softplus = delta_softplus
         return y, last
 
     @staticmethod
     def backward(ctx, dy, dlast):
-        u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
+        u, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
         dy = torch.zeros_like(u, dtype=torch.float32) if dy is None else dy.float().contiguous()
         dlast = None if dlast is None else dlast.float().contiguous()
+        want_dh0 = h0 is not None and ctx.needs_input_grad[9]
         g = ssm_scan_bwd(u, delta, A, B, C, dy, D=D, z=z, delta_bias=delta_bias,
-                         delta_softplus=ctx.delta_softplus, dlast_state=dlast)
+                         delta_softplus=ctx.delta_softplus, dlast_state=dlast, h0=h0,
+                         return_dh0=want_dh0)
         cast = lambda t, like: None if t is None else t.to(like.dtype)
         return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B),
                 cast(g["dC"], C), g["dD"] if D is not None else None,
                 cast(g["dz"], z) if z is not None else None,
-                g["ddelta_bias"] if delta_bias is not None else None, None)
+                g["ddelta_bias"] if delta_bias is not None else None, None,
+                g["dh0"] if want_dh0 else None)
 
 
-def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False):
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                   h0=None):
     """Differentiable forward scan on CUDA tensors: returns (y, last_state)
     and, under autograd, gradients for every tensor input from the library's
-    backward kernel.  Gradients are computed in fp32 and returned in each
+    backward kernel, h0 (the initial state, (batch, dim, N) fp32, or None for
+    zero) included.  Gradients are computed in fp32 and returned in each
     input's dtype."""
-    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus))
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus), h0)

@@ -35,7 +35,8 @@ SSM_IO_F32 = 0
 SSM_IO_BF16 = 1
 
 # every symbol include/ssm_scan.h declares
-EXPORTS = ("ssm_build_id", "ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
+EXPORTS = ("ssm_build_id", "ssm_probe_ex2", "ssm_scan_bwd", "ssm_scan_bwd_ex",
+           "ssm_scan_bwd_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_ex", "ssm_scan_fwd_host", "ssm_scan_fwd_noalloc",
            "ssm_scan_fwd_noalloc_max_scratch", "ssm_scan_fwd_noalloc_status",
            "ssm_scan_fwd_status", "ssm_scan_fwd_workspace_size", "ssm_state_step",
@@ -89,6 +90,9 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     lib.ssm_scan_bwd.restype = i32
     lib.ssm_scan_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssm_scan_bwd_ex.restype = i32
+    lib.ssm_scan_bwd_ex.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                    vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssm_scan_bwd_workspace_size.restype = i32
     lib.ssm_scan_bwd_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
     lib.ssm_scan_fwd_host.restype = i32

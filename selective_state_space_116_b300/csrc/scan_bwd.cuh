@@ -59,6 +59,7 @@ struct BwdParams {
     const float* bias;   // may be null
     const float* dy;     // (batch, dim, L) fp32
     const float* dlast;  // (batch, dim, N) fp32, may be null
+    const float* h0;     // (batch, dim, N) fp32 initial state of the forward, may be null
     float* du;           // (batch, dim, L)
     float* ddelta;       // (batch, dim, L)
     float* dz;           // (batch, dim, L), null when z is null
@@ -263,11 +264,13 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         auto g0 = [&](int i) {
             return (act[k] && i < S && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
         };
+        auto s0 = [&](int i) { return (act[k] && i < S && p.h0) ? p.h0[crow[k] * N + n0 + i] : 0.0f; };
 #pragma unroll
         for (int pi = 0; pi < SP; pi++) {
             A2[k * SP + pi] = make_float2(a2(2 * pi), a2(2 * pi + 1));
             g[k * SP + pi] = make_float2(g0(2 * pi), g0(2 * pi + 1));
-            dA[k * SP + pi] = h[k * SP + pi] = f2(0.0f);
+            h[k * SP + pi] = make_float2(s0(2 * pi), s0(2 * pi + 1));   // the forward's start
+            dA[k * SP + pi] = f2(0.0f);
         }
     }
     // staging role: tokens sj .. sj+EPT-1 of channel sc of the CTA

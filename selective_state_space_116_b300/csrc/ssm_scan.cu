@@ -280,12 +280,12 @@ int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
     return SSM_OK;
 }
 
-int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
-                 const void* B, const void* C, const float* D, const void* z,
-                 const float* delta_bias, int delta_softplus, const float* dy,
-                 const float* dlast_state, float* du, float* ddelta, float* dz, float* dA,
-                 float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                    const void* B, const void* C, const float* D, const void* z,
+                    const float* delta_bias, int delta_softplus, const float* dy,
+                    const float* dlast_state, const float* h0, float* du, float* ddelta,
+                    float* dz, float* dA, float* dB, float* dC, float* dD, float* ddelta_bias,
+                    float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
@@ -298,7 +298,8 @@ int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const f
         if (!aligned(q, es)) return SSM_ERR_MISALIGNED;
     for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
                           static_cast<const void*>(delta_bias), static_cast<const void*>(dy),
-                          static_cast<const void*>(dlast_state), static_cast<const void*>(du),
+                          static_cast<const void*>(dlast_state), static_cast<const void*>(h0),
+                          static_cast<const void*>(du),
                           static_cast<const void*>(ddelta), static_cast<const void*>(dz),
                           static_cast<const void*>(dA), static_cast<const void*>(dB),
                           static_cast<const void*>(dC), static_cast<const void*>(dD),
@@ -320,7 +321,7 @@ int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const f
     if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)dims->dim * 4, st) != cudaSuccess)
         return SSM_ERR_CUDA;
     ssm::bwd::BwdParams p{u, delta, A, B, C, D, z && !empty ? z : nullptr, delta_bias, dy,
-                          dlast_state, du, ddelta, z ? dz : nullptr, dA, dB, dC,
+                          dlast_state, h0, du, ddelta, z ? dz : nullptr, dA, dB, dC,
                           D ? dD : nullptr, delta_bias ? ddelta_bias : nullptr, dh0,
                           static_cast<float*>(workspace), dims->batch, dims->dim, dims->seqlen,
                           (dims->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT};
@@ -328,6 +329,17 @@ int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const f
     const bool zz = p.z != nullptr, sp = delta_softplus != 0;
     if (dims->io == SSM_IO_BF16) return bwd_bf16((int)N, p, zz, sp, st);
     return bwd_f32((int)N, p, zz, sp, st);
+}
+
+int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, int delta_softplus, const float* dy,
+                 const float* dlast_state, float* du, float* ddelta, float* dz, float* dA,
+                 float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    return ssm_scan_bwd_ex(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
+                           dlast_state, nullptr, du, ddelta, dz, dA, dB, dC, dD, ddelta_bias, dh0,
+                           workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

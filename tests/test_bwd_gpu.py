@@ -24,21 +24,24 @@ pytestmark = pytest.mark.gpu
 NAMES = ["du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"]
 
 
-def run_both(w, seed=0, with_dlast=True):
+def run_both(w, seed=0, with_dlast=True, with_h0=False):
     inp = make_scan_inputs(w, seed)
     rng = np.random.default_rng(seed + 100)
     b, d, L, N = w.batch, w.dim, w.seqlen, w.dstate
     dy = torch.from_numpy(rng.standard_normal((b, d, L)).astype(np.float32))
     dlast = torch.from_numpy(rng.standard_normal((b, d, N)).astype(np.float32)) if with_dlast else None
+    h0 = torch.from_numpy((rng.standard_normal((b, d, N)) * 3.0).astype(np.float32)) if with_h0 else None
     g = to_cuda(inp)
     got = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
                            delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
-                           dlast_state=None if dlast is None else dlast.cuda(), return_dh0=True)
+                           dlast_state=None if dlast is None else dlast.cuda(), return_dh0=True,
+                           h0=None if h0 is None else h0.cuda())
     torch.cuda.synchronize()
     ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy.double().numpy(),
                           D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
                           delta_softplus=inp["delta_softplus"],
-                          dlast=None if dlast is None else dlast.double().numpy(), nthreads=nthreads())
+                          dlast=None if dlast is None else dlast.double().numpy(),
+                          h0=None if h0 is None else h0.double().numpy(), nthreads=nthreads())
     return got, ref
 
 
@@ -69,6 +72,17 @@ def test_bwd_state_sizes(io, N):
     w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=37, dstate=N, io=io, last_state=True)
     got, ref = run_both(w, seed=N)
     check(got, ref, f"{io} N={N}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [37, 64])
+def test_bwd_from_an_initial_state(io, L):
+    """ssm_scan_bwd_ex: the forward ran from h0, so every gradient (dA and
+    ddelta through h_(-1), dh0 itself) includes it; L = 64 takes the
+    16-byte staging path, L = 37 the element-wise one with a ragged tile."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=L, dstate=16, io=io, last_state=True)
+    got, ref = run_both(w, seed=L, with_h0=True)
+    check(got, ref, f"{io} L={L} h0")
 
 
 @pytest.mark.parametrize("gate", [False, True])
@@ -135,6 +149,35 @@ def test_bwd_layer_shape_m2p8_sampled_channels():
         gt = got[gname][ds].double().cpu().numpy()
         err = np.abs(gt - r).max()
         assert err <= 1e-3 * np.abs(r).max() + 1e-6, (gname, err)
+
+
+def test_autograd_wrapper_with_initial_state():
+    """selective_scan(h0=...): the forward starts from h0 (equal to
+    ssm_scan_fwd's) and h0 gets its gradient, matching the oracle."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=45, io="f32", last_state=True)
+    inp = make_scan_inputs(w, seed=6)
+    g = to_cuda(inp)
+    rng = np.random.default_rng(9)
+    h0 = torch.from_numpy(rng.standard_normal((w.batch, w.dim, w.dstate)).astype(np.float32)).cuda()
+    leaves = {k: g[k].clone().requires_grad_(True) for k in ("u", "A")}
+    h0l = h0.clone().requires_grad_(True)
+    y, last = ssm.selective_scan(leaves["u"], g["delta"], leaves["A"], g["B"], g["C"], D=g["D"],
+                                 z=g["z"], delta_bias=g["delta_bias"], delta_softplus=True, h0=h0l)
+    y_ref, last_ref = ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                       delta_bias=g["delta_bias"], delta_softplus=True, h0=h0)
+    assert torch.equal(y.detach(), y_ref) and torch.equal(last.detach(), last_ref)
+    wy = torch.from_numpy(rng.standard_normal(tuple(y.shape)).astype(np.float32)).cuda()
+    wl = torch.from_numpy(rng.standard_normal(tuple(last.shape)).astype(np.float32)).cuda()
+    ((y * wy).sum() + (last * wl).sum()).backward()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], wy.double().cpu().numpy(),
+                          D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"], delta_softplus=True,
+                          dlast=wl.double().cpu().numpy(), h0=h0.double().cpu().numpy())
+    for gt, r, name in ((leaves["u"].grad, ref["du"], "du"), (leaves["A"].grad, ref["dA"], "dA"),
+                        (h0l.grad, ref["dh0"], "dh0")):
+        gt = gt.double().cpu().numpy()
+        assert gt.shape == r.shape, (name, gt.shape, r.shape)
+        err = np.abs(gt - r).max()
+        assert err <= 1e-3 * np.abs(r).max() + 1e-6, (name, err)
 
 
 def test_autograd_wrapper_returns_the_library_gradients():
