@@ -63,7 +63,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_scan_bwd.restype = i32
         lib.oracle_scan_bwd.argtypes = [i64, i64, i64, i64, i32, i32,
                                         vp, vp, vp, vp, vp, vp, vp, vp, i32,
-                                        dp, dp, dp, vp, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, i32]
+                                        dp, dp, dp, i32, vp, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, i32]
         _lib_cache[path] = lib
     return _lib_cache[path]
 
@@ -206,11 +206,12 @@ def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
              dlast=None, h0=None, channels=None, nthreads: int = 1,
-             lib: ctypes.CDLL | None = None):
+             lib: ctypes.CDLL | None = None, zoh: bool = False):
     """Oracle backward scan: the gradients of a loss with dLoss/dy = ``dy``
     (batch, dim, L) and dLoss/dlast_state = ``dlast`` (batch, dim, N, or
     None) with respect to every input of ``scan_fwd`` run from the initial
-    state ``h0`` (batch, dim, N, or None for zero).
+    state ``h0`` (batch, dim, N, or None for zero), with the exact
+    zero-order-hold input term when ``zoh``.
 
     Returns a dict of fp64 arrays: du, ddelta, dz (batch, dim, L; dz is None
     without z), dA (dim, N), dD, ddelta_bias (dim,), dB, dC (batch, L, N),
@@ -255,7 +256,7 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softp
                              _ptr(arrs["u"][0]), _ptr(arrs["delta"][0]), _ptr(parr["A"][0]),
                              _ptr(arrs["B"][0]), _ptr(arrs["C"][0]), _ptr(parr["D"][0]),
                              _ptr(arrs["z"][0]), _ptr(parr["bias"][0]), int(bool(delta_softplus)),
-                             _ptr(dy), _ptr(dlast), _ptr(h0), _ptr(chan), nchan, _ptr(du),
+                             _ptr(dy), _ptr(dlast), _ptr(h0), int(bool(zoh)), _ptr(chan), nchan, _ptr(du),
                              _ptr(ddelta),
                              _ptr(dz), _ptr(dA), _ptr(dD), _ptr(dbias), _ptr(dBc), _ptr(dCc),
                              _ptr(dh0), int(nthreads))

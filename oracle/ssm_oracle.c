@@ -80,6 +80,28 @@ static double input_weight(int zoh, double dt, double a) {
     return a != 0.0 ? expm1(dt * a) / a : dt;
 }
 
+/* The weight's derivatives, for the backward pass.  d w / d Delta: 1, or
+ * exp(Delta A) for the exact hold.  d w / d A: 0, or for the exact hold
+ * (Delta e^x - (e^x - 1) / A) / A with x = Delta A, which is Delta^2 psi(x),
+ * psi(x) = (x e^x - e^x + 1) / x^2 = sum_{k>=0} (k + 1) x^k / (k + 2)!; the
+ * series (to k = 29, far below double rounding for |x| < 1/2) stands in for
+ * the closed form where it would cancel, and gives Delta^2 / 2 at A = 0. */
+static double input_weight_ddt(int zoh, double dt, double a) { return zoh ? exp(dt * a) : 1.0; }
+static double input_weight_da(int zoh, double dt, double a) {
+    if (!zoh) return 0.0;
+    const double x = dt * a;
+    if (fabs(x) < 0.5) {
+        double sum = 0.0, xp = 1.0, fact = 2.0;   /* x^k, (k + 2)! */
+        for (int k = 0; k < 30; k++) {
+            sum += (k + 1) * xp / fact;
+            xp *= x;
+            fact *= (double)(k + 3);
+        }
+        return dt * dt * sum;
+    }
+    return (dt * exp(x) - expm1(x) / a) / a;
+}
+
 typedef struct {
     int64_t batch, dim, dstate, seqlen;
     int io, pio; /* element types: io for u/delta/B/C/z, pio for A/D/bias */
@@ -234,15 +256,17 @@ int oracle_state_step(int64_t batch, int64_t dim, int64_t dstate, int io, int pi
  * Delta_t = softplus(v_t) (or v_t), a_tn = exp(Delta_t A_n),
  * h_tn = a_tn h_(t-1)n + Delta_t B_tn x_t, s_t = sum_n C_tn h_tn + D x_t and
  * y_t = s_t silu(z_t) (or s_t), let g_n be the adjoint of h_tn.  The forward
- * starts from h_(-1) = h0 (zero when no initial state is given).  Going from
- * t = L-1 down to 0, starting from g = dlast:
+ * starts from h_(-1) = h0 (zero when no initial state is given); its input
+ * term is w_tn B_tn x_t with w = Delta (first order) or (exp(Delta A) - 1) / A
+ * (exact hold), w' = dw/dDelta, w_A = dw/dA (input_weight_ddt, _da).  Going
+ * from t = L-1 down to 0, starting from g = dlast:
  *
  *   ds_t   = dy_t silu(z_t)           dz_t = dy_t s_t silu'(z_t)
  *   dD    += ds_t x_t                 dx_t = ds_t D
  *   g_n   += ds_t C_tn                dC_tn = ds_t h_tn
- *   dDelta_t = sum_n g_n (A_n a_tn h_(t-1)n + B_tn x_t)
- *   dx_t  += sum_n g_n Delta_t B_tn   dB_tn = g_n Delta_t x_t
- *   dA_n  += g_n Delta_t a_tn h_(t-1)n
+ *   dDelta_t = sum_n g_n (A_n a_tn h_(t-1)n + w'_tn B_tn x_t)
+ *   dx_t  += sum_n g_n w_tn B_tn      dB_tn = g_n w_tn x_t
+ *   dA_n  += g_n (Delta_t a_tn h_(t-1)n + w_A,tn B_tn x_t)
  *   g_n    = g_n a_tn                 (the adjoint of h_(t-1)n)
  *   ddelta_t = dDelta_t sigmoid(v_t) (softplus' = sigmoid) or dDelta_t
  *   dbias += ddelta_t
@@ -260,6 +284,7 @@ typedef struct {
     int softplus_on;
     const double *dy, *dlast;   /* (batch, dim, L), (batch, dim, N) (dlast may be NULL) */
     const double* h0;           /* (batch, dim, N) initial state, or NULL for zero */
+    int zoh;                    /* input term: 0 first order, 1 exact zero-order hold */
     double *du, *ddelta, *dz, *dA, *dD, *dbias, *dBc, *dCc, *dh0;
     const int64_t* chan;        /* flat channel ids, or NULL for all */
     int64_t nchan, next;
@@ -284,8 +309,10 @@ static void bwd_channel(const bwd_job* j, int64_t k, double* hs, double* g) {
         const double dt = j->softplus_on ? softplus(v) : v;
         const double x = load(j->io, j->u, row + t);
         for (int64_t n = 0; n < N; n++) {
-            const double a = exp(dt * load(j->pio, j->A, d * N + n));
-            hs[(t + 1) * N + n] = a * hs[t * N + n] + dt * load(j->io, j->B, bc_row + t * N + n) * x;
+            const double An = load(j->pio, j->A, d * N + n);
+            const double a = exp(dt * An);
+            hs[(t + 1) * N + n] = a * hs[t * N + n] +
+                                  input_weight(j->zoh, dt, An) * load(j->io, j->B, bc_row + t * N + n) * x;
         }
     }
     /* reverse */
@@ -319,12 +346,13 @@ static void bwd_channel(const bwd_job* j, int64_t k, double* hs, double* g) {
             const double Bv = load(j->io, j->B, bc_row + t * N + n);
             const double An = load(j->pio, j->A, d * N + n);
             const double a = exp(dt * An);
+            const double w = input_weight(j->zoh, dt, An);
             g[n] += ds * Cv;
             j->dCc[(k * L + t) * N + n] = ds * h[n];
-            ddt += g[n] * (An * a * hp[n] + Bv * x);
-            dx += g[n] * dt * Bv;
-            j->dBc[(k * L + t) * N + n] = g[n] * dt * x;
-            j->dA[k * N + n] += g[n] * dt * a * hp[n];
+            ddt += g[n] * (An * a * hp[n] + input_weight_ddt(j->zoh, dt, An) * Bv * x);
+            dx += g[n] * w * Bv;
+            j->dBc[(k * L + t) * N + n] = g[n] * w * x;
+            j->dA[k * N + n] += g[n] * (dt * a * hp[n] + input_weight_da(j->zoh, dt, An) * Bv * x);
             g[n] *= a;
         }
         const double dv = j->softplus_on ? ddt * sigmoid(v) : ddt;
@@ -364,7 +392,8 @@ static void* bwd_worker(void* arg) {
  * b*dim + d; NULL means every channel in order, and then nchan must equal
  * batch*dim); see the comment above.  Inputs as for oracle_scan_fwd; dy is
  * (batch, dim, L) fp64, dlast (batch, dim, N) fp64 or NULL and h0, the
- * forward's initial state, (batch, dim, N) fp64 or NULL, all full.
+ * forward's initial state, (batch, dim, N) fp64 or NULL, all full; zoh
+ * selects the input term as for oracle_scan_fwd.
  * Outputs (fp64, compact, one row per listed channel): du, ddelta, dz
  * (nchan x L; dz may be NULL when z is), dA (nchan x N: the channel's
  * share, summed over the batch by the caller), dD, dbias (nchan), dBc, dCc
@@ -375,7 +404,7 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
                     const void* u, const void* delta, const void* A, const void* B,
                     const void* C, const void* D, const void* z, const void* delta_bias,
                     int delta_softplus, const double* dy, const double* dlast, const double* h0,
-                    const int64_t* chan, int64_t nchan, double* du, double* ddelta, double* dz,
+                    int zoh, const int64_t* chan, int64_t nchan, double* du, double* ddelta, double* dz,
                     double* dA, double* dD, double* dbias, double* dBc, double* dCc, double* dh0,
                     int nthreads) {
     if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return -1;
@@ -394,7 +423,7 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, 
     j.io = io; j.pio = pio;
     j.u = u; j.delta = delta; j.A = A; j.B = B; j.C = C; j.D = D; j.z = z;
     j.bias = delta_bias; j.softplus_on = delta_softplus;
-    j.dy = dy; j.dlast = dlast; j.h0 = h0;
+    j.dy = dy; j.dlast = dlast; j.h0 = h0; j.zoh = zoh;
     j.du = du; j.ddelta = ddelta; j.dz = dz; j.dA = dA; j.dD = dD; j.dbias = dbias;
     j.dBc = dBc; j.dCc = dCc; j.dh0 = dh0;
     j.chan = chan;

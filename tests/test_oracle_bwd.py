@@ -28,9 +28,9 @@ def make(rng, b, d, L, N, z, softplus, bias, skip):
     return x
 
 
-def loss(x, softplus, Wy, Wh, h0=None):
+def loss(x, softplus, Wy, Wh, h0=None, zoh=False):
     y, h = oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
-                           delta_bias=x["delta_bias"], delta_softplus=softplus, h0=h0)
+                           delta_bias=x["delta_bias"], delta_softplus=softplus, h0=h0, zoh=zoh)
     return float((y * Wy).sum() + (h * Wh).sum())
 
 
@@ -121,6 +121,56 @@ def test_backward_oracle_with_initial_state_matches_finite_differences(opts):
         hp = h0.copy(); hp.reshape(-1)[i] += EPS
         hm = h0.copy(); hm.reshape(-1)[i] -= EPS
         fd = (loss(x, sp, Wy, Wh, hp) - loss(x, sp, Wy, Wh, hm)) / (2 * EPS)
+        got = g["dh0"].reshape(-1)[i]
+        assert abs(fd - got) <= RTOL * (1 + abs(fd)), ("h0", int(i), fd, got)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(z=True, softplus=True, bias=True, skip=True),
+    dict(z=False, softplus=False, bias=False, skip=True),
+])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_backward_oracle_exact_hold_matches_finite_differences(opts, with_h0):
+    """The exact zero-order-hold input term ((exp(Delta A) - 1) / A B u): every
+    gradient against central differences of the forward oracle.  Some A are
+    0 and some -1e-3 (|Delta A| below the series switch of dw/dA), the rest
+    ordinary, so dA is checked on both sides of the switch and at A = 0."""
+    b, d, L, N = 2, 3, 8, 4
+    rng = np.random.default_rng(31)
+    x = make(rng, b, d, L, N, **opts)
+    x["A"][0, 0] = 0.0
+    x["A"][1, 1] = -1e-3
+    x["A"][2, 2] = -1.0 / 16
+    sp = opts["softplus"]
+    Wy = rng.standard_normal((b, d, L))
+    Wh = rng.standard_normal((b, d, N))
+    h0 = rng.standard_normal((b * d, N)) if with_h0 else None
+    g = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], Wy, D=x["D"], z=x["z"],
+                        delta_bias=x["delta_bias"], delta_softplus=sp, dlast=Wh,
+                        h0=None if h0 is None else h0.reshape(b, d, N), zoh=True)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    for name, gname in names.items():
+        if x[name] is None:
+            continue
+        flat = x[name].reshape(-1)
+        idx = np.arange(flat.size) if name == "A" else \
+            rng.choice(flat.size, size=min(flat.size, 10), replace=False)
+        for i in idx:
+            keep = flat[i]
+            flat[i] = keep + EPS
+            lp = loss(x, sp, Wy, Wh, h0, zoh=True)
+            flat[i] = keep - EPS
+            lm = loss(x, sp, Wy, Wh, h0, zoh=True)
+            flat[i] = keep
+            fd = (lp - lm) / (2 * EPS)
+            got = g[gname].reshape(-1)[i]
+            assert abs(fd - got) <= RTOL * (1 + abs(fd)), (name, int(i), fd, got)
+    hb = np.zeros((b * d, N)) if h0 is None else h0
+    for i in rng.choice(hb.size, size=6, replace=False):
+        hp = hb.copy(); hp.reshape(-1)[i] += EPS
+        hm = hb.copy(); hm.reshape(-1)[i] -= EPS
+        fd = (loss(x, sp, Wy, Wh, hp, zoh=True) - loss(x, sp, Wy, Wh, hm, zoh=True)) / (2 * EPS)
         got = g["dh0"].reshape(-1)[i]
         assert abs(fd - got) <= RTOL * (1 + abs(fd)), ("h0", int(i), fd, got)
 
