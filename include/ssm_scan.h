@@ -86,7 +86,7 @@ typedef enum ssm_status {
     SSM_ERR_ALIAS = -8,         /* an output overlaps an input */
     SSM_ERR_TIMEOUT = -9,       /* a bounded on-device wait gave up */
     SSM_ERR_TOO_LARGE = -10,    /* needs more scratch than ssm_scan_fwd_noalloc holds */
-    SSM_ERR_BAD_OPTION = -11,   /* a field of ssm_scan_opts is out of range */
+    SSM_ERR_BAD_OPTION = -11,   /* an option (a field of ssm_scan_opts, an input_term) is out of range */
     SSM_ERR_DEVICE = -12        /* a -DSSM_DEBUG build's bounds check failed on the device */
 } ssm_status;
 
@@ -285,21 +285,30 @@ SSM_API int ssm_scan_bwd(const ssm_dims* dims,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * ssm_scan_bwd for a forward scan that started from the initial state h0
- * (batch, dim, dstate) fp32 (device; NULL: zero, i.e. ssm_scan_bwd), the
- * state ssm_scan_fwd_ex takes in ssm_scan_opts.h0 ("Mamba remembers by
- * forgetting, read closely", interactiveml.org: the selective_scan
- * recurrence started from a given state).  The recomputed forward states
- * start from h0, so every gradient includes its effect (dA and ddelta
- * through h_(-1)); dh0 is the gradient with respect to h0.  The first-order
- * input term only (the ZOH term and the fused convolution have no backward
- * here).  Other arguments, workspace and errors as for ssm_scan_bwd.
+ * ssm_scan_bwd for the forward scan ssm_scan_fwd_ex runs with
+ * ssm_scan_opts.h0 = h0 and ssm_scan_opts.input_term = input_term
+ * ("Mamba remembers by forgetting, read closely", interactiveml.org: the
+ * selective_scan recurrence started from a given state, and its exact
+ * zero-order-hold discretisation).
+ *   h0          (batch, dim, dstate) fp32 initial state (device), or NULL
+ *               for zero.  The recomputed forward states start from h0, so
+ *               every gradient includes its effect (dA and ddelta through
+ *               h_(-1)); dh0 is the gradient with respect to h0.
+ *   input_term  an ssm_input_term.  With SSM_INPUT_ZOH the input weight
+ *               w = (exp(Delta A) - 1) / A of every state is differentiated
+ *               too: dw/dDelta = exp(Delta A), dw/dA = (Delta exp(Delta A) -
+ *               w) / A (Delta^2 / 2 at A = 0); out of range:
+ *               SSM_ERR_BAD_OPTION.
+ * h0 = NULL with SSM_INPUT_DELTA_B is ssm_scan_bwd.  The fused convolution
+ * of ssm_scan_opts has no backward here.  Other arguments, workspace and
+ * errors as for ssm_scan_bwd.
  */
 SSM_API int ssm_scan_bwd_ex(const ssm_dims* dims,
                  const void* u, const void* delta, const float* A,
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus,
                  const float* dy, const float* dlast_state, const float* h0,
+                 int input_term,
                  float* du, float* ddelta, float* dz, float* dA,
                  float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
                  void* workspace, size_t workspace_bytes, void* stream);

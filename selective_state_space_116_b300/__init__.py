@@ -277,11 +277,13 @@ def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
-                 dlast_state=None, return_dh0=False, workspace=None, h0=None):
+                 dlast_state=None, return_dh0=False, workspace=None, h0=None,
+                 input_term="delta_b"):
     """Backward selective scan (CUDA tensors): the gradients of a loss with
     dLoss/dy = ``dy`` (and dLoss/dlast_state = ``dlast_state``) with respect
     to the inputs of ``ssm_scan_fwd`` run from the initial state ``h0``
-    ((batch, dim, N) fp32, or None for zero; the first-order input term).
+    ((batch, dim, N) fp32, or None for zero) with the input term
+    ``input_term`` ("delta_b" or "zoh", as for ``ssm_scan_fwd``).
     The forward states are recomputed inside the kernel.  Returns a dict of
     fp32 tensors: du, ddelta (gradient of the raw delta), dz (None without
     z), dA, dB, dC, dD (None without D), ddelta_bias (None without
@@ -306,6 +308,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     _check(dy, "dy", (batch, dim, L), torch.float32, device)
     _check(dlast_state, "dlast_state", (batch, dim, N), torch.float32, device, optional=True)
     _check(h0, "h0", (batch, dim, N), torch.float32, device, optional=True)
+    if input_term not in ("delta_b", "zoh"):
+        raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
+    term = _lib.SSM_INPUT_ZOH if input_term == "zoh" else _lib.SSM_INPUT_DELTA_B
     f32 = dict(dtype=torch.float32, device=device)
     g = {"du": torch.empty((batch, dim, L), **f32), "ddelta": torch.empty((batch, dim, L), **f32),
          "dz": torch.empty((batch, dim, L), **f32) if z is not None else None,
@@ -325,7 +330,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.ssm_scan_bwd_ex(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                              _ptr(D), _ptr(z), _ptr(delta_bias), 1 if delta_softplus else 0,
-                             _ptr(dy), _ptr(dlast_state), _ptr(h0), _ptr(g["du"]),
+                             _ptr(dy), _ptr(dlast_state), _ptr(h0), term, _ptr(g["du"]),
                              _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
                              _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
                              _ptr(workspace), ws_bytes, _stream(device))
@@ -339,11 +344,13 @@ class _SelectiveScan(torch.autograd.Function):
     recomputes the forward states; nothing but the inputs is saved)."""
 
     @staticmethod
-    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0):
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, input_term):
         y, last = ssm_scan_fwd(u, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
-                               delta_softplus=delta_softplus, return_last_state=True, h0=h0)
+                               delta_softplus=delta_softplus, return_last_state=True, h0=h0,
+                               input_term=input_term)
         ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0)
         ctx.delta_softplus = delta_softplus
+        ctx.input_term = input_term
         return y, last
 
     @staticmethod
@@ -354,20 +361,24 @@ class _SelectiveScan(torch.autograd.Function):
         want_dh0 = h0 is not None and ctx.needs_input_grad[9]
         g = ssm_scan_bwd(u, delta, A, B, C, dy, D=D, z=z, delta_bias=delta_bias,
                          delta_softplus=ctx.delta_softplus, dlast_state=dlast, h0=h0,
-                         return_dh0=want_dh0)
+                         return_dh0=want_dh0, input_term=ctx.input_term)
         cast = lambda t, like: None if t is None else t.to(like.dtype)
         return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B),
                 cast(g["dC"], C), g["dD"] if D is not None else None,
                 cast(g["dz"], z) if z is not None else None,
                 g["ddelta_bias"] if delta_bias is not None else None, None,
-                g["dh0"] if want_dh0 else None)
+                g["dh0"] if want_dh0 else None, None)
 
 
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
-                   h0=None):
+                   h0=None, input_term="delta_b"):
     """Differentiable forward scan on CUDA tensors: returns (y, last_state)
     and, under autograd, gradients for every tensor input from the library's
     backward kernel, h0 (the initial state, (batch, dim, N) fp32, or None for
-    zero) included.  Gradients are computed in fp32 and returned in each
+    zero) included.  ``input_term`` is "delta_b" or "zoh", as for
+    ``ssm_scan_fwd``.  Gradients are computed in fp32 and returned in each
     input's dtype."""
-    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus), h0)
+    if input_term not in ("delta_b", "zoh"):
+        raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus), h0,
+                                input_term)

@@ -1,0 +1,63 @@
+// Backward-scan launch and dispatch over the compile-time variants (state
+// size, gate, softplus, vector staging, input term); instantiated by bwd.cu
+// (first-order input term) and bwd_zoh.cu (exact zero-order hold).
+#pragma once
+#include "host_plan.h"
+
+namespace ssm_host {
+namespace bwd_detail {
+
+// Channels per thread: two at N = 16 (their dB, dC products summed in
+// registers before the shared-memory reduction), one for smaller states.
+template <int N> constexpr int bwd_channels_per_thread() { return N == 16 ? 2 : 1; }
+
+template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH>
+int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
+    constexpr int K = bwd_channels_per_thread<N>();
+    using Sh = ssm::bwd::BwdShape<T, N, K>;
+    auto kern = ssm::bwd::scan_bwd_kernel<T, N, K, Z, SP, VEC, ZOH>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    const dim3 grid((unsigned)((p.dim + Sh::CH - 1) / Sh::CH), (unsigned)p.batch);
+    kern<<<grid, ssm::bwd::kThreads, Sh::SMEM, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int N, bool VEC, bool ZOH>
+int dispatch_bwd_zs(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
+    if (z && sp) return launch_bwd<T, N, true, true, VEC, ZOH>(p, st);
+    if (z) return launch_bwd<T, N, true, false, VEC, ZOH>(p, st);
+    if (sp) return launch_bwd<T, N, false, true, VEC, ZOH>(p, st);
+    return launch_bwd<T, N, false, false, VEC, ZOH>(p, st);
+}
+
+inline bool bwd_aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+// The vector path (asynchronous staging, 16-byte stores) needs whole tiles
+// and 16-byte aligned sequence tensors.
+template <typename T, int N, bool ZOH>
+int dispatch_bwd_n(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
+    const bool vec = p.L % ssm::bwd::kTT == 0 && bwd_aligned16(p.u) && bwd_aligned16(p.delta) &&
+                     bwd_aligned16(p.B) && bwd_aligned16(p.C) && bwd_aligned16(p.dy) &&
+                     bwd_aligned16(p.du) && bwd_aligned16(p.ddelta) &&
+                     (!z || (bwd_aligned16(p.z) && bwd_aligned16(p.dz)));
+    return vec ? dispatch_bwd_zs<T, N, true, ZOH>(p, z, sp, st)
+               : dispatch_bwd_zs<T, N, false, ZOH>(p, z, sp, st);
+}
+
+template <typename T, bool ZOH>
+int dispatch_bwd(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
+    switch (n) {
+        case 1: return dispatch_bwd_n<T, 1, ZOH>(p, z, sp, st);
+        case 2: return dispatch_bwd_n<T, 2, ZOH>(p, z, sp, st);
+        case 4: return dispatch_bwd_n<T, 4, ZOH>(p, z, sp, st);
+        case 8: return dispatch_bwd_n<T, 8, ZOH>(p, z, sp, st);
+        case 16: return dispatch_bwd_n<T, 16, ZOH>(p, z, sp, st);
+    }
+    return SSM_ERR_UNSUPPORTED_N;
+}
+
+}  // namespace bwd_detail
+}  // namespace ssm_host

@@ -231,8 +231,10 @@ int fwd_chunked_bf16(int n, const ssm::ScanParams& p, const ChunkPlan& c, bool z
 // Single-token state step.
 int step_f32(int n, const ssm::StepParams& p, bool z, bool sp, bool vec, cudaStream_t st);
 int step_bf16(int n, const ssm::StepParams& p, bool z, bool sp, bool vec, cudaStream_t st);
-// Backward scan.
+// Backward scan: first-order input term, exact zero-order hold.
 int bwd_f32(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
 int bwd_bf16(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
+int bwd_zoh_f32(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
+int bwd_zoh_bf16(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
 
 }  // namespace ssm_host

@@ -16,6 +16,15 @@
 //             dB_tn = sum_channels g_tn Delta_t x_t, dC_tn = sum_channels ds_t h_tn
 //             dz_t = dy_t (s_t + D x_t) silu'(z_t),  dD = sum_t ds_t x_t
 //
+// With the exact zero-order hold (ZOH) the input term is w_tn B_tn x_t with
+// w = (exp(Delta A) - 1) / A per state ("Mamba remembers by forgetting, read
+// closely", interactiveml.org, the discretisation and the selective_scan
+// recurrence): dw/dDelta = a, dw/dA = (Delta a - w) / A, so
+//             dx_t = ds_t D + sum_n g_tn w_tn B_tn
+//             dDelta_t = r_t + x_t v_t,             v_t = sum_n g_tn a_tn B_tn
+//             dA_n = sum_t g_tn (Delta_t a_tn h_(t-1)n + dw/dA_tn B_tn x_t)
+//             dB_tn = sum_channels g_tn w_tn x_t
+//
 // Work split.  A thread holds S = min(N, 4) states of K channels (the same
 // batch row); the G = N / S adjacent lanes of a "slot" hold the whole state of
 // those K channels.  A CTA of one warp covers SLOTS = 32 / G slots, i.e.
@@ -164,6 +173,47 @@ __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 // 2^x of both lanes on the special-function unit
 __device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
 
+// Exact zero-order hold, for a pair of states: e = Delta A log2(e), a = 2^e,
+// ia = 1 / A (0 where A = 0).
+// The weight w = (exp(Delta A) - 1) / A = (a - 1) ia, except for |e| < 1/8,
+// where a - 1 keeps only the absolute accuracy of 2^x; there the series
+// Delta (1 + x / 2 + x^2 / 6 + x^3 / 24) in x = Delta A (Delta at A = 0)
+// is used, as in the forward scan.
+constexpr float kZohW = 0.125f;
+constexpr float kW1 = 0.34657359027997264f;    // ln 2 / 2
+constexpr float kW2 = 0.08007550231970023f;    // (ln 2)^2 / 6
+constexpr float kW3 = 0.013876027166205394f;   // (ln 2)^3 / 24
+__device__ __forceinline__ float2 zoh_weight(float2 a, float2 e, float2 dt, float2 ia) {
+    float2 w = __fmul2_rn(__fadd2_rn(a, f2(-1.0f)), ia);
+    float2 t = __ffma2_rn(e, f2(kW3), f2(kW2));
+    t = __ffma2_rn(e, t, f2(kW1));
+    t = __ffma2_rn(e, t, f2(1.0f));
+    const float2 ws = __fmul2_rn(dt, t);
+    if (fabsf(e.x) < kZohW) w.x = ws.x;
+    if (fabsf(e.y) < kZohW) w.y = ws.y;
+    return w;
+}
+// dw/dA = (Delta a - w) / A = Delta^2 psi(x), psi(x) = (x e^x - e^x + 1) / x^2
+// = sum_k (k + 1) x^k / (k + 2)!.  Where |x| < 1/2 the difference Delta a - w
+// cancels, and psi is summed to k = 7 instead (the first term left out is
+// below 3e-8 of psi there); the coefficients are in powers of e = x log2(e).
+constexpr float kZohWA = 0.72134752044448170f;   // |x| < 1/2
+__device__ __forceinline__ float2 zoh_weight_da(float2 a, float2 e, float2 dt, float2 ia, float2 w) {
+    float2 wa = __fmul2_rn(__ffma2_rn(dt, a, make_float2(-w.x, -w.y)), ia);
+    // (k + 1) (ln 2)^k / (k + 2)!, k = 7 down to 0
+    float2 t = __ffma2_rn(e, f2(1.694748200451093e-06f), f2(1.925441299172701e-05f));
+    t = __ffma2_rn(e, t, f2(0.0001904794020918349f));
+    t = __ffma2_rn(e, t, f2(0.0016030215179380792f));
+    t = __ffma2_rn(e, t, f2(0.011100821732964315f));
+    t = __ffma2_rn(e, t, f2(0.060056626739775174f));
+    t = __ffma2_rn(e, t, f2(0.23104906018664842f));
+    t = __ffma2_rn(e, t, f2(0.5f));
+    const float2 ws = __fmul2_rn(__fmul2_rn(dt, dt), t);
+    if (fabsf(e.x) < kZohWA) wa.x = ws.x;
+    if (fabsf(e.y) < kZohWA) wa.y = ws.y;
+    return wa;
+}
+
 // cp.async of `bytes` (4, 8, 16 or 32) from global to shared memory, both
 // aligned to min(bytes, 16); src_ok false fills zeros
 template <int BYTES>
@@ -224,8 +274,10 @@ __device__ __forceinline__ void stg_row(float* dst, const float* v, int valid) {
 }
 
 // VEC: L % 8 == 0 and every tensor 16-byte aligned (cp.async staging, vector
-// stores); otherwise bounds-checked scalar copies.
-template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC>
+// stores); otherwise bounds-checked scalar copies.  ZOH: the exact
+// zero-order-hold input term; the records then carry x where they carry
+// Delta x for the first-order term.
+template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC, bool ZOH>
 __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<T, N, K>;
     constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH;
@@ -254,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     int64_t crow[K];                 // flat channel b * dim + d (0 when inactive)
     float* ckp[K];
     float2 A2[KP], g[KP], dA[KP], h[KP];   // A log2(e), adjoint, dA sums, state
+    float2 IA[KP];                          // 1 / A (ZOH; 0 where A = 0)
 #pragma unroll
     for (int k = 0; k < K; k++) {
         const int64_t d = d0 + slot + k * SLOTS;
@@ -261,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         crow[k] = act[k] ? b * p.dim + d : 0;
         ckp[k] = p.ckpt + crow[k] * p.ntiles * N + n0;
         auto a2 = [&](int i) { return (act[k] && i < S) ? p.A[d * N + n0 + i] * kLog2e : 0.0f; };
+        auto ia = [&](int i) {
+            const float av = (act[k] && i < S) ? p.A[d * N + n0 + i] : 0.0f;
+            return (ZOH && av != 0.0f) ? 1.0f / av : 0.0f;
+        };
         auto g0 = [&](int i) {
             return (act[k] && i < S && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
         };
@@ -268,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
         for (int pi = 0; pi < SP; pi++) {
             A2[k * SP + pi] = make_float2(a2(2 * pi), a2(2 * pi + 1));
+            IA[k * SP + pi] = make_float2(ia(2 * pi), ia(2 * pi + 1));
             g[k * SP + pi] = make_float2(g0(2 * pi), g0(2 * pi + 1));
             h[k * SP + pi] = make_float2(s0(2 * pi), s0(2 * pi + 1));   // the forward's start
             dA[k * SP + pi] = f2(0.0f);
@@ -345,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
                 ds = dyr[e] * zr[e] * sg;
                 dzf = dyr[e] * sg * fmaf(zr[e], 1.0f - sg, 1.0f);
             }
-            wrec(sc, sj + e) = make_float4(dt, dt * xr[e], ds, 0.0f);
+            wrec(sc, sj + e) = make_float4(dt, ZOH ? xr[e] : dt * xr[e], ds, 0.0f);
             if (full) {
                 ex[e][0] = xr[e];
                 ex[e][1] = dzf;
@@ -369,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         const int64_t goff1 = (b * p.dim + (okc1 ? d0 + sc1 : 0)) * L + sj1;
         const float bias1 = (p.bias && okc1) ? p.bias[d0 + sc1] : 0.0f;
         unsigned char* raw1 = smem + Sh::OFF1_RAW + (sc1 * T1 + sj1) * ES;
-        // (Delta, Delta x) of channel c, token j of the tile
+        // (Delta, Delta x) of channel c, token j of the tile ((Delta, x) with ZOH)
         auto w1rec = [&](int c, int j) -> float2& {
             return *reinterpret_cast<float2*>(smem + Sh::OFF1_W + c * Sh::W1_ROW + j * 8);
         };
@@ -415,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
                     const bool ok = okc1 && t0 + sj1 + e0 + e < L;
                     const float v = vr[e] + bias1;
                     const float dt = ok ? (SOFTPLUS ? softplus(v) : v) : 0.0f;
-                    w1rec(sc1, sj1 + e0 + e) = make_float2(dt, dt * xr[e]);
+                    w1rec(sc1, sj1 + e0 + e) = make_float2(dt, ZOH ? xr[e] : dt * xr[e]);
                 }
             }
             const T* rb = reinterpret_cast<const T*>(smem + Sh::OFF1_RB);
@@ -450,8 +508,11 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
                     for (int pi = 0; pi < SP; pi++) {
                         const int q = k * SP + pi;
-                        const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
-                        h[q] = __ffma2_rn(a, h[q], __fmul2_rn(f2(w.y), Bv[pi]));
+                        const float2 e = __fmul2_rn(f2(w.x), A2[q]);
+                        const float2 a = ex2x2(e);
+                        float2 in = __fmul2_rn(f2(w.y), Bv[pi]);
+                        if constexpr (ZOH) in = __fmul2_rn(zoh_weight(a, e, f2(w.x), IA[q]), in);
+                        h[q] = __ffma2_rn(a, h[q], in);
                     }
                 }
             }
@@ -502,8 +563,11 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
                 for (int pi = 0; pi < SP; pi++) {
                     const int q = k * SP + pi;
-                    const float2 a = ex2x2(__fmul2_rn(f2(w.x), A2[q]));
-                    hs[j + 1][q] = __ffma2_rn(a, hs[j][q], __fmul2_rn(f2(w.y), Bv[pi]));
+                    const float2 e = __fmul2_rn(f2(w.x), A2[q]);
+                    const float2 a = ex2x2(e);
+                    float2 in = __fmul2_rn(f2(w.y), Bv[pi]);
+                    if constexpr (ZOH) in = __fmul2_rn(zoh_weight(a, e, f2(w.x), IA[q]), in);
+                    hs[j + 1][q] = __ffma2_rn(a, hs[j][q], in);
                 }
             }
         }
@@ -515,25 +579,37 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             ld_pairs<S>(CC + j * N + n0, Cv);
 #pragma unroll
             for (int k = 0; k < K; k++) {
-                const float4 w = wrec(slot + k * SLOTS, j);   // Delta, Delta x, ds
+                const float4 w = wrec(slot + k * SLOTS, j);   // Delta, Delta x (ZOH: x), ds
                 const float2 dt = f2(w.x), dtx = f2(w.y), ds = f2(w.z);
-                float2 sa = f2(0.0f), qa = f2(0.0f), ra = f2(0.0f);
+                float2 sa = f2(0.0f), qa = f2(0.0f), ra = f2(0.0f), va = f2(0.0f);
 #pragma unroll
                 for (int pi = 0; pi < SP; pi++) {
                     const int q = k * SP + pi;
-                    const float2 a = ex2x2(__fmul2_rn(dt, A2[q]));
+                    const float2 e = __fmul2_rn(dt, A2[q]);
+                    const float2 a = ex2x2(e);
                     g[q] = __ffma2_rn(ds, Cv[pi], g[q]);                      // + ds C
                     if constexpr (HAS_Z) sa = __ffma2_rn(Cv[pi], hs[j + 1][q], sa);
-                    qa = __ffma2_rn(g[q], Bv[pi], qa);
                     pc[pi] = k == 0 ? __fmul2_rn(ds, hs[j + 1][q]) : __ffma2_rn(ds, hs[j + 1][q], pc[pi]);
-                    pb[pi] = k == 0 ? __fmul2_rn(g[q], dtx) : __ffma2_rn(g[q], dtx, pb[pi]);
                     const float2 ga = __fmul2_rn(g[q], a);
+                    if constexpr (ZOH) {
+                        const float2 wq = zoh_weight(a, e, dt, IA[q]);
+                        const float2 gw = __fmul2_rn(g[q], wq);
+                        qa = __ffma2_rn(gw, Bv[pi], qa);                      // g w B
+                        pb[pi] = k == 0 ? __fmul2_rn(gw, dtx) : __ffma2_rn(gw, dtx, pb[pi]);
+                        va = __ffma2_rn(ga, Bv[pi], va);                      // g a B
+                        const float2 gwa = __fmul2_rn(g[q], zoh_weight_da(a, e, dt, IA[q], wq));
+                        dA[q] = __ffma2_rn(gwa, __fmul2_rn(Bv[pi], dtx), dA[q]);   // g dw/dA B x
+                    } else {
+                        qa = __ffma2_rn(g[q], Bv[pi], qa);
+                        pb[pi] = k == 0 ? __fmul2_rn(g[q], dtx) : __ffma2_rn(g[q], dtx, pb[pi]);
+                    }
                     const float2 pp = __fmul2_rn(ga, hs[j][q]);              // g a h_(t-1)
                     ra = __ffma2_rn(A2[q], pp, ra);
                     dA[q] = __ffma2_rn(dt, pp, dA[q]);
                     g[q] = ga;
                 }
-                rrec(slot + k * SLOTS, j, gi) = make_float4(sa.x + sa.y, qa.x + qa.y, ra.x + ra.y, 0.0f);
+                rrec(slot + k * SLOTS, j, gi) =
+                    make_float4(sa.x + sa.y, qa.x + qa.y, ra.x + ra.y, ZOH ? va.x + va.y : 0.0f);
             }
             st_pairs<S>(P + slot * Sh::P_ROW + j * 2 * N + n0, pb);
             st_pairs<S>(P + slot * Sh::P_ROW + j * 2 * N + N + n0, pc);
@@ -579,10 +655,16 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
                 for (int l = 1; l < G; l++) {
                     const float4 v = rrec(sc, j, l);
                     rs.x += v.x; rs.y += v.y; rs.z += v.z;
+                    if constexpr (ZOH) rs.w += v.w;
                 }
                 const float4 w = wrec(sc, j);
-                dxo[e] = fmaf(w.z, D_c, w.x * rs.y);                           // ds D + Delta q
-                dvo[e] = fmaf(ex[e][0], rs.y, rs.z * kLn2) * ex[e][2];         // (r + x q) softplus'
+                if constexpr (ZOH) {
+                    dxo[e] = fmaf(w.z, D_c, rs.y);                             // ds D + sum g w B
+                    dvo[e] = fmaf(ex[e][0], rs.w, rs.z * kLn2) * ex[e][2];     // (r + x v) softplus'
+                } else {
+                    dxo[e] = fmaf(w.z, D_c, w.x * rs.y);                       // ds D + Delta q
+                    dvo[e] = fmaf(ex[e][0], rs.y, rs.z * kLn2) * ex[e][2];     // (r + x q) softplus'
+                }
                 dzo[e] = ex[e][1] * fmaf(D_c, ex[e][0], rs.x);                 // dy (s + D x) silu'
                 if (okc && t0 + j < L) {
                     dD_acc = fmaf(w.z, ex[e][0], dD_acc);

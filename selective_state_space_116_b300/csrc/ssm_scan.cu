@@ -283,12 +283,14 @@ int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
 int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, const float* A,
                     const void* B, const void* C, const float* D, const void* z,
                     const float* delta_bias, int delta_softplus, const float* dy,
-                    const float* dlast_state, const float* h0, float* du, float* ddelta,
-                    float* dz, float* dA, float* dB, float* dC, float* dD, float* ddelta_bias,
-                    float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+                    const float* dlast_state, const float* h0, int input_term, float* du,
+                    float* ddelta, float* dz, float* dA, float* dB, float* dC, float* dD,
+                    float* ddelta_bias, float* dh0, void* workspace, size_t workspace_bytes,
+                    void* stream) {
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
+    if (input_term != SSM_INPUT_DELTA_B && input_term != SSM_INPUT_ZOH) return SSM_ERR_BAD_OPTION;
     const bool empty = dims->seqlen == 0;
     if (!A || !dA || (!empty && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)))
         return SSM_ERR_NULL_ARG;
@@ -327,6 +329,10 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
                           (dims->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT};
     if (empty) p.z = nullptr;
     const bool zz = p.z != nullptr, sp = delta_softplus != 0;
+    if (input_term == SSM_INPUT_ZOH) {
+        if (dims->io == SSM_IO_BF16) return bwd_zoh_bf16((int)N, p, zz, sp, st);
+        return bwd_zoh_f32((int)N, p, zz, sp, st);
+    }
     if (dims->io == SSM_IO_BF16) return bwd_bf16((int)N, p, zz, sp, st);
     return bwd_f32((int)N, p, zz, sp, st);
 }
@@ -338,8 +344,8 @@ int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const f
                  float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
                  void* workspace, size_t workspace_bytes, void* stream) {
     return ssm_scan_bwd_ex(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
-                           dlast_state, nullptr, du, ddelta, dz, dA, dB, dC, dD, ddelta_bias, dh0,
-                           workspace, workspace_bytes, stream);
+                           dlast_state, nullptr, SSM_INPUT_DELTA_B, du, ddelta, dz, dA, dB, dC, dD,
+                           ddelta_bias, dh0, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

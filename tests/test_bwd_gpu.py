@@ -24,8 +24,10 @@ pytestmark = pytest.mark.gpu
 NAMES = ["du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"]
 
 
-def run_both(w, seed=0, with_dlast=True, with_h0=False):
+def run_both(w, seed=0, with_dlast=True, with_h0=False, zoh=False, edit=None):
     inp = make_scan_inputs(w, seed)
+    if edit is not None:
+        edit(inp)
     rng = np.random.default_rng(seed + 100)
     b, d, L, N = w.batch, w.dim, w.seqlen, w.dstate
     dy = torch.from_numpy(rng.standard_normal((b, d, L)).astype(np.float32))
@@ -35,13 +37,15 @@ def run_both(w, seed=0, with_dlast=True, with_h0=False):
     got = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
                            delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
                            dlast_state=None if dlast is None else dlast.cuda(), return_dh0=True,
-                           h0=None if h0 is None else h0.cuda())
+                           h0=None if h0 is None else h0.cuda(),
+                           input_term="zoh" if zoh else "delta_b")
     torch.cuda.synchronize()
     ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy.double().numpy(),
                           D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
                           delta_softplus=inp["delta_softplus"],
                           dlast=None if dlast is None else dlast.double().numpy(),
-                          h0=None if h0 is None else h0.double().numpy(), nthreads=nthreads())
+                          h0=None if h0 is None else h0.double().numpy(), nthreads=nthreads(),
+                          zoh=zoh)
     return got, ref
 
 
@@ -83,6 +87,46 @@ def test_bwd_from_an_initial_state(io, L):
     w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=L, dstate=16, io=io, last_state=True)
     got, ref = run_both(w, seed=L, with_h0=True)
     check(got, ref, f"{io} L={L} h0")
+
+
+def zero_and_small_A(inp):
+    """A = 0 on one channel and |A| = 1e-3 on another, so that Delta A falls
+    on both sides of the kernel's series switches and on their limit."""
+    inp["A"][0, :] = 0.0
+    inp["A"][1, :] = -1e-3
+    inp["A"][2, ::2] = -1e-4
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("L", [37, 64])
+def test_bwd_exact_zero_order_hold(io, N, L):
+    """ssm_scan_bwd_ex with the exact zero-order-hold input term, from an
+    initial state: every gradient against the oracle's (pinned by finite
+    differences of the forward oracle with the same term), with A = 0 and
+    A near 0 on some channels; L = 64 stages 16 bytes at a time, L = 37 has a
+    ragged tile."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=L, dstate=N, io=io, last_state=True)
+    got, ref = run_both(w, seed=L + N, with_h0=True, zoh=True, edit=zero_and_small_A)
+    check(got, ref, f"{io} N={N} L={L} zoh")
+
+
+def test_bwd_exact_zero_order_hold_long_sequence():
+    """The exact-hold backward over 2048 tokens with softplus(delta) up to
+    about 2 (Delta A down to about -30: a = exp(Delta A) underflows to 0 and
+    the weight is -1/A), no initial state, against the oracle."""
+    w = WORKLOADS["m130"].scaled(batch=1, dim=40, seqlen=2048, dstate=16, io="bf16",
+                                 last_state=True, bias_range=(-1.0, 2.0))
+    got, ref = run_both(w, seed=5, zoh=True)
+    check(got, ref, "zoh L=2048")
+
+
+def test_bwd_rejects_an_unknown_input_term():
+    w = WORKLOADS["m130"].scaled(batch=1, dim=8, seqlen=16, dstate=4, io="f32")
+    g = to_cuda(make_scan_inputs(w, 0))
+    dy = torch.zeros((1, 8, 16), device="cuda")
+    with pytest.raises(ValueError):
+        ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, input_term="exact")
 
 
 @pytest.mark.parametrize("gate", [False, True])
@@ -178,6 +222,39 @@ def test_autograd_wrapper_with_initial_state():
         assert gt.shape == r.shape, (name, gt.shape, r.shape)
         err = np.abs(gt - r).max()
         assert err <= 1e-3 * np.abs(r).max() + 1e-6, (name, err)
+
+
+def test_autograd_wrapper_exact_zero_order_hold():
+    """selective_scan(input_term="zoh"): the forward equals ssm_scan_fwd's
+    with the same term bit for bit, and every gradient matches the oracle's
+    backward of the exact-hold recurrence."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=45, io="f32", last_state=True)
+    inp = make_scan_inputs(w, seed=12)
+    zero_and_small_A(inp)
+    g = to_cuda(inp)
+    names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
+    leaves = {k: g[k].clone().requires_grad_(True) for k in names}
+    y, last = ssm.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"],
+                                 D=leaves["D"], z=leaves["z"], delta_bias=leaves["delta_bias"],
+                                 delta_softplus=True, input_term="zoh")
+    y_ref, last_ref = ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                       delta_bias=g["delta_bias"], delta_softplus=True,
+                                       return_last_state=True, input_term="zoh")
+    assert torch.equal(y.detach(), y_ref) and torch.equal(last.detach(), last_ref)
+    rng = np.random.default_rng(13)
+    wy = torch.from_numpy(rng.standard_normal(tuple(y.shape)).astype(np.float32)).cuda()
+    wl = torch.from_numpy(rng.standard_normal(tuple(last.shape)).astype(np.float32)).cuda()
+    ((y * wy).sum() + (last * wl).sum()).backward()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], wy.double().cpu().numpy(),
+                          D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"], delta_softplus=True,
+                          dlast=wl.double().cpu().numpy(), zoh=True)
+    for k, rk in (("u", "du"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("D", "dD"),
+                  ("z", "dz"), ("delta_bias", "ddelta_bias")):
+        gt = leaves[k].grad.double().cpu().numpy()
+        r = ref[rk]
+        assert gt.shape == r.shape, (k, gt.shape, r.shape)
+        err = np.abs(gt - r).max()
+        assert err <= 1e-3 * np.abs(r).max() + 1e-6, (k, err)
 
 
 def test_autograd_wrapper_returns_the_library_gradients():
