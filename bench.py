@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the generation-step line")
-    p.add_argument("--only", choices=["step", "bwd", "conv", "zoh"], default=None,
+    p.add_argument("--only", choices=["step", "bwd", "bwd_zoh", "conv", "zoh"], default=None,
                    help="time one part alone and print its line (for profiling commands)")
     p.add_argument("--probe-only", action="store_true",
                    help="only measure the special-function unit's 2^x rate")
@@ -406,13 +406,14 @@ def time_e2e(w, inp, steps, warmup, local):
     return sec, h2d, d2h
 
 
-def time_scan_bwd(w, local, reps=5):
+def time_scan_bwd(w, local, reps=5, input_term="delta_b"):
     """Backward scan (gradients of every input from dy, forward recomputed
     inside the kernel) at the workload's shape, CUDA events on the current
     stream.  Roofline: the forward states are computed twice (checkpoint pass
     and tile recompute) and the decay once more in the adjoint pass, 3 x
     batch*dim*L*N exps; bytes: the forward inputs twice, dy and the fp32
-    gradients of the (batch, dim, L) tensors once."""
+    gradients of the (batch, dim, L) tensors once.  input_term "zoh": the
+    exact zero-order-hold term, same exps and bytes."""
     import selective_state_space_116_b300 as ssm
     from selective_state_space_116_b300.workloads import make_scan_inputs
     dev = torch.device("cuda", local)
@@ -423,7 +424,8 @@ def time_scan_bwd(w, local, reps=5):
 
     def run():
         return ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], z=g["z"],
-                                delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"])
+                                delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
+                                input_term=input_term)
     for _ in range(2):
         run()
     torch.cuda.synchronize(dev)
@@ -444,8 +446,8 @@ def time_scan_bwd(w, local, reps=5):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     t_roof = max(byts / (pk["hbm_gbs"] * 1e9),
                  exps / (EX2_PER_CLK_PER_SM * sms * pk["sm_max_mhz"] * 1e6))
-    return {"workload": w.name, "ms": sec * 1e3, "roofline_ms": t_roof * 1e3,
-            "frac": t_roof / sec, "launches": 1,
+    return {"workload": w.name, "input_term": input_term, "ms": sec * 1e3,
+            "roofline_ms": t_roof * 1e3, "frac": t_roof / sec, "launches": 1,
             "timing": f"{reps} calls, CUDA events (outputs ~1.4 GB: larger than L2)"}
 
 
@@ -672,6 +674,7 @@ def run_ours(args, world, rank, local):
     if not args.no_step and rank == 0:
         out["state_step"] = time_state_step(local)
         out["scan_bwd"] = time_scan_bwd(w, local)
+        out["scan_bwd_zoh"] = time_scan_bwd(w, local, input_term="zoh")
         out["other_workloads"] = [time_other("m130"), time_other("tiny"),
                                   time_other("dna", reps=5),
                                   time_other(args.workload, variant="conv"),
@@ -694,6 +697,7 @@ def main():
             w = WORKLOADS[args.workload]
             part = {"step": lambda: time_state_step(local),
                     "bwd": lambda: time_scan_bwd(w, local),
+                    "bwd_zoh": lambda: time_scan_bwd(w, local, input_term="zoh"),
                     "conv": lambda: time_other(args.workload, variant="conv"),
                     "zoh": lambda: time_other(args.workload, variant="zoh")}[args.only]()
             print(json.dumps({args.only: part}), flush=True)

@@ -319,8 +319,8 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
 // A = 0 it is Delta, the limit of w).
 constexpr float kZohSeries = 0.125f;
 constexpr float kZ2 = 0.34657359027997264f;    // ln 2 / 2
-constexpr float kZ3 = 0.08007374029168081f;    // (ln 2)^2 / 6
-constexpr float kZ4 = 0.013874441803734374f;   // (ln 2)^3 / 24
+constexpr float kZ3 = 0.08007550231970023f;    // (ln 2)^2 / 6
+constexpr float kZ4 = 0.013876027166205394f;   // (ln 2)^3 / 24
 
 template <bool ZOH>
 __device__ __forceinline__ float2 input_term2(float2 a, float2 e, float dt, float xs, float2 Bv,

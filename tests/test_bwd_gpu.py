@@ -98,7 +98,7 @@ def zero_and_small_A(inp):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("L", [37, 64])
 def test_bwd_exact_zero_order_hold(io, N, L):
     """ssm_scan_bwd_ex with the exact zero-order-hold input term, from an
