@@ -99,7 +99,7 @@ typedef struct ssm_dims {
     int64_t dstate;  /* N in {1, 2, 4, 8, 16}: state entries per channel */
     int64_t seqlen;  /* L >= 0: tokens */
     int32_t io;      /* ssm_io_dtype of u, delta, z, B, C, y */
-    int32_t chunk;   /* ssm_scan_fwd only; >= 0.  0: library default schedule.
+    int32_t chunk;   /* >= 0.  ssm_scan_fwd: 0: library default schedule.
                         chunk >= seqlen: a cap on the work of one CTA, in
                         tokens of a channel group: the scan then runs on at most
                         ceil(groups * seqlen / chunk) CTAs, splitting a group's
@@ -115,7 +115,17 @@ typedef struct ssm_dims {
                         the maps are composed into carry-ins, and the chunks
                         are scanned from those; outputs agree up to fp32
                         rounding order.  The default schedule takes it by
-                        itself for long sequences over few channels. */
+                        itself for long sequences over few channels.
+                        ssm_scan_bwd, ssm_scan_bwd_ex: 0 < chunk < seqlen
+                        cuts the sequence into chunks of chunk tokens
+                        (rounded up to 32) whose backward passes run side by
+                        side, each from the state before it and the adjoint
+                        after it (both composed from per-chunk maps found by
+                        walks that stop where the decay product is below
+                        2^-40); chunk >= seqlen: one chunk; 0: the library
+                        chunks long sequences (>= 8192 tokens) over few
+                        channels by itself.  Gradients agree with the
+                        unchunked pass up to fp32 rounding order. */
 } ssm_dims;
 
 /*
@@ -266,7 +276,8 @@ SSM_API int ssm_scan_fwd_workspace_size(const ssm_dims* dims, size_t* bytes);
  *   dh0            (batch, dim, dstate) fp32 gradient with respect to the
  *                  initial state, or NULL
  *   workspace      device scratch of ssm_scan_bwd_workspace_size() bytes
- *                  (the state at every 8th token), 16-byte aligned
+ *                  (the state at every 8th token; with chunks, the states
+ *                  and adjoints at the chunk boundaries), 16-byte aligned
  *   stream         cudaStream_t to enqueue on
  *
  * All gradients are fp32 whatever the I/O type.  dA, dB, dC, dD and

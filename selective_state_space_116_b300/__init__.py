@@ -19,7 +19,8 @@ import torch
 from . import _lib
 from ._lib import SSMError, ssm_dims
 
-__all__ = ["ssm_scan_fwd", "scan_status", "ssm_scan_bwd", "selective_scan", "ssm_state_step", "ssm_scan_fwd_workspace_size", "SSMError",
+__all__ = ["ssm_scan_fwd", "scan_status", "ssm_scan_bwd", "selective_scan", "ssm_state_step",
+           "ssm_scan_fwd_workspace_size", "ssm_scan_bwd_workspace_size", "SSMError",
            "library_path", "version"]
 
 _IO = {torch.float32: _lib.SSM_IO_F32, torch.bfloat16: _lib.SSM_IO_BF16}
@@ -73,6 +74,17 @@ def ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen, dtype=torch.bfloat16
     rc = _lib.load().ssm_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(out))
     if rc != 0:
         raise SSMError(rc, "ssm_scan_fwd_workspace_size")
+    return int(out.value)
+
+
+def ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, dtype=torch.bfloat16, chunk=0) -> int:
+    """Bytes of device workspace one backward scan of these sizes needs
+    (more than the checkpoints alone when the sequence is cut into chunks)."""
+    out = ctypes.c_size_t(0)
+    d = _dims(batch, dim, dstate, seqlen, _IO[dtype], chunk)
+    rc = _lib.load().ssm_scan_bwd_workspace_size(ctypes.byref(d), ctypes.byref(out))
+    if rc != 0:
+        raise SSMError(rc, "ssm_scan_bwd_workspace_size")
     return int(out.value)
 
 
@@ -278,13 +290,16 @@ def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
                  dlast_state=None, return_dh0=False, workspace=None, h0=None,
-                 input_term="delta_b"):
+                 input_term="delta_b", chunk=0):
     """Backward selective scan (CUDA tensors): the gradients of a loss with
     dLoss/dy = ``dy`` (and dLoss/dlast_state = ``dlast_state``) with respect
     to the inputs of ``ssm_scan_fwd`` run from the initial state ``h0``
     ((batch, dim, N) fp32, or None for zero) with the input term
     ``input_term`` ("delta_b" or "zoh", as for ``ssm_scan_fwd``).
-    The forward states are recomputed inside the kernel.  Returns a dict of
+    The forward states are recomputed inside the kernel.  ``chunk``: 0 for
+    the library's schedule (long sequences over few channels are cut into
+    chunks run side by side), else chunks of about that many tokens
+    (ssm_dims.chunk).  Returns a dict of
     fp32 tensors: du, ddelta (gradient of the raw delta), dz (None without
     z), dA, dB, dC, dD (None without D), ddelta_bias (None without
     delta_bias) and dh0 (None unless ``return_dh0``).
@@ -320,7 +335,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
          "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
          "dh0": torch.empty((batch, dim, N), **f32) if return_dh0 else None}
     lib = _lib.load()
-    d = _dims(batch, dim, N, L, _IO[io])
+    d = _dims(batch, dim, N, L, _IO[io], chunk)
     need = ctypes.c_size_t(0)
     rc = lib.ssm_scan_bwd_workspace_size(ctypes.byref(d), ctypes.byref(need))
     if rc != 0:

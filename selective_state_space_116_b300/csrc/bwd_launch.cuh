@@ -7,20 +7,31 @@
 namespace ssm_host {
 namespace bwd_detail {
 
-// Channels per thread: two at N = 16 (their dB, dC products summed in
-// registers before the shared-memory reduction), one for smaller states.
-template <int N> constexpr int bwd_channels_per_thread() { return N == 16 ? 2 : 1; }
-
+// With more than one chunk: the chunks' maps (one thread per channel and
+// min(N, 4) states), their composition (one thread per channel and state),
+// then every chunk at once (grid z).
 template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH>
 int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
-    constexpr int K = bwd_channels_per_thread<N>();
+    constexpr int K = ssm::bwd::channels_per_thread(N);
     using Sh = ssm::bwd::BwdShape<T, N, K>;
+    static_assert(Sh::CH == ssm::bwd::channels_per_cta(N), "channels per CTA");
+    if (p.nchunks > 1) {
+        constexpr int S = N < 4 ? N : 4;
+        const int64_t threads = p.batch * p.dim * (N / S), cells = p.batch * p.dim * N;
+        const dim3 ga((unsigned)((threads + ssm::bwd::kAggThreads - 1) / ssm::bwd::kAggThreads),
+                      (unsigned)p.nchunks);
+        ssm::bwd::scan_bwd_chunk_agg_kernel<T, N, Z, SP, ZOH><<<ga, ssm::bwd::kAggThreads, 0, st>>>(p);
+        ssm::bwd::scan_bwd_chunk_carry_kernel<N><<<(unsigned)((cells + ssm::bwd::kAggThreads - 1) /
+                                                              ssm::bwd::kAggThreads),
+                                                   ssm::bwd::kAggThreads, 0, st>>>(p);
+        if (cudaPeekAtLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    }
     auto kern = ssm::bwd::scan_bwd_kernel<T, N, K, Z, SP, VEC, ZOH>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return SSM_ERR_CUDA;
-    const dim3 grid((unsigned)((p.dim + Sh::CH - 1) / Sh::CH), (unsigned)p.batch);
+    const dim3 grid((unsigned)((p.dim + Sh::CH - 1) / Sh::CH), (unsigned)p.batch, (unsigned)p.nchunks);
     kern<<<grid, ssm::bwd::kThreads, Sh::SMEM, st>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

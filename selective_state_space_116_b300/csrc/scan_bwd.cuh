@@ -47,6 +47,20 @@
 // token)) is done once per element by the thread that stages it: each thread
 // stages EPT consecutive tokens of one channel, copied in by cp.async while
 // the tile before computes, and writes their gradients with vector stores.
+//
+// Long sequences over few channels (too few CTAs to fill the GPU) are cut
+// into chunks that run side by side (grid z).  Both recurrences are affine
+// in their carried vector ("Mamba remembers by forgetting, read closely",
+// interactiveml.org: the compose operator and its associativity; "Mamba",
+// sghael.github.io, "Training without stepping token by token"): per chunk
+// the state at its end from a zero start is F plus PF times the state at
+// its start, and the adjoint it hands to the state before it is Q plus PQ
+// times the adjoint it receives, PF = PQ = the product of its decays.
+// scan_bwd_chunk_agg_kernel finds F and Q by walks that stop where the
+// decay product passed falls below 2^-40 (forward: back from the chunk's
+// end; adjoint: on from its start), scan_bwd_chunk_carry_kernel composes
+// them across the chunks into each chunk's starting state and incoming
+// adjoint, and scan_bwd_kernel then runs every chunk from those.
 #pragma once
 
 #include "common.cuh"
@@ -56,6 +70,13 @@ namespace bwd {
 
 constexpr int kThreads = 32;    // threads per CTA (one warp: the finest split of the channels)
 constexpr int kTT = 8;          // tokens per tile
+constexpr int kChunkAlign = 32; // chunk boundaries of the chunked backward: multiples of pass 1's staging
+
+// Channels per thread: two at N = 16 (their dB, dC products summed in
+// registers before the shared-memory reduction), one for smaller states;
+// channels per CTA follow (32 / (N / min(N, 4)) slots).
+constexpr int channels_per_thread(int n) { return n == 16 ? 2 : 1; }
+constexpr int channels_per_cta(int n) { return kThreads / (n / (n < 4 ? n : 4)) * channels_per_thread(n); }
 
 struct BwdParams {
     const void* u;
@@ -79,7 +100,17 @@ struct BwdParams {
     float* dbias;        // (dim), accumulated, may be null
     float* dh0;          // (batch, dim, N), may be null
     float* ckpt;         // workspace: (batch, dim, ntiles, N)
+    // Chunked backward (nchunks > 1): CTA z takes tokens [z chunk_len,
+    // (z + 1) chunk_len), starting from the state hc[z] (z > 0; h0 for z = 0)
+    // with the adjoint xc[z] flowing in from the later chunks (z < nchunks - 1;
+    // dlast for the last chunk); only chunk 0 writes dh0.  Both are
+    // (nchunks, batch, dim, N) in the workspace.
+    float* hc;
+    float* xc;
+    float* agg;          // the chunks' maps: F, PF, Q, PQ, each (nchunks, batch, dim, N)
     int64_t batch, dim, L, ntiles;
+    int64_t chunk_len;   // a multiple of kChunkAlign, or >= L with one chunk
+    int nchunks;
 };
 
 
@@ -301,6 +332,14 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CH;
     const int64_t L = p.L;
+    // this CTA's chunk of the sequence, its initial state and incoming adjoint
+    const int cz = (int)blockIdx.z;
+    const int64_t t_lo = (int64_t)cz * p.chunk_len;
+    const int64_t t_hi = L - t_lo < p.chunk_len ? L : t_lo + p.chunk_len;
+    const int64_t chunk_off = (int64_t)cz * p.batch * p.dim * N;
+    const float* h0p = cz == 0 ? p.h0 : p.hc + chunk_off;
+    const float* dlastp = cz == p.nchunks - 1 ? p.dlast : p.xc + chunk_off;
+    float* dh0p = cz == 0 ? p.dh0 : nullptr;
     // recurrence role: channels slot + k SLOTS of the CTA, states n0 .. n0+S-1
     bool act[K];
     int64_t crow[K];                 // flat channel b * dim + d (0 when inactive)
@@ -319,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             return (ZOH && av != 0.0f) ? 1.0f / av : 0.0f;
         };
         auto g0 = [&](int i) {
-            return (act[k] && i < S && p.dlast) ? p.dlast[crow[k] * N + n0 + i] : 0.0f;
+            return (act[k] && i < S && dlastp) ? dlastp[crow[k] * N + n0 + i] : 0.0f;
         };
-        auto s0 = [&](int i) { return (act[k] && i < S && p.h0) ? p.h0[crow[k] * N + n0 + i] : 0.0f; };
+        auto s0 = [&](int i) { return (act[k] && i < S && h0p) ? h0p[crow[k] * N + n0 + i] : 0.0f; };
 #pragma unroll
         for (int pi = 0; pi < SP; pi++) {
             A2[k * SP + pi] = make_float2(a2(2 * pi), a2(2 * pi + 1));
@@ -481,15 +520,15 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             for (int i = tid; i < T1 * N; i += kThreads) bb1[i] = io<T>::to_f32(rb[i]);
         };
         const float* bb1 = reinterpret_cast<const float*>(smem + Sh::OFF1_B);
-        const int64_t ntiles1 = (L + T1 - 1) / T1;
-        if (ntiles1 > 0) load1(0);
-        for (int64_t k1 = 0; k1 < ntiles1; k1++) {
+        const int64_t k1_lo = t_lo / T1, k1_hi = (t_hi + T1 - 1) / T1;   // t_lo: a multiple of T1
+        if (k1_hi > k1_lo) load1(k1_lo * T1);
+        for (int64_t k1 = k1_lo; k1 < k1_hi; k1++) {
             const int64_t t0 = k1 * T1;
             if constexpr (VEC) cp_async_wait_all();
             __syncthreads();             // raw tile complete, previous tile's records consumed
             put1(t0);
             __syncthreads();
-            if (k1 + 1 < ntiles1) load1(t0 + T1);
+            if (k1 + 1 < k1_hi) load1(t0 + T1);
 #pragma unroll
             for (int j = 0; j < T1; j++) {
                 if (j % kTT == 0) {      // the state before each kTT-token tile
@@ -536,11 +575,12 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             }
         }
     };
-    if (p.ntiles > 0) {
-        load_tile((p.ntiles - 1) * kTT, true);
-        load_ckpt(p.ntiles - 1);
+    const int64_t kt_lo = t_lo / kTT, kt_hi = (t_hi + kTT - 1) / kTT;
+    if (kt_hi > kt_lo) {
+        load_tile((kt_hi - 1) * kTT, true);
+        load_ckpt(kt_hi - 1);
     }
-    for (int64_t kt = p.ntiles - 1; kt >= 0; kt--) {
+    for (int64_t kt = kt_hi - 1; kt >= kt_lo; kt--) {
         const int64_t t0 = kt * kTT;
         if constexpr (VEC) cp_async_wait_all();
         __syncthreads();                 // raw tile complete, the previous tile's epilogue done
@@ -549,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
 #pragma unroll
         for (int q = 0; q < KP; q++) hs[0][q] = hc[q];
         __syncthreads();
-        if (kt > 0) {                    // the tile before, in flight while this one computes
+        if (kt > kt_lo) {                // the tile before, in flight while this one computes
             load_tile(t0 - kTT, true);
             load_ckpt(kt - 1);
         }
@@ -699,8 +739,164 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         for (int i = 0; i < S; i++) {
             const float2 da = dA[k * SP + i / 2], gg = g[k * SP + i / 2];
             atomicAdd(p.dA + d * N + n0 + i, i % 2 ? da.y : da.x);
-            if (p.dh0) p.dh0[crow[k] * N + n0 + i] = i % 2 ? gg.y : gg.x;
+            if (dh0p) dh0p[crow[k] * N + n0 + i] = i % 2 ? gg.y : gg.x;
         }
+    }
+}
+
+constexpr float kWalkCut = 9.094947017729282e-13f;   // 2^-40
+constexpr int kAggThreads = 128;
+constexpr int kWalkBlock = 8;   // tokens whose inputs are loaded before they are walked
+
+// Chunked backward, step 1.  Thread: S = min(N, 4) states of one channel
+// (flat row b dim + d) in chunk blockIdx.y.  The same Delta, decay, input
+// weight and ds as scan_bwd_kernel:
+//   F  = sum_t (prod_(r > t) a_r) w_t B_t x_t   over the chunk's tokens t
+//        (walked back from its end: F += W w B x, then W *= a)
+//   Q  = sum_t (prod_(r <= t) a_r) ds_t C_t     (walked on from its start:
+//        W *= a, then Q += W ds C)
+//   PF, PQ = the W each walk ends with: the product of all the chunk's decays
+//        when it walked the whole chunk; below 2^-40 when it stopped early,
+//        where the terms left out and the product are below 2^-40 of what
+//        the carry keeps.
+template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool ZOH>
+__global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_agg_kernel(BwdParams p) {
+    constexpr int S = N < 4 ? N : 4, G = N / S;
+    const int64_t rows = p.batch * p.dim;
+    const int64_t i = (int64_t)blockIdx.x * kAggThreads + threadIdx.x;
+    if (i >= rows * G) return;
+    const int64_t row = i / G, b = row / p.dim, d = row % p.dim;
+    const int n0 = (int)(i % G) * S;
+    const int cz = (int)blockIdx.y;
+    const int64_t L = p.L;
+    const int64_t t_lo = (int64_t)cz * p.chunk_len;
+    const int64_t t_hi = L - t_lo < p.chunk_len ? L : t_lo + p.chunk_len;
+    float A2[S], IA[S];
+#pragma unroll
+    for (int j = 0; j < S; j++) {
+        const float av = p.A[d * N + n0 + j];
+        A2[j] = av * kLog2e;
+        IA[j] = (ZOH && av != 0.0f) ? 1.0f / av : 0.0f;
+    }
+    const float bias = p.bias ? p.bias[d] : 0.0f;
+    const T* u = static_cast<const T*>(p.u) + row * L;
+    const T* dl = static_cast<const T*>(p.delta) + row * L;
+    const T* z = static_cast<const T*>(p.z) + row * L;
+    const float* dy = p.dy + row * L;
+    const T* Bm = static_cast<const T*>(p.B) + b * L * N + n0;
+    const T* Cm = static_cast<const T*>(p.C) + b * L * N + n0;
+    auto delta_at = [&](int64_t t) {
+        const float v = io<T>::to_f32(dl[t]) + bias;
+        return SOFTPLUS ? softplus(v) : v;
+    };
+    auto decay = [&](float dt, int j, float& e) {
+        e = dt * A2[j];
+        return ex2(e);
+    };
+    auto below_cut = [&](const float (&W)[S]) {
+        bool all = true;
+#pragma unroll
+        for (int j = 0; j < S; j++) all = all && W[j] < kWalkCut;   // NaN keeps walking
+        return all;
+    };
+
+    // forward map: back from the chunk's end
+    float Fv[S], W[S];
+#pragma unroll
+    for (int j = 0; j < S; j++) { Fv[j] = 0.0f; W[j] = 1.0f; }
+    for (int64_t tb = t_hi - 1; tb >= t_lo; tb -= kWalkBlock) {
+        float dtv[kWalkBlock], xv[kWalkBlock], Bv[kWalkBlock][S];
+#pragma unroll
+        for (int k = 0; k < kWalkBlock; k++) {
+            const int64_t t = tb - k;
+            const bool ok = t >= t_lo;
+            dtv[k] = ok ? delta_at(t) : 0.0f;
+            xv[k] = ok ? io<T>::to_f32(u[t]) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < S; j++) Bv[k][j] = ok ? io<T>::to_f32(Bm[t * N + j]) : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kWalkBlock; k++) {
+#pragma unroll
+            for (int j = 0; j < S; j++) {
+                float e;
+                const float a = decay(dtv[k], j, e);
+                float wgt = dtv[k];
+                if constexpr (ZOH)
+                    wgt = zoh_weight(f2(a), f2(e), f2(dtv[k]), f2(IA[j])).x;
+                Fv[j] = fmaf(W[j], wgt * Bv[k][j] * xv[k], Fv[j]);
+                W[j] *= a;
+            }
+        }
+        if (below_cut(W)) break;
+    }
+    const int64_t o = ((int64_t)cz * rows + row) * N + n0;
+    float* F = p.agg;
+    float* PF = F + (int64_t)p.nchunks * rows * N;
+    float* Q = PF + (int64_t)p.nchunks * rows * N;
+    float* PQ = Q + (int64_t)p.nchunks * rows * N;
+#pragma unroll
+    for (int j = 0; j < S; j++) { F[o + j] = Fv[j]; PF[o + j] = W[j]; }
+
+    // adjoint map: on from the chunk's start
+    float Qv[S];
+#pragma unroll
+    for (int j = 0; j < S; j++) { Qv[j] = 0.0f; W[j] = 1.0f; }
+    for (int64_t tb = t_lo; tb < t_hi; tb += kWalkBlock) {
+        float dtv[kWalkBlock], dsv[kWalkBlock], Cv[kWalkBlock][S];
+#pragma unroll
+        for (int k = 0; k < kWalkBlock; k++) {
+            const int64_t t = tb + k;
+            const bool ok = t < t_hi;
+            dtv[k] = ok ? delta_at(t) : 0.0f;
+            float ds = ok ? dy[t] : 0.0f;
+            if (HAS_Z && ok) {
+                const float zv = io<T>::to_f32(z[t]);
+                ds = ds * zv * sigmoid(zv);
+            }
+            dsv[k] = ds;
+#pragma unroll
+            for (int j = 0; j < S; j++) Cv[k][j] = ok ? io<T>::to_f32(Cm[t * N + j]) : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kWalkBlock; k++) {
+#pragma unroll
+            for (int j = 0; j < S; j++) {
+                float e;
+                W[j] *= decay(dtv[k], j, e);
+                Qv[j] = fmaf(W[j], dsv[k] * Cv[k][j], Qv[j]);
+            }
+        }
+        if (below_cut(W)) break;
+    }
+#pragma unroll
+    for (int j = 0; j < S; j++) { Q[o + j] = Qv[j]; PQ[o + j] = W[j]; }
+}
+
+// Chunked backward, step 2.  Thread: one (channel, state).  The state before
+// every chunk, H[z + 1] = F[z] + PF[z] H[z] from H[0] = h0 (0 if none), and
+// the adjoint flowing into every chunk from the ones after it,
+// X[z - 1] = Q[z] + PQ[z] X[z] from X[nchunks - 1] = dlast (0 if none).
+// H[0] and X[nchunks - 1] are not stored (the kernel reads h0, dlast).
+template <int N>
+__global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_carry_kernel(BwdParams p) {
+    const int64_t cells = p.batch * p.dim * N;
+    const int64_t i = (int64_t)blockIdx.x * kAggThreads + threadIdx.x;
+    if (i >= cells) return;
+    const int nc = p.nchunks;
+    const float* F = p.agg;
+    const float* PF = F + (int64_t)nc * cells;
+    const float* Q = PF + (int64_t)nc * cells;
+    const float* PQ = Q + (int64_t)nc * cells;
+    float h = p.h0 ? p.h0[i] : 0.0f;
+    for (int c = 0; c + 1 < nc; c++) {
+        h = fmaf(PF[c * cells + i], h, F[c * cells + i]);
+        p.hc[(c + 1) * cells + i] = h;
+    }
+    float x = p.dlast ? p.dlast[i] : 0.0f;
+    for (int c = nc - 1; c > 0; c--) {
+        x = fmaf(PQ[c * cells + i], x, Q[c * cells + i]);
+        p.xc[(c - 1) * cells + i] = x;
     }
 }
 

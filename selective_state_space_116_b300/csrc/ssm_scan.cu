@@ -262,10 +262,54 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
 
 namespace {
 
-size_t bwd_workspace(const ssm_dims* d) {
-    const int64_t ntiles = (d->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT;
-    return (size_t)d->batch * d->dim * ntiles * d->dstate * sizeof(float);
+// Chunk plan and workspace of the backward scan.  dims->chunk > 0: chunks
+// of that many tokens (rounded up to a multiple of 32), one chunk when it is
+// >= seqlen.  0: a sequence of at least 8192 tokens is chunked by itself when
+// its grid would hold fewer than 640 one-warp CTAs (under half of what 148
+// SMs hold at 8 or 9 per SM), into about 4608 CTAs' worth of chunks of at
+// least 2048 tokens: several waves, so that the last one's share is small
+// (at the DNA-like shape 1 x 1024 x 2^20: 18 chunks, one wave, 35.2 ms; 20
+// chunks, a second wave of 96 CTAs, 48.3 ms; 72 chunks 34.0 ms).  Chunks
+// never exceed the 65535 of grid z.
+// Workspace: the checkpoints (batch, dim, ceil(L / 8), N), then with more
+// than one chunk six (nchunks, batch, dim, N) arrays: the states before the
+// chunks, the adjoints into them, and the maps F, PF, Q, PQ.
+struct BwdPlan {
+    int64_t chunk_len;
+    int nchunks;
+    size_t ckpt_bytes, arr_bytes, total;
+};
+
+size_t round16(int64_t v) { return (size_t)((v + 15) / 16 * 16); }
+
+BwdPlan bwd_plan(const ssm_dims* d) {
+    const int64_t L = d->seqlen, N = d->dstate, rows = d->batch * d->dim;
+    const int64_t al = ssm::bwd::kChunkAlign;
+    int64_t len = L;
+    if (d->chunk > 0 && d->chunk < L) {
+        len = ((int64_t)d->chunk + al - 1) / al * al;
+    } else if (d->chunk == 0 && L >= 8192) {
+        const int64_t cpc = ssm::bwd::channels_per_cta((int)N);
+        const int64_t ctas = d->batch * ((d->dim + cpc - 1) / cpc);
+        if (ctas < 640) {
+            const int64_t want = (4608 + ctas - 1) / ctas;
+            len = ((L + want - 1) / want + al - 1) / al * al;
+            if (len < 2048) len = 2048;
+        }
+    }
+    const int64_t cap = ((L + 65534) / 65535 + al - 1) / al * al;
+    if (len < cap) len = cap;
+    BwdPlan pl;
+    pl.nchunks = len >= L ? 1 : (int)((L + len - 1) / len);
+    pl.chunk_len = pl.nchunks == 1 ? (L > 1 ? L : 1) : len;
+    const int64_t ntiles = (L + ssm::bwd::kTT - 1) / ssm::bwd::kTT;
+    pl.ckpt_bytes = round16(rows * ntiles * N * 4);
+    pl.arr_bytes = pl.nchunks > 1 ? round16((int64_t)pl.nchunks * rows * N * 4) : 0;
+    pl.total = pl.ckpt_bytes + 6 * pl.arr_bytes;
+    return pl;
 }
+
+size_t bwd_workspace(const ssm_dims* d) { return bwd_plan(d).total; }
 
 }  // namespace
 
@@ -307,7 +351,8 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
                           static_cast<const void*>(dC), static_cast<const void*>(dD),
                           static_cast<const void*>(ddelta_bias), static_cast<const void*>(dh0)})
         if (!aligned(q, 4)) return SSM_ERR_MISALIGNED;
-    const size_t need = bwd_workspace(dims);
+    const BwdPlan pl = bwd_plan(dims);
+    const size_t need = pl.total;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return SSM_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -325,8 +370,16 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
     ssm::bwd::BwdParams p{u, delta, A, B, C, D, z && !empty ? z : nullptr, delta_bias, dy,
                           dlast_state, h0, du, ddelta, z ? dz : nullptr, dA, dB, dC,
                           D ? dD : nullptr, delta_bias ? ddelta_bias : nullptr, dh0,
-                          static_cast<float*>(workspace), dims->batch, dims->dim, dims->seqlen,
-                          (dims->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT};
+                          static_cast<float*>(workspace), nullptr, nullptr, nullptr,
+                          dims->batch, dims->dim, dims->seqlen,
+                          (dims->seqlen + ssm::bwd::kTT - 1) / ssm::bwd::kTT, pl.chunk_len,
+                          pl.nchunks};
+    if (pl.nchunks > 1) {
+        unsigned char* ws = static_cast<unsigned char*>(workspace) + pl.ckpt_bytes;
+        p.hc = reinterpret_cast<float*>(ws);
+        p.xc = reinterpret_cast<float*>(ws + pl.arr_bytes);
+        p.agg = reinterpret_cast<float*>(ws + 2 * pl.arr_bytes);
+    }
     if (empty) p.z = nullptr;
     const bool zz = p.z != nullptr, sp = delta_softplus != 0;
     if (input_term == SSM_INPUT_ZOH) {

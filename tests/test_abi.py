@@ -163,6 +163,32 @@ def test_scan_workspace_size_formula(lib, N, ch):
     assert need.value == 256 + r256(groups * 4) + r256(groups * ch * N * 4)
 
 
+def bwd_need(lib, **kw):
+    need = ctypes.c_size_t(0)
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(dims(**kw)), ctypes.byref(need)) == _lib.SSM_OK
+    return need.value
+
+
+@pytest.mark.parametrize("batch,dim,N,L,chunk,nchunks", [
+    (4, 5120, 16, 4096, 0, 1),          # Mamba-2.8B layer: a full grid, one chunk
+    (8, 1536, 16, 2048, 0, 1),          # Mamba-130M layer: below 8192 tokens
+    (1, 1024, 16, 1 << 20, 0, 72),      # DNA-like: 64 CTAs -> 4608 / 64 chunks
+    (1, 32, 4, 1 << 18, 0, 128),        # 1 CTA: chunks of the 2048-token minimum
+    (2, 40, 16, 4001, 200, 18),         # 200 -> 224 tokens per chunk
+    (2, 40, 16, 4001, 4001, 1),         # chunk >= seqlen: one chunk
+    (1, 8, 1, 1 << 31, 32, 65473),      # chunks of 32800 tokens: at most 65535 (grid z)
+])
+def test_bwd_chunk_plan(lib, batch, dim, N, L, chunk, nchunks):
+    """The backward's workspace: the checkpoints (batch, dim, ceil(L / 8), N)
+    fp32, plus six (nchunks, batch, dim, N) fp32 arrays when the sequence is
+    cut into chunks (the states before the chunks, the adjoints into them and
+    the chunks' maps), each rounded up to 16 bytes."""
+    r16 = lambda x: -(-x // 16) * 16
+    ckpt = r16(batch * dim * -(-L // 8) * N * 4)
+    arr = r16(nchunks * batch * dim * N * 4) if nchunks > 1 else 0
+    assert bwd_need(lib, batch=batch, dim=dim, dstate=N, seqlen=L, chunk=chunk) == ckpt + 6 * arr
+
+
 def test_noalloc_refuses_problems_beyond_its_buffer(lib):
     """The allocation-free scan rejects, on the host, any problem whose scratch
     would not fit its built-in buffer; bad sizes get the usual errors."""

@@ -24,7 +24,8 @@ pytestmark = pytest.mark.gpu
 NAMES = ["du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"]
 
 
-def run_both(w, seed=0, with_dlast=True, with_h0=False, zoh=False, edit=None):
+def run_both(w, seed=0, with_dlast=True, with_h0=False, zoh=False, edit=None, chunk=0,
+             channels=None):
     inp = make_scan_inputs(w, seed)
     if edit is not None:
         edit(inp)
@@ -38,14 +39,14 @@ def run_both(w, seed=0, with_dlast=True, with_h0=False, zoh=False, edit=None):
                            delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
                            dlast_state=None if dlast is None else dlast.cuda(), return_dh0=True,
                            h0=None if h0 is None else h0.cuda(),
-                           input_term="zoh" if zoh else "delta_b")
+                           input_term="zoh" if zoh else "delta_b", chunk=chunk)
     torch.cuda.synchronize()
     ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy.double().numpy(),
                           D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
                           delta_softplus=inp["delta_softplus"],
                           dlast=None if dlast is None else dlast.double().numpy(),
                           h0=None if h0 is None else h0.double().numpy(), nthreads=nthreads(),
-                          zoh=zoh)
+                          zoh=zoh, channels=channels)
     return got, ref
 
 
@@ -119,6 +120,63 @@ def test_bwd_exact_zero_order_hold_long_sequence():
                                  last_state=True, bias_range=(-1.0, 2.0))
     got, ref = run_both(w, seed=5, zoh=True)
     check(got, ref, "zoh L=2048")
+
+
+def ckpt_bytes(b, d, L, N):
+    return b * d * ((L + 7) // 8) * N * 4
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("zoh", [False, True])
+@pytest.mark.parametrize("L,chunk", [(4096, 1024), (4001, 200)])
+def test_bwd_chunked(io, N, zoh, L, chunk):
+    """The chunked backward (ssm_dims.chunk): chunks of 1024 tokens, where the
+    walks for the chunks' maps stop early for most states, and of 200 tokens
+    (rounded up to 224: walks over whole chunks) with a ragged last chunk and
+    element-wise staging (L = 4001); from h0 with dlast, either input term,
+    against the oracle."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=40, seqlen=L, dstate=N, io=io, last_state=True)
+    assert (ssm.ssm_scan_bwd_workspace_size(2, 40, N, L, w.torch_io, chunk=chunk) >
+            ckpt_bytes(2, 40, L, N))
+    got, ref = run_both(w, seed=L + N, with_h0=True, zoh=zoh, chunk=chunk)
+    check(got, ref, f"{io} N={N} zoh={zoh} L={L} chunk={chunk}")
+
+
+def test_bwd_long_sequence_takes_chunks_by_itself():
+    """A DNA-like sequence (one-hot inputs, fp32, 2^18 tokens) over 32
+    channels: the default schedule cuts it into chunks (its workspace holds
+    the chunk arrays).  Per-channel gradients of 8 sampled channels (the
+    first and last included) against the oracle; dB and dC, which sum over
+    all channels, against the unchunked backward on the GPU."""
+    w = WORKLOADS["dna"].scaled(dim=32, seqlen=1 << 18)
+    b, d, L, N = w.batch, w.dim, w.seqlen, w.dstate
+    assert ssm.ssm_scan_bwd_workspace_size(b, d, N, L, torch.float32) > ckpt_bytes(b, d, L, N)
+    assert ssm.ssm_scan_bwd_workspace_size(b, d, N, L, torch.float32, chunk=L) == ckpt_bytes(b, d, L, N)
+    chans = [0, 1, 7, 8, 15, 16, 30, 31]
+    got, ref = run_both(w, seed=3, channels=chans)
+    inp = make_scan_inputs(w, 3)
+    rng = np.random.default_rng(103)
+    dy = torch.from_numpy(rng.standard_normal((b, d, L)).astype(np.float32))
+    dlast = torch.from_numpy(rng.standard_normal((b, d, N)).astype(np.float32))
+    g = to_cuda(inp)
+    whole = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+                             delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
+                             dlast_state=dlast.cuda(), chunk=L)
+    for name in ("du", "ddelta", "dh0"):
+        gt = got[name].reshape(b * d, -1)[chans].double().cpu().numpy()
+        r = ref[name]
+        err = np.abs(gt - r)
+        assert err.max() <= 1e-3 * np.abs(r).max() + 1e-6, (name, err.max())
+        assert np.all(err <= 2e-3 * np.abs(r) + 1e-4 * np.abs(r).max() + 1e-6), name
+    for name, gname in (("dA_chan", "dA"), ("dD_chan", "dD")):
+        gt = got[gname][chans].double().cpu().numpy()
+        r = ref[name]
+        assert np.abs(gt - r).max() <= 1e-3 * np.abs(r).max() + 1e-6, gname
+    for name in ("dB", "dC"):
+        gt, r = got[name].double().cpu().numpy(), whole[name].double().cpu().numpy()
+        err = np.abs(gt - r)
+        assert err.max() <= 1e-3 * np.abs(r).max() + 1e-6, (name, err.max())
 
 
 def test_bwd_rejects_an_unknown_input_term():
