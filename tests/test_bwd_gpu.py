@@ -127,7 +127,7 @@ def ckpt_bytes(b, d, L, N):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [1, 4, 16])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("zoh", [False, True])
 @pytest.mark.parametrize("L,chunk", [(4096, 1024), (4001, 200)])
 def test_bwd_chunked(io, N, zoh, L, chunk):
