@@ -28,7 +28,8 @@
 // Work split.  A thread holds S = min(N, 4) states of K channels (the same
 // batch row); the G = N / S adjacent lanes of a "slot" hold the whole state of
 // those K channels.  A CTA of one warp covers SLOTS = 32 / G slots, i.e.
-// CH = SLOTS K channels, through the whole sequence in 8-token tiles:
+// CH = SLOTS K channels, through the whole sequence (or its chunk of it, see
+// below) in 8-token tiles, from the initial state h0 (zero if none):
 //
 //   pass 1  the forward recurrence, writing the state at the start of every
 //           8-token tile to the workspace (batch x dim x ceil(L/8) x N fp32);
