@@ -59,6 +59,8 @@ def check(got, ref, what):
         gt = gt.double().cpu().numpy()
         assert gt.shape == r.shape, (what, name, gt.shape, r.shape)
         assert np.all(np.isfinite(gt)), (what, name, "non-finite")
+        if r.size == 0:
+            continue
         err = np.abs(gt - r)
         scale = np.abs(r).max()
         bound = 1e-3 * scale + 1e-6
@@ -141,6 +143,17 @@ def test_bwd_chunked(io, N, zoh, L, chunk):
             ckpt_bytes(2, 40, L, N))
     got, ref = run_both(w, seed=L + N, with_h0=True, zoh=zoh, chunk=chunk)
     check(got, ref, f"{io} N={N} zoh={zoh} L={L} chunk={chunk}")
+
+
+@pytest.mark.parametrize("N", [1, 16])
+@pytest.mark.parametrize("L,chunk", [(33, 1), (64, 32), (100, 64), (0, 5)])
+def test_bwd_chunk_edges(N, L, chunk):
+    """Chunks at their smallest: chunk = 1 rounds up to 32, so 33 tokens make
+    a 32-token chunk and a 1-token one; two whole 32-token chunks; 64 and 36
+    tokens; an empty sequence (one chunk, dh0 = dlast)."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=40, seqlen=L, dstate=N, io="f32", last_state=True)
+    got, ref = run_both(w, seed=L + 7, with_h0=True, chunk=chunk)
+    check(got, ref, f"N={N} L={L} chunk={chunk}")
 
 
 def test_bwd_long_sequence_takes_chunks_by_itself():
