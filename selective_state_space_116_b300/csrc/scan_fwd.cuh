@@ -312,11 +312,12 @@ __device__ __forceinline__ float2 bf2_to_f2(unsigned w) {
 // Exact zero-order hold (ZOH = true): Bbar u = w B u with the weight
 // w = (exp(Delta A) - 1) / A; xs is u, dt is Delta, ia = 1 / A (0 where
 // A = 0), a = exp(Delta A) = 2^e with e = Delta A log2(e).
-// w = (a - 1) ia, except for |e| < 1/8, where a - 1 would keep only the
-// absolute accuracy of the 2^x unit (~2^-22, a relative error up to
-// 2^-22 / |Delta A|) and w = Delta (1 + Delta A / 2 + (Delta A)^2 / 6 +
-// (Delta A)^3 / 24) is used instead (truncation below 5e-7 relative; at
-// A = 0 it is Delta, the limit of w).
+// w = (a - 1) ia = a ia - ia (one fused multiply-add), except for |e| < 1/8,
+// where a - 1 would keep only the absolute accuracy of the 2^x unit
+// (~2^-22, a relative error up to 2^-22 / |Delta A|) and w = Delta (1 +
+// Delta A / 2 + (Delta A)^2 / 6 + (Delta A)^3 / 24) is used instead, in
+// Horner form in e with the coefficients times Delta, formed once per token
+// (truncation below 5e-7 relative; at A = 0 it is Delta, the limit of w).
 constexpr float kZohSeries = 0.125f;
 constexpr float kZ2 = 0.34657359027997264f;    // ln 2 / 2
 constexpr float kZ3 = 0.08007550231970023f;    // (ln 2)^2 / 6
@@ -329,11 +330,11 @@ __device__ __forceinline__ float2 input_term2(float2 a, float2 e, float dt, floa
     if constexpr (!ZOH) {
         return xb;
     } else {
-        float2 w = __fmul2_rn(__fadd2_rn(a, make_float2(-1.0f, -1.0f)), ia);
-        float2 t = __ffma2_rn(e, make_float2(kZ4, kZ4), make_float2(kZ3, kZ3));
-        t = __ffma2_rn(e, t, make_float2(kZ2, kZ2));
-        t = __ffma2_rn(e, t, make_float2(1.0f, 1.0f));
-        const float2 ws = __fmul2_rn(make_float2(dt, dt), t);
+        float2 w = __ffma2_rn(a, ia, make_float2(-ia.x, -ia.y));
+        const float d2 = dt * kZ2, d3 = dt * kZ3, d4 = dt * kZ4;
+        float2 t = __ffma2_rn(e, make_float2(d4, d4), make_float2(d3, d3));
+        t = __ffma2_rn(e, t, make_float2(d2, d2));
+        const float2 ws = __ffma2_rn(e, t, make_float2(dt, dt));
         if (fabsf(e.x) < kZohSeries) w.x = ws.x;
         if (fabsf(e.y) < kZohSeries) w.y = ws.y;
         return __fmul2_rn(w, xb);
@@ -346,8 +347,8 @@ __device__ __forceinline__ float input_term1(float a, float e, float dt, float x
     if constexpr (!ZOH) {
         return xb;
     } else {
-        float w = (a - 1.0f) * ia;
-        if (fabsf(e) < kZohSeries) w = dt * fmaf(e, fmaf(e, fmaf(e, kZ4, kZ3), kZ2), 1.0f);
+        float w = fmaf(a, ia, -ia);
+        if (fabsf(e) < kZohSeries) w = fmaf(e, fmaf(e, fmaf(e, dt * kZ4, dt * kZ3), dt * kZ2), dt);
         return w * xb;
     }
 }
