@@ -216,10 +216,11 @@ constexpr float kW1 = 0.34657359027997264f;    // ln 2 / 2
 constexpr float kW2 = 0.08007550231970023f;    // (ln 2)^2 / 6
 constexpr float kW3 = 0.013876027166205394f;   // (ln 2)^3 / 24
 __device__ __forceinline__ float2 zoh_weight(float2 a, float2 e, float2 dt, float2 ia) {
-    float2 w = __ffma2_rn(a, ia, make_float2(-ia.x, -ia.y));   // a ia - ia
-    float2 t = __ffma2_rn(e, __fmul2_rn(dt, f2(kW3)), __fmul2_rn(dt, f2(kW2)));
-    t = __ffma2_rn(e, t, __fmul2_rn(dt, f2(kW1)));
-    const float2 ws = __ffma2_rn(e, t, dt);                    // the series times Delta
+    float2 w = __fmul2_rn(__fadd2_rn(a, f2(-1.0f)), ia);
+    float2 t = __ffma2_rn(e, f2(kW3), f2(kW2));
+    t = __ffma2_rn(e, t, f2(kW1));
+    t = __ffma2_rn(e, t, f2(1.0f));
+    const float2 ws = __fmul2_rn(dt, t);
     if (fabsf(e.x) < kZohW) w.x = ws.x;
     if (fabsf(e.y) < kZohW) w.y = ws.y;
     return w;
