@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the generation-step line")
-    p.add_argument("--only", choices=["step", "bwd", "bwd_zoh", "conv", "zoh"], default=None,
+    p.add_argument("--only", choices=["step", "bwd", "bwd_zoh", "train", "conv", "zoh"], default=None,
                    help="time one part alone and print its line (for profiling commands)")
     p.add_argument("--probe-only", action="store_true",
                    help="only measure the special-function unit's 2^x rate")
@@ -457,6 +457,45 @@ def time_scan_bwd(w, local, reps=5, input_term="delta_b"):
             "timing": f"{reps} calls, CUDA events (outputs {out_gb:.1f} GB: larger than L2)"}
 
 
+def time_train_step(w, local, reps=5):
+    """One training step of the scan through the autograd wrapper
+    (selective_scan forward, then backward from a fixed upstream gradient of
+    y and last_state), as a user's training loop runs it: the library's
+    forward and backward kernels plus the wrapper's casts of the gradients
+    to the inputs' dtype.  CUDA events on the current stream."""
+    import selective_state_space_116_b300 as ssm
+    dev = torch.device("cuda", local)
+    inp = make_scan_inputs(w, seed=0)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
+    leaves = {k: g[k].clone().requires_grad_(True) for k in names if g[k] is not None}
+    gen = torch.Generator(device=dev).manual_seed(1)
+    wy = torch.randn(w.batch, w.dim, w.seqlen, device=dev, generator=gen)
+    wl = torch.randn(w.batch, w.dim, w.dstate, device=dev, generator=gen)
+
+    def step():
+        for t in leaves.values():
+            t.grad = None
+        y, last = ssm.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"],
+                                     D=leaves.get("D"), z=leaves.get("z"),
+                                     delta_bias=leaves.get("delta_bias"),
+                                     delta_softplus=g["delta_softplus"])
+        torch.autograd.backward((y, last), (wy.to(y.dtype), wl))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        step()
+    b.record()
+    torch.cuda.synchronize(dev)
+    sec = a.elapsed_time(b) / 1e3 / reps
+    elems = w.batch * w.dim * w.seqlen
+    return {"workload": w.name, "ms": sec * 1e3, "elements_per_s": elems / sec,
+            "timing": f"{reps} steps (forward + backward through selective_scan), CUDA events"}
+
+
 def time_state_step(local, graph_steps=1024, reps=5):
     """Generation: 128 x 5120 channels, N = 16, bf16 inputs, fp32 state, one token
     per launch, 1024 consecutive launches captured in one CUDA graph.  The state
@@ -682,6 +721,7 @@ def run_ours(args, world, rank, local):
         out["scan_bwd"] = time_scan_bwd(w, local)
         out["scan_bwd_zoh"] = time_scan_bwd(w, local, input_term="zoh")
         out["scan_bwd_dna"] = time_scan_bwd(WORKLOADS["dna"], local, reps=3)
+        out["train_step"] = time_train_step(w, local)
         out["other_workloads"] = [time_other("m130"), time_other("tiny"),
                                   time_other("dna", reps=5),
                                   time_other(args.workload, variant="conv"),
@@ -705,6 +745,7 @@ def main():
             part = {"step": lambda: time_state_step(local),
                     "bwd": lambda: time_scan_bwd(w, local),
                     "bwd_zoh": lambda: time_scan_bwd(w, local, input_term="zoh"),
+                    "train": lambda: time_train_step(w, local),
                     "conv": lambda: time_other(args.workload, variant="conv"),
                     "zoh": lambda: time_other(args.workload, variant="zoh")}[args.only]()
             print(json.dumps({args.only: part}), flush=True)
