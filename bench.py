@@ -470,7 +470,7 @@ def time_train_step(w, local, reps=5):
     names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
     leaves = {k: g[k].clone().requires_grad_(True) for k in names if g[k] is not None}
     gen = torch.Generator(device=dev).manual_seed(1)
-    wy = torch.randn(w.batch, w.dim, w.seqlen, device=dev, generator=gen)
+    wy = torch.randn(w.batch, w.dim, w.seqlen, device=dev, generator=gen).to(w.torch_io)
     wl = torch.randn(w.batch, w.dim, w.dstate, device=dev, generator=gen)
 
     def step():
@@ -480,7 +480,7 @@ def time_train_step(w, local, reps=5):
                                      D=leaves.get("D"), z=leaves.get("z"),
                                      delta_bias=leaves.get("delta_bias"),
                                      delta_softplus=g["delta_softplus"])
-        torch.autograd.backward((y, last), (wy.to(y.dtype), wl))
+        torch.autograd.backward((y, last), (wy, wl))
     for _ in range(2):
         step()
     torch.cuda.synchronize(dev)
