@@ -290,7 +290,7 @@ def ssm_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
                  dlast_state=None, return_dh0=False, workspace=None, h0=None,
-                 input_term="delta_b", chunk=0):
+                 input_term="delta_b", chunk=0, grad_dtype=torch.float32):
     """Backward selective scan (CUDA tensors): the gradients of a loss with
     dLoss/dy = ``dy`` (and dLoss/dlast_state = ``dlast_state``) with respect
     to the inputs of ``ssm_scan_fwd`` run from the initial state ``h0``
@@ -299,8 +299,10 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     The forward states are recomputed inside the kernel.  ``chunk``: 0 for
     the library's schedule (long sequences over few channels are cut into
     chunks run side by side), else chunks of about that many tokens
-    (ssm_dims.chunk).  Returns a dict of
-    fp32 tensors: du, ddelta (gradient of the raw delta), dz (None without
+    (ssm_dims.chunk).  ``grad_dtype``: float32, or the I/O dtype, in which
+    du, ddelta and dz are then written (the fp32 values rounded once).
+    Returns a dict of
+    tensors: du, ddelta (gradient of the raw delta), dz (None without
     z), dA, dB, dC, dD (None without D), ddelta_bias (None without
     delta_bias) and dh0 (None unless ``return_dh0``).
     """
@@ -326,9 +328,12 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     if input_term not in ("delta_b", "zoh"):
         raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
     term = _lib.SSM_INPUT_ZOH if input_term == "zoh" else _lib.SSM_INPUT_DELTA_B
+    if grad_dtype not in (torch.float32, io):
+        raise TypeError(f"grad_dtype must be float32 or the I/O dtype {io}, not {grad_dtype}")
     f32 = dict(dtype=torch.float32, device=device)
-    g = {"du": torch.empty((batch, dim, L), **f32), "ddelta": torch.empty((batch, dim, L), **f32),
-         "dz": torch.empty((batch, dim, L), **f32) if z is not None else None,
+    gt = dict(dtype=grad_dtype, device=device)
+    g = {"du": torch.empty((batch, dim, L), **gt), "ddelta": torch.empty((batch, dim, L), **gt),
+         "dz": torch.empty((batch, dim, L), **gt) if z is not None else None,
          "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, L, N), **f32),
          "dC": torch.empty((batch, L, N), **f32),
          "dD": torch.empty((dim,), **f32) if D is not None else None,
@@ -345,7 +350,8 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.ssm_scan_bwd_ex(ctypes.byref(d), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                              _ptr(D), _ptr(z), _ptr(delta_bias), 1 if delta_softplus else 0,
-                             _ptr(dy), _ptr(dlast_state), _ptr(h0), term, _ptr(g["du"]),
+                             _ptr(dy), _ptr(dlast_state), _ptr(h0), term, _IO[grad_dtype],
+                             _ptr(g["du"]),
                              _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
                              _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
                              _ptr(workspace), ws_bytes, _stream(device))
@@ -374,9 +380,10 @@ class _SelectiveScan(torch.autograd.Function):
         dy = torch.zeros_like(u, dtype=torch.float32) if dy is None else dy.float().contiguous()
         dlast = None if dlast is None else dlast.float().contiguous()
         want_dh0 = h0 is not None and ctx.needs_input_grad[9]
+        # du, ddelta, dz come out in the inputs' dtype (u, delta, z share it)
         g = ssm_scan_bwd(u, delta, A, B, C, dy, D=D, z=z, delta_bias=delta_bias,
                          delta_softplus=ctx.delta_softplus, dlast_state=dlast, h0=h0,
-                         return_dh0=want_dh0, input_term=ctx.input_term)
+                         return_dh0=want_dh0, input_term=ctx.input_term, grad_dtype=u.dtype)
         cast = lambda t, like: None if t is None else t.to(like.dtype)
         return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B),
                 cast(g["dC"], C), g["dD"] if D is not None else None,

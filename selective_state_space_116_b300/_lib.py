@@ -91,8 +91,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     lib.ssm_scan_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssm_scan_bwd_ex.restype = i32
-    lib.ssm_scan_bwd_ex.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp,
-                                    vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssm_scan_bwd_ex.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, i32,
+                                    vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssm_scan_bwd_workspace_size.restype = i32
     lib.ssm_scan_bwd_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
     lib.ssm_scan_fwd_host.restype = i32

@@ -1,6 +1,8 @@
 // Backward-scan launch and dispatch over the compile-time variants (state
-// size, gate, softplus, vector staging, input term); instantiated by bwd.cu
-// (first-order input term) and bwd_zoh.cu (exact zero-order hold).
+// size, gate, softplus, vector staging, input term, gradient type GT of du,
+// ddelta, dz); instantiated by bwd.cu and bwd_zoh.cu (first-order and exact
+// zero-order-hold input terms, fp32 gradients) and bwd_gio.cu and
+// bwd_zoh_gio.cu (the same with bf16 gradients for bf16 I/O).
 #pragma once
 #include "host_plan.h"
 
@@ -10,7 +12,7 @@ namespace bwd_detail {
 // With more than one chunk: the chunks' maps (one thread per channel and
 // min(N, 4) states), their composition (one thread per channel and state),
 // then every chunk at once (grid z).
-template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH>
+template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH, typename GT>
 int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
     constexpr int K = ssm::bwd::channels_per_thread(N);
     using Sh = ssm::bwd::BwdShape<T, N, K>;
@@ -26,7 +28,7 @@ int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
                                                    ssm::bwd::kAggThreads, 0, st>>>(p);
         if (cudaPeekAtLastError() != cudaSuccess) return SSM_ERR_CUDA;
     }
-    auto kern = ssm::bwd::scan_bwd_kernel<T, N, K, Z, SP, VEC, ZOH>;
+    auto kern = ssm::bwd::scan_bwd_kernel<T, N, K, Z, SP, VEC, ZOH, GT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
@@ -36,36 +38,36 @@ int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename T, int N, bool VEC, bool ZOH>
+template <typename T, int N, bool VEC, bool ZOH, typename GT>
 int dispatch_bwd_zs(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
-    if (z && sp) return launch_bwd<T, N, true, true, VEC, ZOH>(p, st);
-    if (z) return launch_bwd<T, N, true, false, VEC, ZOH>(p, st);
-    if (sp) return launch_bwd<T, N, false, true, VEC, ZOH>(p, st);
-    return launch_bwd<T, N, false, false, VEC, ZOH>(p, st);
+    if (z && sp) return launch_bwd<T, N, true, true, VEC, ZOH, GT>(p, st);
+    if (z) return launch_bwd<T, N, true, false, VEC, ZOH, GT>(p, st);
+    if (sp) return launch_bwd<T, N, false, true, VEC, ZOH, GT>(p, st);
+    return launch_bwd<T, N, false, false, VEC, ZOH, GT>(p, st);
 }
 
 inline bool bwd_aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
 // The vector path (asynchronous staging, 16-byte stores) needs whole tiles
 // and 16-byte aligned sequence tensors.
-template <typename T, int N, bool ZOH>
+template <typename T, int N, bool ZOH, typename GT>
 int dispatch_bwd_n(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
     const bool vec = p.L % ssm::bwd::kTT == 0 && bwd_aligned16(p.u) && bwd_aligned16(p.delta) &&
                      bwd_aligned16(p.B) && bwd_aligned16(p.C) && bwd_aligned16(p.dy) &&
                      bwd_aligned16(p.du) && bwd_aligned16(p.ddelta) &&
                      (!z || (bwd_aligned16(p.z) && bwd_aligned16(p.dz)));
-    return vec ? dispatch_bwd_zs<T, N, true, ZOH>(p, z, sp, st)
-               : dispatch_bwd_zs<T, N, false, ZOH>(p, z, sp, st);
+    return vec ? dispatch_bwd_zs<T, N, true, ZOH, GT>(p, z, sp, st)
+               : dispatch_bwd_zs<T, N, false, ZOH, GT>(p, z, sp, st);
 }
 
-template <typename T, bool ZOH>
+template <typename T, bool ZOH, typename GT = float>
 int dispatch_bwd(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
     switch (n) {
-        case 1: return dispatch_bwd_n<T, 1, ZOH>(p, z, sp, st);
-        case 2: return dispatch_bwd_n<T, 2, ZOH>(p, z, sp, st);
-        case 4: return dispatch_bwd_n<T, 4, ZOH>(p, z, sp, st);
-        case 8: return dispatch_bwd_n<T, 8, ZOH>(p, z, sp, st);
-        case 16: return dispatch_bwd_n<T, 16, ZOH>(p, z, sp, st);
+        case 1: return dispatch_bwd_n<T, 1, ZOH, GT>(p, z, sp, st);
+        case 2: return dispatch_bwd_n<T, 2, ZOH, GT>(p, z, sp, st);
+        case 4: return dispatch_bwd_n<T, 4, ZOH, GT>(p, z, sp, st);
+        case 8: return dispatch_bwd_n<T, 8, ZOH, GT>(p, z, sp, st);
+        case 16: return dispatch_bwd_n<T, 16, ZOH, GT>(p, z, sp, st);
     }
     return SSM_ERR_UNSUPPORTED_N;
 }

@@ -91,9 +91,9 @@ struct BwdParams {
     const float* dy;     // (batch, dim, L) fp32
     const float* dlast;  // (batch, dim, N) fp32, may be null
     const float* h0;     // (batch, dim, N) fp32 initial state of the forward, may be null
-    float* du;           // (batch, dim, L)
-    float* ddelta;       // (batch, dim, L)
-    float* dz;           // (batch, dim, L), null when z is null
+    void* du;            // (batch, dim, L) of the gradient type GT: fp32 or the I/O type
+    void* ddelta;        // (batch, dim, L) GT
+    void* dz;            // (batch, dim, L) GT, null when z is null
     float* dA;           // (dim, N), accumulated: zeroed by the host
     float* dB;           // (batch, L, N), accumulated
     float* dC;           // (batch, L, N), accumulated
@@ -291,25 +291,36 @@ __device__ __forceinline__ void lds_row(const unsigned char* p, float* v) {
     }
 }
 
-// E consecutive fp32 to global memory: 16-byte stores when VEC (dst aligned)
-template <int E, bool VEC>
-__device__ __forceinline__ void stg_row(float* dst, const float* v, int valid) {
+// E consecutive fp32 values to global memory as GT (fp32, or bf16 rounded to
+// nearest even): 16-byte (fp32) or 8-byte (bf16) stores of 4 values when VEC
+// (dst 16-byte aligned at the row, 4-element aligned here)
+template <typename GT, int E, bool VEC>
+__device__ __forceinline__ void stg_row(GT* dst, const float* v, int valid) {
     if constexpr (VEC && E % 4 == 0) {
 #pragma unroll
-        for (int q = 0; q < E / 4; q++)
-            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < E / 4; q++) {
+            if constexpr (sizeof(GT) == 4) {
+                reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(v[4 * q], v[4 * q + 1]);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(v[4 * q + 2], v[4 * q + 3]);
+                reinterpret_cast<uint2*>(dst)[q] = make_uint2(*reinterpret_cast<const unsigned*>(&lo),
+                                                              *reinterpret_cast<const unsigned*>(&hi));
+            }
+        }
     } else {
 #pragma unroll
         for (int e = 0; e < E; e++)
-            if (e < valid) dst[e] = v[e];
+            if (e < valid) dst[e] = io<GT>::from_f32(v[e]);
     }
 }
 
 // VEC: L % 8 == 0 and every tensor 16-byte aligned (cp.async staging, vector
 // stores); otherwise bounds-checked scalar copies.  ZOH: the exact
 // zero-order-hold input term; the records then carry x where they carry
-// Delta x for the first-order term.
-template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC, bool ZOH>
+// Delta x for the first-order term.  GT: the type du, ddelta and dz are
+// written in (fp32, or the I/O type: the same fp32 values rounded once).
+template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC, bool ZOH, typename GT = float>
 __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<T, N, K>;
     constexpr int S = Sh::S, G = Sh::G, SLOTS = Sh::SLOTS, CH = Sh::CH;
@@ -715,9 +726,9 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             if (okc) {
                 const int64_t rem = L - (t0 + sj);
                 const int valid = rem < EPT ? (int)rem : EPT;
-                stg_row<EPT, VEC>(p.du + srow + t0 + sj, dxo, valid);
-                stg_row<EPT, VEC>(p.ddelta + srow + t0 + sj, dvo, valid);
-                if constexpr (HAS_Z) stg_row<EPT, VEC>(p.dz + srow + t0 + sj, dzo, valid);
+                stg_row<GT, EPT, VEC>(static_cast<GT*>(p.du) + srow + t0 + sj, dxo, valid);
+                stg_row<GT, EPT, VEC>(static_cast<GT*>(p.ddelta) + srow + t0 + sj, dvo, valid);
+                if constexpr (HAS_Z) stg_row<GT, EPT, VEC>(static_cast<GT*>(p.dz) + srow + t0 + sj, dzo, valid);
             }
         }
     }

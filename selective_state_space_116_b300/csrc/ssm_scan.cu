@@ -262,6 +262,16 @@ int ssm_state_step(const ssm_dims* dims, float* state, const void* x, const void
 
 namespace {
 
+}  // namespace
+
+namespace ssm_host {
+// bf16 I/O with du, ddelta, dz written in bf16 (bwd_gio.cu, bwd_zoh_gio.cu).
+int bwd_bf16_gio(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
+int bwd_zoh_bf16_gio(int n, const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st);
+}  // namespace ssm_host
+
+namespace {
+
 // Chunk plan and workspace of the backward scan.  dims->chunk > 0: chunks
 // of that many tokens (rounded up to a multiple of 32), one chunk when it is
 // >= seqlen.  0: a sequence of at least 8192 tokens is chunked by itself when
@@ -327,14 +337,16 @@ int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
 int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, const float* A,
                     const void* B, const void* C, const float* D, const void* z,
                     const float* delta_bias, int delta_softplus, const float* dy,
-                    const float* dlast_state, const float* h0, int input_term, float* du,
-                    float* ddelta, float* dz, float* dA, float* dB, float* dC, float* dD,
+                    const float* dlast_state, const float* h0, int input_term, int grad_io,
+                    void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC, float* dD,
                     float* ddelta_bias, float* dh0, void* workspace, size_t workspace_bytes,
                     void* stream) {
     Sizes s;
     int rc = check_dims(dims, true, &s);
     if (rc != SSM_OK) return rc;
     if (input_term != SSM_INPUT_DELTA_B && input_term != SSM_INPUT_ZOH) return SSM_ERR_BAD_OPTION;
+    if (grad_io != SSM_IO_F32 && grad_io != dims->io) return SSM_ERR_BAD_DTYPE;
+    const bool gio = grad_io == SSM_IO_BF16;   // du, ddelta, dz in bf16
     const bool empty = dims->seqlen == 0;
     if (!A || !dA || (!empty && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)))
         return SSM_ERR_NULL_ARG;
@@ -342,11 +354,11 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
     const size_t es = io_size(dims->io);
     for (const void* q : {u, delta, B, C, z})
         if (!aligned(q, es)) return SSM_ERR_MISALIGNED;
+    for (const void* q : {du, ddelta, dz})
+        if (!aligned(q, io_size(grad_io))) return SSM_ERR_MISALIGNED;
     for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
                           static_cast<const void*>(delta_bias), static_cast<const void*>(dy),
                           static_cast<const void*>(dlast_state), static_cast<const void*>(h0),
-                          static_cast<const void*>(du),
-                          static_cast<const void*>(ddelta), static_cast<const void*>(dz),
                           static_cast<const void*>(dA), static_cast<const void*>(dB),
                           static_cast<const void*>(dC), static_cast<const void*>(dD),
                           static_cast<const void*>(ddelta_bias), static_cast<const void*>(dh0)})
@@ -383,10 +395,12 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
     if (empty) p.z = nullptr;
     const bool zz = p.z != nullptr, sp = delta_softplus != 0;
     if (input_term == SSM_INPUT_ZOH) {
-        if (dims->io == SSM_IO_BF16) return bwd_zoh_bf16((int)N, p, zz, sp, st);
+        if (dims->io == SSM_IO_BF16)
+            return gio ? bwd_zoh_bf16_gio((int)N, p, zz, sp, st) : bwd_zoh_bf16((int)N, p, zz, sp, st);
         return bwd_zoh_f32((int)N, p, zz, sp, st);
     }
-    if (dims->io == SSM_IO_BF16) return bwd_bf16((int)N, p, zz, sp, st);
+    if (dims->io == SSM_IO_BF16)
+        return gio ? bwd_bf16_gio((int)N, p, zz, sp, st) : bwd_bf16((int)N, p, zz, sp, st);
     return bwd_f32((int)N, p, zz, sp, st);
 }
 
@@ -397,8 +411,8 @@ int ssm_scan_bwd(const ssm_dims* dims, const void* u, const void* delta, const f
                  float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
                  void* workspace, size_t workspace_bytes, void* stream) {
     return ssm_scan_bwd_ex(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
-                           dlast_state, nullptr, SSM_INPUT_DELTA_B, du, ddelta, dz, dA, dB, dC, dD,
-                           ddelta_bias, dh0, workspace, workspace_bytes, stream);
+                           dlast_state, nullptr, SSM_INPUT_DELTA_B, SSM_IO_F32, du, ddelta, dz, dA,
+                           dB, dC, dD, ddelta_bias, dh0, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

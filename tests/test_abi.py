@@ -189,6 +189,18 @@ def test_bwd_chunk_plan(lib, batch, dim, N, L, chunk, nchunks):
     assert bwd_need(lib, batch=batch, dim=dim, dstate=N, seqlen=L, chunk=chunk) == ckpt + 6 * arr
 
 
+def test_bwd_ex_option_checks(lib):
+    """ssm_scan_bwd_ex rejects an unknown input term and a gradient type that
+    is neither fp32 nor the I/O type, before looking at any pointer."""
+    d = dims(io=_lib.SSM_IO_F32)
+    def bwd_ex(term, gio, d=d):
+        return lib.ssm_scan_bwd_ex(ctypes.byref(d), *P[:8], 1, P[8], None, None, term, gio,
+                                   *([None] * 9), None, 0, None)
+    assert bwd_ex(2, _lib.SSM_IO_F32) == _lib.SSM_ERR_BAD_OPTION
+    assert bwd_ex(_lib.SSM_INPUT_DELTA_B, _lib.SSM_IO_BF16) == _lib.SSM_ERR_BAD_DTYPE
+    assert bwd_ex(_lib.SSM_INPUT_DELTA_B, 7, d=dims(io=_lib.SSM_IO_BF16)) == _lib.SSM_ERR_BAD_DTYPE
+
+
 def test_noalloc_refuses_problems_beyond_its_buffer(lib):
     """The allocation-free scan rejects, on the host, any problem whose scratch
     would not fit its built-in buffer; bad sizes get the usual errors."""
