@@ -310,12 +310,13 @@ SSM_API int ssm_scan_bwd(const ssm_dims* dims,
  *               too: dw/dDelta = exp(Delta A), dw/dA = (Delta exp(Delta A) -
  *               w) / A (Delta^2 / 2 at A = 0); out of range:
  *               SSM_ERR_BAD_OPTION.
- *   grad_io     the ssm_io_dtype of du, ddelta and dz: SSM_IO_F32 (as for
- *               ssm_scan_bwd), or dims->io, which writes them in the I/O
- *               type (bf16: the fp32 values rounded to nearest even once, so
- *               that a bf16 training step needs no conversion pass);
- *               anything else: SSM_ERR_BAD_DTYPE.  du, ddelta, dz must then
- *               be aligned to that type's size.  dA, dB, dC, dD,
+ *   grad_io     the ssm_io_dtype of dy, du, ddelta and dz: SSM_IO_F32 (as
+ *               for ssm_scan_bwd), or dims->io: dy is then read in the I/O
+ *               type and du, ddelta, dz written in it (bf16: the fp32
+ *               values rounded to nearest even once), so that a bf16
+ *               training step needs no conversion pass; anything else:
+ *               SSM_ERR_BAD_DTYPE.  dy, du, ddelta, dz must be aligned to
+ *               that type's size.  dlast_state, dA, dB, dC, dD,
  *               ddelta_bias and dh0 are fp32 either way.
  * h0 = NULL, SSM_INPUT_DELTA_B and SSM_IO_F32 is ssm_scan_bwd.  The fused convolution
  * of ssm_scan_opts has no backward here.  Other arguments, workspace and
@@ -325,7 +326,7 @@ SSM_API int ssm_scan_bwd_ex(const ssm_dims* dims,
                  const void* u, const void* delta, const float* A,
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, int delta_softplus,
-                 const float* dy, const float* dlast_state, const float* h0,
+                 const void* dy, const float* dlast_state, const float* h0,
                  int input_term, int grad_io,
                  void* du, void* ddelta, void* dz, float* dA,
                  float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,

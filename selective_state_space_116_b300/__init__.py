@@ -299,8 +299,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     The forward states are recomputed inside the kernel.  ``chunk``: 0 for
     the library's schedule (long sequences over few channels are cut into
     chunks run side by side), else chunks of about that many tokens
-    (ssm_dims.chunk).  ``grad_dtype``: float32, or the I/O dtype, in which
-    du, ddelta and dz are then written (the fp32 values rounded once).
+    (ssm_dims.chunk).  ``grad_dtype``: float32, or the I/O dtype: the dtype
+    of ``dy`` and of du, ddelta and dz (written as the fp32 values rounded
+    once).
     Returns a dict of
     tensors: du, ddelta (gradient of the raw delta), dz (None without
     z), dA, dB, dC, dD (None without D), ddelta_bias (None without
@@ -322,14 +323,14 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     _check(D, "D", (dim,), torch.float32, device, optional=True)
     _check(z, "z", (batch, dim, L), io, device, optional=True)
     _check(delta_bias, "delta_bias", (dim,), torch.float32, device, optional=True)
-    _check(dy, "dy", (batch, dim, L), torch.float32, device)
+    if grad_dtype not in (torch.float32, io):
+        raise TypeError(f"grad_dtype must be float32 or the I/O dtype {io}, not {grad_dtype}")
+    _check(dy, "dy", (batch, dim, L), grad_dtype, device)
     _check(dlast_state, "dlast_state", (batch, dim, N), torch.float32, device, optional=True)
     _check(h0, "h0", (batch, dim, N), torch.float32, device, optional=True)
     if input_term not in ("delta_b", "zoh"):
         raise ValueError(f"input_term must be 'delta_b' or 'zoh', not {input_term!r}")
     term = _lib.SSM_INPUT_ZOH if input_term == "zoh" else _lib.SSM_INPUT_DELTA_B
-    if grad_dtype not in (torch.float32, io):
-        raise TypeError(f"grad_dtype must be float32 or the I/O dtype {io}, not {grad_dtype}")
     f32 = dict(dtype=torch.float32, device=device)
     gt = dict(dtype=grad_dtype, device=device)
     g = {"du": torch.empty((batch, dim, L), **gt), "ddelta": torch.empty((batch, dim, L), **gt),
@@ -377,10 +378,11 @@ class _SelectiveScan(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy, dlast):
         u, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
-        dy = torch.zeros_like(u, dtype=torch.float32) if dy is None else dy.float().contiguous()
+        dy = torch.zeros_like(u) if dy is None else dy.to(u.dtype).contiguous()
         dlast = None if dlast is None else dlast.float().contiguous()
         want_dh0 = h0 is not None and ctx.needs_input_grad[9]
-        # du, ddelta, dz come out in the inputs' dtype (u, delta, z share it)
+        # dy goes in, and du, ddelta, dz come out, in the inputs' dtype (u,
+        # delta, z and y share it)
         g = ssm_scan_bwd(u, delta, A, B, C, dy, D=D, z=z, delta_bias=delta_bias,
                          delta_softplus=ctx.delta_softplus, dlast_state=dlast, h0=h0,
                          return_dh0=want_dh0, input_term=ctx.input_term, grad_dtype=u.dtype)

@@ -22,7 +22,7 @@ int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
         const int64_t threads = p.batch * p.dim * (N / S), cells = p.batch * p.dim * N;
         const dim3 ga((unsigned)((threads + ssm::bwd::kAggThreads - 1) / ssm::bwd::kAggThreads),
                       (unsigned)p.nchunks);
-        ssm::bwd::scan_bwd_chunk_agg_kernel<T, N, Z, SP, ZOH><<<ga, ssm::bwd::kAggThreads, 0, st>>>(p);
+        ssm::bwd::scan_bwd_chunk_agg_kernel<T, N, Z, SP, ZOH, GT><<<ga, ssm::bwd::kAggThreads, 0, st>>>(p);
         ssm::bwd::scan_bwd_chunk_carry_kernel<N><<<(unsigned)((cells + ssm::bwd::kAggThreads - 1) /
                                                               ssm::bwd::kAggThreads),
                                                    ssm::bwd::kAggThreads, 0, st>>>(p);

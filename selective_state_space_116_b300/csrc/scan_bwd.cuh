@@ -88,7 +88,7 @@ struct BwdParams {
     const float* D;      // may be null
     const void* z;       // may be null
     const float* bias;   // may be null
-    const float* dy;     // (batch, dim, L) fp32
+    const void* dy;      // (batch, dim, L) of the gradient type GT
     const float* dlast;  // (batch, dim, N) fp32, may be null
     const float* h0;     // (batch, dim, N) fp32 initial state of the forward, may be null
     void* du;            // (batch, dim, L) of the gradient type GT: fp32 or the I/O type
@@ -143,7 +143,7 @@ template <typename T, int N, int K> struct BwdShape {
     static constexpr int P_ROW = kTT * 2 * N + 16;        // floats
     static constexpr int OFF_P = OFF_BC + 2 * kTT * N * 4;
     // the next tile's raw inputs: u, delta, z as [CH][kTT] of T, dy as
-    // [CH][kTT] fp32, B and C as [kTT][N] of T
+    // [CH][kTT] of fp32 or T (room for fp32), B and C as [kTT][N] of T
     static constexpr int RAW_PLANE = CH * kTT * ES;
     static constexpr int OFF_RAW = OFF_P + SLOTS * P_ROW * 4;
     static constexpr int OFF_DY = OFF_RAW + 3 * RAW_PLANE;
@@ -318,8 +318,9 @@ __device__ __forceinline__ void stg_row(GT* dst, const float* v, int valid) {
 // VEC: L % 8 == 0 and every tensor 16-byte aligned (cp.async staging, vector
 // stores); otherwise bounds-checked scalar copies.  ZOH: the exact
 // zero-order-hold input term; the records then carry x where they carry
-// Delta x for the first-order term.  GT: the type du, ddelta and dz are
-// written in (fp32, or the I/O type: the same fp32 values rounded once).
+// Delta x for the first-order term.  GT: the type of dy and of du, ddelta,
+// dz (fp32, or the I/O type: read as given, written as the fp32 values
+// rounded once).
 template <typename T, int N, int K, bool HAS_Z, bool SOFTPLUS, bool VEC, bool ZOH, typename GT = float>
 __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     using Sh = BwdShape<T, N, K>;
@@ -394,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
     const T* bB = static_cast<const T*>(p.B) + b * L * N;
     const T* bC = static_cast<const T*>(p.C) + b * L * N;
     unsigned char* raw = smem + Sh::OFF_RAW + (sc * kTT + sj) * ES;
-    float* rawdy = reinterpret_cast<float*>(smem + Sh::OFF_DY) + sc * kTT + sj;
+    unsigned char* rawdy = smem + Sh::OFF_DY + (sc * kTT + sj) * (int)sizeof(GT);
+    const GT* gdy = static_cast<const GT*>(p.dy);
 
     // Copy tile [t0, t0 + kTT)'s inputs into the raw buffers (asynchronously
     // when VEC); `full` adds z, dy and C.
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
             cp_async_bytes<EPT * ES>(raw, bu + g0, okc);
             cp_async_bytes<EPT * ES>(raw + Sh::RAW_PLANE, bdl + g0, okc);
             if (full && HAS_Z) cp_async_bytes<EPT * ES>(raw + 2 * Sh::RAW_PLANE, bz + g0, okc);
-            if (full) cp_async_bytes<EPT * 4>(rawdy, p.dy + g0, okc);
+            if (full) cp_async_bytes<EPT * (int)sizeof(GT)>(rawdy, gdy + g0, okc);
             constexpr int BCQ = kTT * N * ES / 16;   // 16-byte chunks of one tile of B
             for (int i = tid; i < (full ? 2 : 1) * BCQ; i += kThreads) {
                 const int which = i / BCQ, q = i % BCQ;
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
                 reinterpret_cast<T*>(raw + Sh::RAW_PLANE)[e] = ok ? bdl[srow + t] : io<T>::from_f32(0.0f);
                 if (full && HAS_Z)
                     reinterpret_cast<T*>(raw + 2 * Sh::RAW_PLANE)[e] = ok ? bz[srow + t] : io<T>::from_f32(0.0f);
-                if (full) rawdy[e] = ok ? p.dy[srow + t] : 0.0f;
+                if (full) reinterpret_cast<GT*>(rawdy)[e] = ok ? gdy[srow + t] : io<GT>::from_f32(0.0f);
             }
             for (int i = tid; i < (full ? 2 : 1) * kTT * N; i += kThreads) {
                 const int which = i / (kTT * N), q = i % (kTT * N);
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 12) scan_bwd_kernel(BwdParams p) {
         lds_row<T, EPT>(raw, xr);
         lds_row<T, EPT>(raw + Sh::RAW_PLANE, vr);
         if (full && HAS_Z) lds_row<T, EPT>(raw + 2 * Sh::RAW_PLANE, zr);
-        if (full) lds_row<float, EPT>(reinterpret_cast<const unsigned char*>(rawdy), dyr);
+        if (full) lds_row<GT, EPT>(rawdy, dyr);
 #pragma unroll
         for (int e = 0; e < EPT; e++) {
             const bool ok = okc && t0 + sj + e < L;
@@ -771,7 +773,7 @@ constexpr int kWalkBlock = 8;   // tokens whose inputs are loaded before they ar
 //        when it walked the whole chunk; below 2^-40 when it stopped early,
 //        where the terms left out and the product are below 2^-40 of what
 //        the carry keeps.
-template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool ZOH>
+template <typename T, int N, bool HAS_Z, bool SOFTPLUS, bool ZOH, typename GT>
 __global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_agg_kernel(BwdParams p) {
     constexpr int S = N < 4 ? N : 4, G = N / S;
     const int64_t rows = p.batch * p.dim;
@@ -794,7 +796,7 @@ __global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_agg_kernel(BwdPara
     const T* u = static_cast<const T*>(p.u) + row * L;
     const T* dl = static_cast<const T*>(p.delta) + row * L;
     const T* z = static_cast<const T*>(p.z) + row * L;
-    const float* dy = p.dy + row * L;
+    const GT* dy = static_cast<const GT*>(p.dy) + row * L;
     const T* Bm = static_cast<const T*>(p.B) + b * L * N + n0;
     const T* Cm = static_cast<const T*>(p.C) + b * L * N + n0;
     auto delta_at = [&](int64_t t) {
@@ -861,7 +863,7 @@ __global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_agg_kernel(BwdPara
             const int64_t t = tb + k;
             const bool ok = t < t_hi;
             dtv[k] = ok ? delta_at(t) : 0.0f;
-            float ds = ok ? dy[t] : 0.0f;
+            float ds = ok ? io<GT>::to_f32(dy[t]) : 0.0f;
             if (HAS_Z && ok) {
                 const float zv = io<T>::to_f32(z[t]);
                 ds = ds * zv * sigmoid(zv);

@@ -336,7 +336,7 @@ int ssm_scan_bwd_workspace_size(const ssm_dims* dims, size_t* bytes) {
 
 int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, const float* A,
                     const void* B, const void* C, const float* D, const void* z,
-                    const float* delta_bias, int delta_softplus, const float* dy,
+                    const float* delta_bias, int delta_softplus, const void* dy,
                     const float* dlast_state, const float* h0, int input_term, int grad_io,
                     void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC, float* dD,
                     float* ddelta_bias, float* dh0, void* workspace, size_t workspace_bytes,
@@ -354,10 +354,11 @@ int ssm_scan_bwd_ex(const ssm_dims* dims, const void* u, const void* delta, cons
     const size_t es = io_size(dims->io);
     for (const void* q : {u, delta, B, C, z})
         if (!aligned(q, es)) return SSM_ERR_MISALIGNED;
-    for (const void* q : {du, ddelta, dz})
+    for (const void* q : {dy, static_cast<const void*>(du), static_cast<const void*>(ddelta),
+                          static_cast<const void*>(dz)})
         if (!aligned(q, io_size(grad_io))) return SSM_ERR_MISALIGNED;
     for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D),
-                          static_cast<const void*>(delta_bias), static_cast<const void*>(dy),
+                          static_cast<const void*>(delta_bias),
                           static_cast<const void*>(dlast_state), static_cast<const void*>(h0),
                           static_cast<const void*>(dA), static_cast<const void*>(dB),
                           static_cast<const void*>(dC), static_cast<const void*>(dD),

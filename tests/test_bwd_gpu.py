@@ -195,17 +195,18 @@ def test_bwd_long_sequence_takes_chunks_by_itself():
 @pytest.mark.parametrize("zoh", [False, True])
 @pytest.mark.parametrize("L,chunk", [(64, 0), (37, 0), (4096, 1024)])
 def test_bwd_gradients_in_the_io_type(zoh, L, chunk):
-    """grad_dtype = bf16: du, ddelta, dz written in bf16 are the fp32 results
-    rounded to nearest even, bit for bit (16-byte staging at L = 64,
+    """grad_dtype = bf16: dy read in bf16 gives the fp32 path's gradients for
+    the same dy values, and du, ddelta, dz written in bf16 are those fp32
+    results rounded to nearest even, bit for bit (16-byte staging at L = 64,
     element-wise at L = 37, chunks at L = 4096); the fp32-only gradients
     agree up to the atomics' order."""
     w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=L, io="bf16", last_state=True)
     g = to_cuda(make_scan_inputs(w, seed=L))
     rng = np.random.default_rng(L)
-    dy = torch.from_numpy(rng.standard_normal((2, 70, L)).astype(np.float32)).cuda()
+    dy = torch.from_numpy(rng.standard_normal((2, 70, L)).astype(np.float32)).cuda().to(torch.bfloat16)
     kw = dict(D=g["D"], z=g["z"], delta_bias=g["delta_bias"], delta_softplus=True,
               input_term="zoh" if zoh else "delta_b", chunk=chunk)
-    full = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, **kw)
+    full = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.float(), **kw)
     half = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, grad_dtype=torch.bfloat16, **kw)
     for name in ("du", "ddelta", "dz"):
         assert half[name].dtype == torch.bfloat16
@@ -216,6 +217,9 @@ def test_bwd_gradients_in_the_io_type(zoh, L, chunk):
         assert (half[name] - r).abs().max() <= 1e-5 * r.abs().max() + 1e-6, name
     with pytest.raises(TypeError):
         ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, grad_dtype=torch.float16, **kw)
+    with pytest.raises(TypeError):   # dy must have the gradient dtype
+        ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.float(),
+                         grad_dtype=torch.bfloat16, **kw)
 
 
 def test_bwd_rejects_an_unknown_input_term():
