@@ -358,6 +358,33 @@ def test_autograd_wrapper_exact_zero_order_hold():
         assert err <= 1e-3 * np.abs(r).max() + 1e-6, (k, err)
 
 
+def test_autograd_wrapper_bf16_gradients():
+    """selective_scan on bf16 inputs: the backward takes the bf16 upstream
+    gradient as it is and returns du, ddelta, dz in bf16, equal bit for bit
+    to ssm_scan_bwd's fp32 gradients for the same upstream values rounded
+    once; dA, dB, dC, dD, ddelta_bias as ssm_scan_bwd gives them (cast to
+    the inputs' dtype), up to the atomics' order."""
+    w = WORKLOADS["m130"].scaled(batch=2, dim=70, seqlen=64, io="bf16", last_state=True)
+    g = to_cuda(make_scan_inputs(w, seed=21))
+    names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
+    leaves = {k: g[k].clone().requires_grad_(True) for k in names}
+    y, last = ssm.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"],
+                                 D=leaves["D"], z=leaves["z"], delta_bias=leaves["delta_bias"],
+                                 delta_softplus=True)
+    rng = np.random.default_rng(22)
+    wy = torch.from_numpy(rng.standard_normal(tuple(y.shape)).astype(np.float32)).cuda().to(torch.bfloat16)
+    wl = torch.from_numpy(rng.standard_normal(tuple(last.shape)).astype(np.float32)).cuda()
+    torch.autograd.backward((y, last), (wy, wl))
+    ref = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], wy.float(), D=g["D"], z=g["z"],
+                           delta_bias=g["delta_bias"], delta_softplus=True, dlast_state=wl)
+    for k, rk in (("u", "du"), ("delta", "ddelta"), ("z", "dz")):
+        assert leaves[k].grad.dtype == torch.bfloat16, k
+        assert torch.equal(leaves[k].grad, ref[rk].to(torch.bfloat16)), k
+    for k, rk in (("A", "dA"), ("B", "dB"), ("C", "dC"), ("D", "dD"), ("delta_bias", "ddelta_bias")):
+        got, r = leaves[k].grad.float(), ref[rk].to(leaves[k].dtype).float()
+        assert (got - r).abs().max() <= 1e-2 * r.abs().max() + 1e-6, k
+
+
 def test_autograd_wrapper_returns_the_library_gradients():
     """selective_scan under torch.autograd: the forward equals ssm_scan_fwd
     bit for bit and the gradients equal ssm_scan_bwd's for the same upstream
