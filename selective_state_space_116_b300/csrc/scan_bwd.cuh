@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kAggThreads) scan_bwd_chunk_agg_kernel(BwdPara
     const float bias = p.bias ? p.bias[d] : 0.0f;
     const T* u = static_cast<const T*>(p.u) + row * L;
     const T* dl = static_cast<const T*>(p.delta) + row * L;
-    const T* z = static_cast<const T*>(p.z) + row * L;
+    const T* z = HAS_Z ? static_cast<const T*>(p.z) + row * L : nullptr;
     const GT* dy = static_cast<const GT*>(p.dy) + row * L;
     const T* Bm = static_cast<const T*>(p.B) + b * L * N + n0;
     const T* Cm = static_cast<const T*>(p.C) + b * L * N + n0;
