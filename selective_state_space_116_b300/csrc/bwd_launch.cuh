@@ -12,11 +12,10 @@ namespace bwd_detail {
 // With more than one chunk: the chunks' maps (one thread per channel and
 // min(N, 4) states), their composition (one thread per channel and state),
 // then every chunk at once (grid z).
-template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH, typename GT>
+template <typename T, int N, bool Z, bool SP, bool VEC, bool ZOH, typename GT, int K>
 int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
-    constexpr int K = ssm::bwd::channels_per_thread(N);
     using Sh = ssm::bwd::BwdShape<T, N, K>;
-    static_assert(Sh::CH == ssm::bwd::channels_per_cta(N), "channels per CTA");
+    static_assert(Sh::CH == ssm::bwd::channels_per_cta(N, K), "channels per CTA");
     if (p.nchunks > 1) {
         constexpr int S = N < 4 ? N : 4;
         const int64_t threads = p.batch * p.dim * (N / S), cells = p.batch * p.dim * N;
@@ -38,12 +37,22 @@ int launch_bwd(const ssm::bwd::BwdParams& p, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename T, int N, bool VEC, bool ZOH, typename GT>
+template <typename T, int N, bool VEC, bool ZOH, typename GT, int K>
 int dispatch_bwd_zs(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
-    if (z && sp) return launch_bwd<T, N, true, true, VEC, ZOH, GT>(p, st);
-    if (z) return launch_bwd<T, N, true, false, VEC, ZOH, GT>(p, st);
-    if (sp) return launch_bwd<T, N, false, true, VEC, ZOH, GT>(p, st);
-    return launch_bwd<T, N, false, false, VEC, ZOH, GT>(p, st);
+    if (z && sp) return launch_bwd<T, N, true, true, VEC, ZOH, GT, K>(p, st);
+    if (z) return launch_bwd<T, N, true, false, VEC, ZOH, GT, K>(p, st);
+    if (sp) return launch_bwd<T, N, false, true, VEC, ZOH, GT, K>(p, st);
+    return launch_bwd<T, N, false, false, VEC, ZOH, GT, K>(p, st);
+}
+
+// two channels per thread only at N = 16 on a wide enough grid
+template <typename T, int N, bool VEC, bool ZOH, typename GT>
+int dispatch_bwd_k(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t st) {
+    if constexpr (N == 16) {
+        if (ssm::bwd::channels_per_thread(N, p.batch, p.dim, p.L) == 2)
+            return dispatch_bwd_zs<T, N, VEC, ZOH, GT, 2>(p, z, sp, st);
+    }
+    return dispatch_bwd_zs<T, N, VEC, ZOH, GT, 1>(p, z, sp, st);
 }
 
 inline bool bwd_aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
@@ -56,8 +65,8 @@ int dispatch_bwd_n(const ssm::bwd::BwdParams& p, bool z, bool sp, cudaStream_t s
                      bwd_aligned16(p.B) && bwd_aligned16(p.C) && bwd_aligned16(p.dy) &&
                      bwd_aligned16(p.du) && bwd_aligned16(p.ddelta) &&
                      (!z || (bwd_aligned16(p.z) && bwd_aligned16(p.dz)));
-    return vec ? dispatch_bwd_zs<T, N, true, ZOH, GT>(p, z, sp, st)
-               : dispatch_bwd_zs<T, N, false, ZOH, GT>(p, z, sp, st);
+    return vec ? dispatch_bwd_k<T, N, true, ZOH, GT>(p, z, sp, st)
+               : dispatch_bwd_k<T, N, false, ZOH, GT>(p, z, sp, st);
 }
 
 template <typename T, bool ZOH, typename GT = float>

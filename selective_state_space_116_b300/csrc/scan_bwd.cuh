@@ -74,10 +74,20 @@ constexpr int kTT = 8;          // tokens per tile
 constexpr int kChunkAlign = 32; // chunk boundaries of the chunked backward: multiples of pass 1's staging
 
 // Channels per thread: two at N = 16 (their dB, dC products summed in
-// registers before the shared-memory reduction), one for smaller states;
-// channels per CTA follow (32 / (N / min(N, 4)) slots).
-constexpr int channels_per_thread(int n) { return n == 16 ? 2 : 1; }
-constexpr int channels_per_cta(int n) { return kThreads / (n / (n < 4 ? n : 4)) * channels_per_thread(n); }
+// registers before the shared-memory reduction) when the grid of such CTAs
+// holds at least kWideGrid of them, or when the sequence is long enough to
+// be cut into chunks (8192 tokens) that make up the CTAs; one otherwise,
+// and for smaller states, so that a small problem gets twice the CTAs
+// (which also need less shared memory: 12 fit on an SM instead of 9; the
+// Mamba-130M layer shape 1.06 -> 0.93 ms; at the DNA-like shape, chunked,
+// two channels per thread stay faster, 32.7 against 35.9 ms).  Channels per
+// CTA follow (32 / (N / min(N, 4)) slots, times the channels per thread).
+constexpr int64_t kWideGrid = 1024;
+constexpr int64_t kChunkedSeq = 8192;
+constexpr int channels_per_thread(int n, int64_t batch, int64_t dim, int64_t L) {
+    return n == 16 && (batch * ((dim + 15) / 16) >= kWideGrid || L >= kChunkedSeq) ? 2 : 1;
+}
+constexpr int channels_per_cta(int n, int k) { return kThreads / (n / (n < 4 ? n : 4)) * k; }
 
 struct BwdParams {
     const void* u;

@@ -275,12 +275,12 @@ namespace {
 // Chunk plan and workspace of the backward scan.  dims->chunk > 0: chunks
 // of that many tokens (rounded up to a multiple of 32), one chunk when it is
 // >= seqlen.  0: a sequence of at least 8192 tokens is chunked by itself when
-// its grid would hold fewer than 640 one-warp CTAs (under half of what 148
-// SMs hold at 8 or 9 per SM), into about 4608 CTAs' worth of chunks of at
-// least 2048 tokens: several waves, so that the last one's share is small
-// (at the DNA-like shape 1 x 1024 x 2^20: 18 chunks, one wave, 35.2 ms; 20
-// chunks, a second wave of 96 CTAs, 48.3 ms; 72 chunks 34.0 ms).  Chunks
-// never exceed the 65535 of grid z.
+// its grid would hold fewer than 640 one-warp CTAs (about half of what 148
+// SMs hold), into about 4608 CTAs' worth of chunks of at least 2048 tokens:
+// several waves, so that the last one's share is small (at the DNA-like
+// shape 1 x 1024 x 2^20 with two channels per thread: 18 chunks, one wave,
+// 35.2 ms; 20 chunks, a second wave of 96 CTAs, 48.3 ms; 72 chunks 34.0 ms).
+// Chunks never exceed the 65535 of grid z.
 // Workspace: the checkpoints (batch, dim, ceil(L / 8), N), then with more
 // than one chunk six (nchunks, batch, dim, N) arrays: the states before the
 // chunks, the adjoints into them, and the maps F, PF, Q, PQ.
@@ -298,8 +298,9 @@ BwdPlan bwd_plan(const ssm_dims* d) {
     int64_t len = L;
     if (d->chunk > 0 && d->chunk < L) {
         len = ((int64_t)d->chunk + al - 1) / al * al;
-    } else if (d->chunk == 0 && L >= 8192) {
-        const int64_t cpc = ssm::bwd::channels_per_cta((int)N);
+    } else if (d->chunk == 0 && L >= ssm::bwd::kChunkedSeq) {
+        const int64_t cpc = ssm::bwd::channels_per_cta(
+            (int)N, ssm::bwd::channels_per_thread((int)N, d->batch, d->dim, L));
         const int64_t ctas = d->batch * ((d->dim + cpc - 1) / cpc);
         if (ctas < 640) {
             const int64_t want = (4608 + ctas - 1) / ctas;

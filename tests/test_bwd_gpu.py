@@ -81,6 +81,18 @@ def test_bwd_state_sizes(io, N):
     check(got, ref, f"{io} N={N}")
 
 
+@pytest.mark.parametrize("zoh", [False, True])
+@pytest.mark.parametrize("L", [40, 64])
+def test_bwd_two_channels_per_thread(zoh, L):
+    """At N = 16 a grid of at least 1024 two-channel CTAs takes the kernel
+    with two channels per thread (smaller grids take one): 4 x 4096
+    channels, whole (L = 64) and ragged (L = 40) tiles, from h0, every
+    gradient (dB and dC summed over all channels) against the oracle."""
+    w = WORKLOADS["m130"].scaled(batch=4, dim=4096, seqlen=L, dstate=16, io="bf16", last_state=True)
+    got, ref = run_both(w, seed=L + 3, with_h0=True, zoh=zoh)
+    check(got, ref, f"K=2 L={L} zoh={zoh}")
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("L", [37, 64])
 def test_bwd_from_an_initial_state(io, L):
